@@ -1,0 +1,231 @@
+/*
+ * fd.h - C ABI of libfd: split-KV grouped-query flash decode over a paged KV
+ * cache, for NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes. For every request b, query token t < Tq and
+ * query head h, softmax attention of q[b, t, h, :] over the first
+ * L_b - (Tq - 1) + t keys of request b, where L_b = cache_seqlens[b] and key j
+ * lives in cache page page_table[b, j / P] at slot j % P, KV head h / G
+ * (G = Hq / Hkv). This is the decode attention of the kernels listed in
+ * "feat(autotune): separate general and decode attention warmup" (LightLLM
+ * PR 1549), section "Covered decode kernels": GQA flash decode stage 1, the
+ * stage-2 merge, INT8 and INT4 KV variants, MTP attention with several query
+ * tokens per request, and the num_splits knob of FA3 KV-cache decode.
+ * Stage 1 computes, per (request, KV head, KV split), a partial output and its
+ * log-sum-exp; stage 2 merges the splits by LSE. Split boundaries and
+ * per-request metadata are derived on the device from cache_seqlens, so a call
+ * reads no device memory on the host, never synchronises, never allocates and
+ * can be captured in a CUDA graph (sglang PR 29843 summary, sections
+ * "motivation" and "implementation": graph-replayed metadata built from
+ * cache_seqlens / page_table with no .item() call).
+ *
+ * Conventions shared by every entry point:
+ *  - Every function returns an fd_status. None aborts, prints or exits.
+ *    fd_last_error() returns a thread-local message for the last failure.
+ *  - Pointers inside fd_tensor are device pointers unless stated otherwise;
+ *    the caller owns every tensor. The library never frees caller memory.
+ *  - Work is enqueued on the given stream only (NULL = legacy default stream).
+ */
+#ifndef FD_H_
+#define FD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(FD_BUILDING_LIBRARY) && defined(__GNUC__)
+#define FD_API __attribute__((visibility("default")))
+#else
+#define FD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *fd_stream_t;
+
+typedef enum fd_status {
+  FD_OK = 0,
+  FD_ERR_INVALID_ARG = 1,    /* a descriptor or argument is malformed or inconsistent */
+  FD_ERR_UNSUPPORTED = 2,    /* well formed but outside what the kernels implement */
+  FD_ERR_WORKSPACE = 3,      /* the plan's workspace is too small or absent (host-only plan) */
+  FD_ERR_CAPTURING = 4,      /* refused because the stream is capturing a CUDA graph */
+  FD_ERR_CUDA = 5,           /* a CUDA runtime / driver call failed (message has the code) */
+  FD_ERR_DEVICE_STATUS = 6,  /* a kernel recorded a problem in the plan's status word */
+  FD_ERR_TIMEOUT = 7,        /* a bounded device-side wait gave up */
+  FD_ERR_NO_PLAN = 8,        /* no current plan on this thread (see fd_set_plan) */
+  FD_ERR_IO = 9              /* autotune cache file could not be read or written */
+} fd_status;
+
+typedef enum fd_dtype {
+  FD_BF16 = 0,
+  FD_FP32 = 1,
+  FD_INT8 = 2,
+  FD_INT4X2 = 3,  /* two signed 4-bit codes per byte, even channel in the low nibble */
+  FD_INT32 = 4
+} fd_dtype;
+
+/* Bits of the plan's device status word (see fd_read_device_status). */
+#define FD_DEVSTAT_BAD_PAGE 1u         /* a visible key's page id was outside [0, num_pages) */
+#define FD_DEVSTAT_SEQLEN_OVERFLOW 2u  /* cache_seqlens[b] > page_table width * page size, or < 0 */
+#define FD_DEVSTAT_WAIT_TIMEOUT 4u     /* a pipeline wait gave up; results of that call are garbage */
+
+/*
+ * A strided tensor descriptor. shape/stride have ndim valid entries (ndim <=
+ * 5), outermost first; strides are in elements (for FD_INT4X2, in bytes).
+ * data is a device pointer (host pointer only where an entry point says so).
+ */
+typedef struct fd_tensor {
+  void *data;
+  int32_t dtype; /* an fd_dtype */
+  int32_t ndim;
+  int64_t shape[5];
+  int64_t stride[5];
+} fd_tensor;
+
+/* Opaque plan: problem geometry, device workspace, status word and the
+ * num_splits autotune table. */
+typedef struct fd_plan fd_plan;
+
+/*
+ * fd_plan_create - build a plan for one decode geometry, OUTSIDE graph capture.
+ *
+ *  device          CUDA device ordinal; -1 makes a host-only plan that holds a
+ *                  tuning table and validates descriptors but cannot decode
+ *                  (fd_decode_paged then returns FD_ERR_WORKSPACE).
+ *  max_batch       largest B any call will use (>= 1).
+ *  max_q_per_req   largest Tq (query tokens per request, MTP) any call will use.
+ *  num_q_heads     Hq; num_kv_heads Hkv; Hq % Hkv == 0.
+ *  head_dim        D, 64 or 128.
+ *  page_size       P, a power of two in [8, 256] (a page's rows are moved as
+ *                  whole 8-row TMA swizzle atoms).
+ *  kv_dtype        FD_BF16, FD_INT8 or FD_INT4X2.
+ *  max_splits      largest num_splits any call will use, 1..64.
+ *  softmax_scale   > 0, or 0 for 1/sqrt(D).
+ *  plan            out: the new plan.
+ *
+ * Allocates the split workspace (fp32 partial outputs and LSE, sized for
+ * max_batch * max_q_per_req * Hq * max_splits rows of D) and a status word on
+ * the device. Reads FD_AUTOTUNE_CACHE_DIR for the tuning cache directory.
+ */
+FD_API fd_status fd_plan_create(int device, int max_batch, int max_q_per_req, int num_q_heads,
+                         int num_kv_heads, int head_dim, int page_size, fd_dtype kv_dtype,
+                         int max_splits, float softmax_scale, fd_plan **plan);
+
+/* fd_plan_destroy - free a plan and its device memory (NULL is a no-op).
+ * The caller must make sure no enqueued call still uses it. */
+FD_API fd_status fd_plan_destroy(fd_plan *plan);
+
+/* fd_set_plan - make plan the current plan of the calling thread (NULL
+ * clears it). fd_decode_paged uses the current plan. */
+FD_API fd_status fd_set_plan(fd_plan *plan);
+
+/* fd_get_plan - the calling thread's current plan, or NULL. */
+FD_API fd_plan *fd_get_plan(void);
+
+/*
+ * fd_decode_paged - one decode attention call (stage 1 and, when
+ * num_splits > 1, stage 2), enqueued on stream.
+ *
+ *  q             bf16 [B, Tq, Hq, D], innermost stride 1.
+ *  k_cache       [num_pages, P, Hkv, D] bf16 or int8, or [num_pages, P, Hkv, D/2]
+ *                int4x2; innermost stride 1, every other stride a multiple of
+ *                16 bytes, base 16-byte aligned (the cache is read with TMA).
+ *  v_cache       same dtype, shape and strides as k_cache.
+ *  kv_scales     fp32 [2, num_pages, P, Hkv, n_g] (index 0 = K scales, 1 = V
+ *                scales; n_g = 1 for int8, D/32 for int4; innermost stride 1,
+ *                n_g * 4 bytes aligned). NULL for bf16. The scale of a cache
+ *                row sits at the row's (page, slot, head) index:
+ *                value = code * scale[group of the channel].
+ *  page_table    int32 [B, W], innermost stride 1. Entries past a request's
+ *                last page (the -1 sentinel) are never read.
+ *  cache_seqlens int32 [B] (device): L_b, the keys request b owns. Must be
+ *                <= W * P; rows with L_b - (Tq-1) + t <= 0 keys get out = 0,
+ *                lse = -inf.
+ *  q_per_req     Tq, equal to q.shape[1] and <= the plan's max_q_per_req.
+ *                Query token t sees keys [0, L_b - (Tq-1) + t) (causal MTP).
+ *  num_splits    1..plan max_splits, or 0 to use the autotuned value for
+ *                (B, bucket of the max-seqlen hint) (see fd_set_max_seqlen_hint).
+ *                Splits are equal page-aligned chunks of each request's keys;
+ *                results do not depend on it beyond rounding.
+ *  out           [B, Tq, Hq, D] bf16 (round to nearest even) or fp32,
+ *                innermost stride 1.
+ *  lse           fp32 [B, Tq, Hq] natural-log LSE of the scaled scores, or NULL.
+ *  stream        stream to enqueue on.
+ *
+ * Kernels record bad metadata (page id out of range, L_b over capacity) in
+ * the plan's status word instead of faulting; read it with
+ * fd_read_device_status. Calls on one plan that overlap on the device race on
+ * its workspace: serialise them on one stream.
+ */
+FD_API fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cache, const fd_tensor *v_cache,
+                          const fd_tensor *kv_scales, const fd_tensor *page_table,
+                          const fd_tensor *cache_seqlens, int q_per_req, int num_splits,
+                          fd_tensor *out, fd_tensor *lse, fd_stream_t stream);
+
+/* fd_set_max_seqlen_hint - host-known upper bound of cache_seqlens for the
+ * next calls with num_splits = 0; picks the KV-length bucket of the tuning
+ * table without reading device memory ("feat(autotune): ...", section
+ * "Covered decode kernels": run keys bucketed by KV length while execution
+ * uses the real length). 0 clears the hint (the longest bucket is used). */
+FD_API fd_status fd_set_max_seqlen_hint(fd_plan *plan, int max_seqlen);
+
+/*
+ * fd_autotune - pick num_splits per (batch, KV-length bucket) by timing
+ * (same page, sections "Changes" and "Covered decode kernels": decode
+ * attention tuned at startup on representative inputs, outside graph capture,
+ * at a representative length, default 32768; configs persisted and reused).
+ *
+ *  batch_sizes / n_batch  batch sizes to tune (each 1..max_batch).
+ *  min_bucket, max_bucket KV-length buckets: powers of two from min_bucket to
+ *                         max_bucket (0, 0 = 1024 .. FD_AUTOTUNE_SEQ_LEN or 32768).
+ *  stream                 stream for the timing launches.
+ *
+ * Candidates are num_splits in {1, 2, 4, ..., max_splits}. For each key not
+ * already in the table (loaded from the cache directory), synthetic inputs of
+ * the bucket length are timed with CUDA events after an L2 flush; the fastest
+ * is stored and the table saved. Refuses with FD_ERR_CAPTURING while the
+ * stream is capturing. FD_FORCE_AUTOTUNE=1 ignores cached entries once.
+ * Allocates temporary device buffers (freed before return).
+ */
+FD_API fd_status fd_autotune(fd_plan *plan, const int *batch_sizes, int n_batch, int min_bucket,
+                      int max_bucket, fd_stream_t stream);
+
+/* fd_query_splits - the num_splits a num_splits = 0 call would use for
+ * (batch, max_seqlen): the tuned entry of the nearest tuned batch and the
+ * bucket of max_seqlen, else the built-in heuristic. Host only. */
+FD_API fd_status fd_query_splits(fd_plan *plan, int batch, int max_seqlen, int *num_splits);
+
+/* Timer hook for fd_autotune: returns the time of one call with num_splits
+ * for (batch, bucket), in any unit. NULL restores CUDA-event timing. With a
+ * hook installed fd_autotune launches nothing, so its table logic can be
+ * exercised on a host-only plan. */
+typedef double (*fd_timer_fn)(void *user, int batch, int bucket, int num_splits);
+FD_API fd_status fd_autotune_set_timer(fd_plan *plan, fd_timer_fn fn, void *user);
+
+/* fd_autotune_set_cache_dir - directory of the persisted tuning table (NULL
+ * or "" disables persistence). Default: $FD_AUTOTUNE_CACHE_DIR if set. */
+FD_API fd_status fd_autotune_set_cache_dir(fd_plan *plan, const char *dir);
+
+/* fd_autotune_stats - number of (batch, bucket) searches run and cache hits
+ * served by fd_autotune on this plan. */
+FD_API fd_status fd_autotune_stats(fd_plan *plan, int *searches, int *cache_hits);
+
+/* fd_read_device_status - copy the plan's status word (FD_DEVSTAT_* bits) to
+ * *code and clear it. Synchronises the plan's device; not for use inside
+ * graph capture. Returns FD_ERR_DEVICE_STATUS when any bit was set. */
+FD_API fd_status fd_read_device_status(fd_plan *plan, int *code);
+
+/* fd_plan_workspace_bytes - device bytes the plan's split workspace holds. */
+FD_API fd_status fd_plan_workspace_bytes(fd_plan *plan, size_t *bytes);
+
+/* Static strings; never NULL. */
+FD_API const char *fd_status_string(fd_status status);
+FD_API const char *fd_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FD_H_ */

@@ -1,0 +1,241 @@
+"""Split-KV paged GQA flash decode for GB300: Python binding of libfd.
+
+A thin ctypes layer over the C ABI declared in ``include/fd.h``: every function
+here has the name of the C entry point it calls and only marshals arguments
+(torch tensors become ``fd_tensor`` descriptors of their device pointer, dtype,
+shape and strides; the stream defaults to torch's current stream). All work
+runs in the CUDA library; there is no fallback. If ``libfd.so`` has not been
+built, every call raises ``RuntimeError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence, Tuple
+
+__all__ = [
+    "FdError", "load_library", "fd_plan_create", "fd_plan_destroy", "fd_set_plan", "fd_get_plan",
+    "fd_decode_paged", "fd_set_max_seqlen_hint", "fd_autotune", "fd_query_splits",
+    "fd_autotune_set_timer", "fd_autotune_set_cache_dir", "fd_autotune_stats",
+    "fd_read_device_status", "fd_plan_workspace_bytes", "fd_status_string", "fd_last_error",
+    "FD_OK", "FD_ERR_INVALID_ARG", "FD_ERR_UNSUPPORTED", "FD_ERR_WORKSPACE", "FD_ERR_CAPTURING",
+    "FD_ERR_CUDA", "FD_ERR_DEVICE_STATUS", "FD_ERR_TIMEOUT", "FD_ERR_NO_PLAN", "FD_ERR_IO",
+    "FD_BF16", "FD_FP32", "FD_INT8", "FD_INT4X2", "FD_INT32",
+    "FD_DEVSTAT_BAD_PAGE", "FD_DEVSTAT_SEQLEN_OVERFLOW", "FD_DEVSTAT_WAIT_TIMEOUT",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfd.so")
+
+(FD_OK, FD_ERR_INVALID_ARG, FD_ERR_UNSUPPORTED, FD_ERR_WORKSPACE, FD_ERR_CAPTURING, FD_ERR_CUDA,
+ FD_ERR_DEVICE_STATUS, FD_ERR_TIMEOUT, FD_ERR_NO_PLAN, FD_ERR_IO) = range(10)
+FD_BF16, FD_FP32, FD_INT8, FD_INT4X2, FD_INT32 = range(5)
+FD_DEVSTAT_BAD_PAGE, FD_DEVSTAT_SEQLEN_OVERFLOW, FD_DEVSTAT_WAIT_TIMEOUT = 1, 2, 4
+
+_KV_NAMES = {"bf16": FD_BF16, "int8": FD_INT8, "int4": FD_INT4X2}
+
+
+class FdTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 5), ("stride", ctypes.c_int64 * 5)]
+
+
+TIMER_FN = ctypes.CFUNCTYPE(ctypes.c_double, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int)
+
+
+class FdError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_status_name(status)}: {message}")
+        self.status = status
+
+
+def _status_name(s: int) -> str:
+    names = ["FD_OK", "FD_ERR_INVALID_ARG", "FD_ERR_UNSUPPORTED", "FD_ERR_WORKSPACE", "FD_ERR_CAPTURING",
+             "FD_ERR_CUDA", "FD_ERR_DEVICE_STATUS", "FD_ERR_TIMEOUT", "FD_ERR_NO_PLAN", "FD_ERR_IO"]
+    return names[s] if 0 <= s < len(names) else f"status {s}"
+
+
+_LIB = None
+
+
+def load_library(path: Optional[str] = None):
+    """Load libfd.so (once) and declare its signatures."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(p)
+    P, T, I, F = ctypes.c_void_p, ctypes.POINTER(FdTensor), ctypes.c_int, ctypes.c_float
+    sig = {
+        "fd_plan_create": (I, [I, I, I, I, I, I, I, I, I, F, ctypes.POINTER(P)]),
+        "fd_plan_destroy": (I, [P]),
+        "fd_set_plan": (I, [P]),
+        "fd_get_plan": (P, []),
+        "fd_decode_paged": (I, [T, T, T, T, T, T, I, I, T, T, P]),
+        "fd_set_max_seqlen_hint": (I, [P, I]),
+        "fd_autotune": (I, [P, ctypes.POINTER(I), I, I, I, P]),
+        "fd_query_splits": (I, [P, I, I, ctypes.POINTER(I)]),
+        "fd_autotune_set_timer": (I, [P, TIMER_FN, P]),
+        "fd_autotune_set_cache_dir": (I, [P, ctypes.c_char_p]),
+        "fd_autotune_stats": (I, [P, ctypes.POINTER(I), ctypes.POINTER(I)]),
+        "fd_read_device_status": (I, [P, ctypes.POINTER(I)]),
+        "fd_plan_workspace_bytes": (I, [P, ctypes.POINTER(ctypes.c_size_t)]),
+        "fd_status_string": (ctypes.c_char_p, [I]),
+        "fd_last_error": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _LIB = lib
+    return lib
+
+
+def _check(status: int):
+    if status != FD_OK:
+        raise FdError(status, load_library().fd_last_error().decode(errors="replace"))
+
+
+def fd_status_string(status: int) -> str:
+    return load_library().fd_status_string(status).decode()
+
+
+def fd_last_error() -> str:
+    return load_library().fd_last_error().decode(errors="replace")
+
+
+# ---------------------------------------------------------------------------
+# descriptors
+
+
+def _dtype_code(t) -> int:
+    import torch
+    m = {torch.bfloat16: FD_BF16, torch.float32: FD_FP32, torch.int8: FD_INT8, torch.uint8: FD_INT4X2,
+         torch.int32: FD_INT32}
+    return m.get(t.dtype, -1)      # the library rejects unknown codes
+
+
+def make_descriptor(t) -> Optional[FdTensor]:
+    """fd_tensor for a torch tensor (or None for None)."""
+    if t is None:
+        return None
+    if t.dim() > 5:
+        raise ValueError("at most 5 dimensions")
+    d = FdTensor()
+    d.data = t.data_ptr()
+    d.dtype = _dtype_code(t)
+    d.ndim = t.dim()
+    for i, (s, st) in enumerate(zip(t.shape, t.stride())):
+        d.shape[i] = s
+        d.stride[i] = st
+    return d
+
+
+def _ref(d: Optional[FdTensor]):
+    return ctypes.byref(d) if d is not None else None
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _kv_code(kv_dtype) -> int:
+    return _KV_NAMES[kv_dtype] if isinstance(kv_dtype, str) else int(kv_dtype)
+
+
+# ---------------------------------------------------------------------------
+# entry points (same names as the C ABI)
+
+
+def fd_plan_create(device: int, max_batch: int, max_q_per_req: int, num_q_heads: int, num_kv_heads: int,
+                   head_dim: int, page_size: int, kv_dtype, max_splits: int,
+                   softmax_scale: float = 0.0) -> int:
+    """Create a plan; returns the opaque handle (an int). device=-1: host-only plan."""
+    h = ctypes.c_void_p()
+    _check(load_library().fd_plan_create(device, max_batch, max_q_per_req, num_q_heads, num_kv_heads, head_dim,
+                                         page_size, _kv_code(kv_dtype), max_splits, softmax_scale,
+                                         ctypes.byref(h)))
+    return h.value
+
+
+def fd_plan_destroy(plan: int) -> None:
+    _check(load_library().fd_plan_destroy(plan))
+
+
+def fd_set_plan(plan: Optional[int]) -> None:
+    _check(load_library().fd_set_plan(plan))
+
+
+def fd_get_plan() -> Optional[int]:
+    return load_library().fd_get_plan()
+
+
+def fd_decode_paged(q, k_cache, v_cache, kv_scales, page_table, cache_seqlens, q_per_req: int,
+                    num_splits: int, out, lse, stream=None) -> None:
+    """Enqueue one decode call on ``stream`` (default: torch's current stream)."""
+    descs = [make_descriptor(t) for t in (q, k_cache, v_cache, kv_scales, page_table, cache_seqlens, out, lse)]
+    _check(load_library().fd_decode_paged(*(_ref(d) for d in descs[:6]), q_per_req, num_splits,
+                                          _ref(descs[6]), _ref(descs[7]), _stream_handle(stream)))
+
+
+def fd_set_max_seqlen_hint(plan: int, max_seqlen: int) -> None:
+    _check(load_library().fd_set_max_seqlen_hint(plan, max_seqlen))
+
+
+def fd_autotune(plan: int, batch_sizes: Sequence[int], min_bucket: int = 0, max_bucket: int = 0,
+                stream=None) -> None:
+    arr = (ctypes.c_int * len(batch_sizes))(*batch_sizes)
+    st = None if plan in _timers else _stream_handle(stream)   # a timer hook launches nothing
+    _check(load_library().fd_autotune(plan, arr, len(batch_sizes), min_bucket, max_bucket, st))
+
+
+def fd_query_splits(plan: int, batch: int, max_seqlen: int) -> int:
+    v = ctypes.c_int()
+    _check(load_library().fd_query_splits(plan, batch, max_seqlen, ctypes.byref(v)))
+    return v.value
+
+
+_timers = {}
+
+
+def fd_autotune_set_timer(plan: int, fn) -> None:
+    """Install ``fn(batch, bucket, num_splits) -> time`` (None restores CUDA events)."""
+    if fn is None:
+        _timers.pop(plan, None)
+        _check(load_library().fd_autotune_set_timer(plan, TIMER_FN(), None))
+        return
+    cb = TIMER_FN(lambda user, b, k, s: float(fn(b, k, s)))
+    _timers[plan] = cb  # keep the callback alive
+    _check(load_library().fd_autotune_set_timer(plan, cb, None))
+
+
+def fd_autotune_set_cache_dir(plan: int, directory: Optional[str]) -> None:
+    _check(load_library().fd_autotune_set_cache_dir(plan, directory.encode() if directory else None))
+
+
+def fd_autotune_stats(plan: int) -> Tuple[int, int]:
+    a, b = ctypes.c_int(), ctypes.c_int()
+    _check(load_library().fd_autotune_stats(plan, ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+def fd_read_device_status(plan: int) -> int:
+    """Read and clear the plan's device status word (FD_DEVSTAT_* bits)."""
+    v = ctypes.c_int()
+    s = load_library().fd_read_device_status(plan, ctypes.byref(v))
+    if s not in (FD_OK, FD_ERR_DEVICE_STATUS):
+        _check(s)
+    return v.value
+
+
+def fd_plan_workspace_bytes(plan: int) -> int:
+    v = ctypes.c_size_t()
+    _check(load_library().fd_plan_workspace_bytes(plan, ctypes.byref(v)))
+    return v.value

@@ -1,0 +1,426 @@
+// autotune.cu - num_splits selection and the startup autotuner.
+//
+// Follows "feat(autotune): separate general and decode attention warmup"
+// (LightLLM PR 1549): decode attention is tuned only at startup, outside CUDA
+// graph capture, on representative inputs built for the purpose (section
+// "Changes": rebuild_input_func; representative length 32768 by default,
+// section "Covered decode kernels"); KV-length run keys are bucketed while a
+// call still uses its real lengths; chosen configurations are persisted per
+// kernel and reused, and deleting the cache forces a new search (section
+// "Changes": FORCE_AUTOTUNE as adaptive tuning); cached nearest-key matches are
+// invalidated when a new configuration is saved.
+//
+// Table key: (batch, bucket) with bucket a power of two of the KV length.
+// Lookup for a call: the nearest tuned batch (smallest >= B, else the
+// largest), then the bucket of the host-known max length (exact, else the
+// smallest larger, else the largest), memoised until the next save. Without
+// any entry a heuristic sizes the grid to two CTAs per SM.
+#include <cuda_runtime.h>
+#include <sys/stat.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <set>
+#include <string>
+#include <vector>
+
+#include "fd.h"
+#include "kernels.h"
+#include "plan.h"
+
+using fd::fail;
+
+namespace {
+
+int next_pow2(int v) {
+  int r = 1;
+  while (r < v && r < (1 << 30)) r <<= 1;
+  return r;
+}
+
+bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+
+int heuristic_splits(const fd_plan *pl, int batch, int max_seqlen) {
+  const int G = pl->hq / pl->hkv;
+  const long ctas = static_cast<long>(batch) * pl->hkv * ((G + 15) / 16);
+  const long target = 2L * pl->num_sms;
+  int s = 1;
+  while (static_cast<long>(s) * ctas < target && s < pl->max_splits) s <<= 1;
+  const int L = max_seqlen > 0 ? max_seqlen : 32768;
+  while (s > 1 && L / s < 256) s >>= 1;
+  return std::min(s, pl->max_splits);
+}
+
+const char *kv_name(fd_dtype t) {
+  return t == FD_BF16 ? "bf16" : t == FD_INT8 ? "int8" : t == FD_INT4X2 ? "int4" : "x";
+}
+
+std::string cache_path(const fd_plan *pl) {
+  return pl->cache_dir + "/fd_splits_" + fd::autotune_key(pl) + ".json";
+}
+
+// -------------------------------------------------------------- tuning inputs
+
+// Integer mixer ("lowbias32", C. Wellons) for reproducible synthetic fills.
+__device__ __forceinline__ uint32_t mix32(uint32_t x) {
+  x ^= x >> 16;
+  x *= 0x7feb352du;
+  x ^= x >> 15;
+  x *= 0x846ca68bu;
+  x ^= x >> 16;
+  return x;
+}
+
+__global__ void fill_bf16_kernel(__nv_bfloat16 *p, size_t n, uint32_t seed) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const uint32_t h = mix32(static_cast<uint32_t>(i) * 2654435761u ^ seed ^ static_cast<uint32_t>(i >> 32));
+    p[i] = __float2bfloat16_rn((h >> 8) * (2.0f / 16777216.0f) - 1.0f);
+  }
+}
+
+__global__ void fill_u8_kernel(uint8_t *p, size_t n, uint32_t seed) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    p[i] = static_cast<uint8_t>(mix32(static_cast<uint32_t>(i) ^ seed) >> 24);
+}
+
+__global__ void fill_f32_kernel(float *p, size_t n, float v) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    p[i] = v;
+}
+
+struct TuneBuffers {
+  void *q = nullptr, *out = nullptr, *k = nullptr, *v = nullptr, *flush = nullptr;
+  float *lse = nullptr, *scales = nullptr;
+  int *pt = nullptr, *sl = nullptr;
+  size_t flush_bytes = 0;
+  long pool_pages = 0;
+  int width = 0, bmax = 0, tq = 1;
+  ~TuneBuffers() {
+    for (void *p : {q, out, k, v, flush, static_cast<void *>(lse), static_cast<void *>(scales),
+                    static_cast<void *>(pt), static_cast<void *>(sl)})
+      if (p) cudaFree(p);
+  }
+};
+
+#define TRY_CUDA(x)                                                                        \
+  do {                                                                                     \
+    cudaError_t e_ = (x);                                                                  \
+    if (e_ != cudaSuccess) return fail(FD_ERR_CUDA, "autotune: %s: %s", #x, cudaGetErrorString(e_)); \
+  } while (0)
+
+fd_status tune_alloc(fd_plan *pl, TuneBuffers &tb, int bmax, int max_bucket, cudaStream_t st) {
+  int l2 = 0;
+  TRY_CUDA(cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, pl->device));
+  const int rowe = pl->kv_dtype == FD_INT4X2 ? pl->d / 2 : pl->d;
+  const int es = pl->kv_dtype == FD_BF16 ? 2 : 1;
+  const int ng = pl->kv_dtype == FD_INT4X2 ? pl->d / 32 : 1;
+  const size_t page_bytes = static_cast<size_t>(pl->page) * pl->hkv * rowe * es;
+  tb.bmax = bmax;
+  tb.tq = pl->max_q;
+  tb.width = (max_bucket + pl->page - 1) / pl->page;
+  const long need = static_cast<long>(bmax) * tb.width;
+  // a pool well above L2 so timed calls stream from HBM, capped at what is needed
+  const long cap = static_cast<long>((4.0 * std::max(l2, 1 << 20)) / page_bytes) + 1;
+  tb.pool_pages = std::min(need, cap);
+  const size_t qn = static_cast<size_t>(bmax) * tb.tq * pl->hq * pl->d;
+  const size_t kvn = static_cast<size_t>(tb.pool_pages) * pl->page * pl->hkv * rowe;
+  TRY_CUDA(cudaMalloc(&tb.q, qn * 2));
+  TRY_CUDA(cudaMalloc(&tb.out, qn * 2));
+  TRY_CUDA(cudaMalloc(&tb.lse, static_cast<size_t>(bmax) * tb.tq * pl->hq * 4));
+  TRY_CUDA(cudaMalloc(&tb.k, kvn * es));
+  TRY_CUDA(cudaMalloc(&tb.v, kvn * es));
+  if (pl->kv_dtype != FD_BF16) {
+    const size_t sn = 2ull * tb.pool_pages * pl->page * pl->hkv * ng;
+    TRY_CUDA(cudaMalloc(&tb.scales, sn * 4));
+    fill_f32_kernel<<<1024, 256, 0, st>>>(tb.scales, sn, 0.02f);
+  }
+  TRY_CUDA(cudaMalloc(&tb.pt, static_cast<size_t>(bmax) * tb.width * 4));
+  TRY_CUDA(cudaMalloc(&tb.sl, static_cast<size_t>(bmax) * 4));
+  tb.flush_bytes = 2ull * std::max(l2, 1 << 20);
+  TRY_CUDA(cudaMalloc(&tb.flush, tb.flush_bytes));
+  fill_bf16_kernel<<<1024, 256, 0, st>>>(static_cast<__nv_bfloat16 *>(tb.q), qn, 17u);
+  if (pl->kv_dtype == FD_BF16) {
+    fill_bf16_kernel<<<4096, 256, 0, st>>>(static_cast<__nv_bfloat16 *>(tb.k), kvn, 29u);
+    fill_bf16_kernel<<<4096, 256, 0, st>>>(static_cast<__nv_bfloat16 *>(tb.v), kvn, 31u);
+  } else {
+    fill_u8_kernel<<<4096, 256, 0, st>>>(static_cast<uint8_t *>(tb.k), kvn, 29u);
+    fill_u8_kernel<<<4096, 256, 0, st>>>(static_cast<uint8_t *>(tb.v), kvn, 31u);
+  }
+  TRY_CUDA(cudaGetLastError());
+  std::vector<int> pt(static_cast<size_t>(bmax) * tb.width);
+  for (int b = 0; b < bmax; ++b)
+    for (int p = 0; p < tb.width; ++p)
+      pt[static_cast<size_t>(b) * tb.width + p] =
+          static_cast<int>((static_cast<long>(b) * tb.width + p) % tb.pool_pages);
+  TRY_CUDA(cudaMemcpyAsync(tb.pt, pt.data(), pt.size() * 4, cudaMemcpyHostToDevice, st));
+  TRY_CUDA(cudaStreamSynchronize(st));
+  return FD_OK;
+}
+
+void make_desc(fd_tensor &t, void *data, fd_dtype dt, std::initializer_list<int64_t> shape) {
+  std::memset(&t, 0, sizeof(t));
+  t.data = data;
+  t.dtype = dt;
+  t.ndim = static_cast<int>(shape.size());
+  int i = 0;
+  for (int64_t s : shape) t.shape[i++] = s;
+  int64_t st = 1;
+  for (int k = t.ndim - 1; k >= 0; --k) {
+    t.stride[k] = st;
+    st *= t.shape[k];
+  }
+}
+
+fd_status tune_time(fd_plan *pl, TuneBuffers &tb, int batch, int bucket, int S, cudaStream_t st,
+                    double *ms_out) {
+  const int rowe = pl->kv_dtype == FD_INT4X2 ? pl->d / 2 : pl->d;
+  const int ng = pl->kv_dtype == FD_INT4X2 ? pl->d / 32 : 1;
+  std::vector<int> sl(batch, bucket);
+  TRY_CUDA(cudaMemcpyAsync(tb.sl, sl.data(), sl.size() * 4, cudaMemcpyHostToDevice, st));
+  fd_tensor q, k, v, sc, pt, sq, out, lse;
+  make_desc(q, tb.q, FD_BF16, {batch, tb.tq, pl->hq, pl->d});
+  make_desc(k, tb.k, pl->kv_dtype, {tb.pool_pages, pl->page, pl->hkv, rowe});
+  make_desc(v, tb.v, pl->kv_dtype, {tb.pool_pages, pl->page, pl->hkv, rowe});
+  make_desc(sc, tb.scales, FD_FP32, {2, tb.pool_pages, pl->page, pl->hkv, ng});
+  make_desc(pt, tb.pt, FD_INT32, {batch, tb.width});
+  make_desc(sq, tb.sl, FD_INT32, {batch});
+  make_desc(out, tb.out, FD_BF16, {batch, tb.tq, pl->hq, pl->d});
+  make_desc(lse, tb.lse, FD_FP32, {batch, tb.tq, pl->hq});
+  fd_plan *prev = fd_get_plan();
+  fd_set_plan(pl);
+  cudaEvent_t e0, e1;
+  cudaEventCreate(&e0);
+  cudaEventCreate(&e1);
+  std::vector<float> times;
+  fd_status s = FD_OK;
+  for (int rep = 0; rep < 4 && s == FD_OK; ++rep) {
+    cudaMemsetAsync(tb.flush, rep & 0xff, tb.flush_bytes, st);
+    cudaEventRecord(e0, st);
+    s = fd_decode_paged(&q, &k, &v, tb.scales ? &sc : nullptr, &pt, &sq, tb.tq, S, &out, &lse,
+                        reinterpret_cast<fd_stream_t>(st));
+    cudaEventRecord(e1, st);
+    if (cudaEventSynchronize(e1) != cudaSuccess) s = fail(FD_ERR_CUDA, "autotune: timing call failed");
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, e0, e1);
+    if (rep > 0) times.push_back(ms);  // first call warms up
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  fd_set_plan(prev);
+  if (s != FD_OK) return s;
+  std::sort(times.begin(), times.end());
+  *ms_out = times[times.size() / 2];
+  return FD_OK;
+}
+
+}  // namespace
+
+namespace fd {
+
+std::string autotune_key(const fd_plan *pl) {
+  std::string g;
+  for (char c : pl->gpu_name) g += (isalnum(static_cast<unsigned char>(c)) ? c : '_');
+  char buf[256];
+  snprintf(buf, sizeof(buf), "%s_%dsm_%s_hq%d_hkv%d_d%d_p%d_tq%d", g.c_str(), pl->num_sms,
+           kv_name(pl->kv_dtype), pl->hq, pl->hkv, pl->d, pl->page, pl->max_q);
+  return buf;
+}
+
+fd_status autotune_load(fd_plan *pl) {
+  pl->cache_loaded = true;
+  if (pl->cache_dir.empty()) return FD_OK;
+  FILE *f = fopen(cache_path(pl).c_str(), "rb");
+  if (!f) return FD_OK;  // nothing cached yet
+  std::string txt;
+  char buf[4096];
+  size_t n;
+  while ((n = fread(buf, 1, sizeof(buf), f)) > 0) txt.append(buf, n);
+  fclose(f);
+  const size_t ent = txt.find("\"entries\"");
+  if (ent == std::string::npos) return fail(FD_ERR_IO, "autotune cache %s has no entries", cache_path(pl).c_str());
+  size_t pos = ent;
+  auto field = [](const std::string &obj, const char *name, long *v) {
+    const size_t k = obj.find(std::string("\"") + name + "\"");
+    if (k == std::string::npos) return false;
+    const size_t c = obj.find(':', k);
+    if (c == std::string::npos) return false;
+    char *end = nullptr;
+    *v = strtol(obj.c_str() + c + 1, &end, 10);
+    return end != obj.c_str() + c + 1;
+  };
+  while ((pos = txt.find('{', pos + 1)) != std::string::npos) {
+    const size_t close = txt.find('}', pos);
+    if (close == std::string::npos) break;
+    const std::string obj = txt.substr(pos, close - pos);
+    long b, k, s;
+    if (field(obj, "batch", &b) && field(obj, "bucket", &k) && field(obj, "num_splits", &s) && b >= 1 &&
+        is_pow2(static_cast<int>(k)) && s >= 1 && s <= pl->max_splits)
+      pl->table[{static_cast<int>(b), static_cast<int>(k)}] = static_cast<int>(s);
+    pos = close;
+  }
+  pl->memo.clear();
+  return FD_OK;
+}
+
+fd_status autotune_save(fd_plan *pl) {
+  pl->memo.clear();  // a new configuration invalidates nearest-key matches
+  if (pl->cache_dir.empty()) return FD_OK;
+  mkdir(pl->cache_dir.c_str(), 0755);
+  const std::string path = cache_path(pl);
+  const std::string tmp = path + ".tmp";
+  FILE *f = fopen(tmp.c_str(), "wb");
+  if (!f) return fail(FD_ERR_IO, "cannot write %s", tmp.c_str());
+  fprintf(f, "{\n  \"version\": 1,\n  \"key\": \"%s\",\n  \"entries\": [", autotune_key(pl).c_str());
+  bool first = true;
+  for (const auto &kv : pl->table) {
+    auto t = pl->table_time.find(kv.first);
+    fprintf(f, "%s\n    {\"batch\": %d, \"bucket\": %d, \"num_splits\": %d, \"time\": %.6g}", first ? "" : ",",
+            kv.first.first, kv.first.second, kv.second, t == pl->table_time.end() ? 0.0 : t->second);
+    first = false;
+  }
+  fprintf(f, "\n  ]\n}\n");
+  if (fclose(f) != 0 || rename(tmp.c_str(), path.c_str()) != 0)
+    return fail(FD_ERR_IO, "cannot write %s", path.c_str());
+  return FD_OK;
+}
+
+int choose_splits(fd_plan *pl, int batch, int max_seqlen) {
+  if (pl->table.empty()) return heuristic_splits(pl, batch, max_seqlen);
+  const int bucket_q = max_seqlen > 0 ? next_pow2(max_seqlen) : 0;
+  auto m = pl->memo.find({batch, bucket_q});
+  if (m != pl->memo.end()) return m->second;
+  std::set<int> batches;
+  for (const auto &kv : pl->table) batches.insert(kv.first.first);
+  auto bi = batches.lower_bound(batch);
+  const int tb = bi != batches.end() ? *bi : *batches.rbegin();
+  std::set<int> buckets;
+  for (const auto &kv : pl->table)
+    if (kv.first.first == tb) buckets.insert(kv.first.second);
+  int kb;
+  if (bucket_q == 0) {
+    kb = *buckets.rbegin();
+  } else {
+    auto ki = buckets.lower_bound(bucket_q);
+    kb = ki != buckets.end() ? *ki : *buckets.rbegin();
+  }
+  const int S = std::min(pl->table[{tb, kb}], pl->max_splits);
+  pl->memo[{batch, bucket_q}] = S;
+  return S;
+}
+
+}  // namespace fd
+
+extern "C" {
+
+fd_status fd_query_splits(fd_plan *plan, int batch, int max_seqlen, int *num_splits) {
+  if (!plan || !num_splits) return fail(FD_ERR_INVALID_ARG, "NULL argument");
+  if (batch < 1) return fail(FD_ERR_INVALID_ARG, "batch %d < 1", batch);
+  if (max_seqlen < 0) return fail(FD_ERR_INVALID_ARG, "max_seqlen %d < 0", max_seqlen);
+  if (!plan->cache_loaded) fd::autotune_load(plan);
+  *num_splits = fd::choose_splits(plan, batch, max_seqlen);
+  return FD_OK;
+}
+
+fd_status fd_autotune_set_timer(fd_plan *plan, fd_timer_fn fn, void *user) {
+  if (!plan) return fail(FD_ERR_INVALID_ARG, "plan is NULL");
+  plan->timer = fn;
+  plan->timer_user = user;
+  return FD_OK;
+}
+
+fd_status fd_autotune_set_cache_dir(fd_plan *plan, const char *dir) {
+  if (!plan) return fail(FD_ERR_INVALID_ARG, "plan is NULL");
+  plan->cache_dir = dir ? dir : "";
+  return fd::autotune_load(plan);
+}
+
+fd_status fd_autotune_stats(fd_plan *plan, int *searches, int *cache_hits) {
+  if (!plan) return fail(FD_ERR_INVALID_ARG, "plan is NULL");
+  if (searches) *searches = plan->searches;
+  if (cache_hits) *cache_hits = plan->cache_hits;
+  return FD_OK;
+}
+
+fd_status fd_autotune(fd_plan *plan, const int *batch_sizes, int n_batch, int min_bucket, int max_bucket,
+                      fd_stream_t stream) {
+  if (!plan) return fail(FD_ERR_INVALID_ARG, "plan is NULL");
+  if (!batch_sizes || n_batch < 1) return fail(FD_ERR_INVALID_ARG, "no batch sizes");
+  for (int i = 0; i < n_batch; ++i)
+    if (batch_sizes[i] < 1 || batch_sizes[i] > plan->max_batch)
+      return fail(FD_ERR_INVALID_ARG, "batch size %d not in [1, %d]", batch_sizes[i], plan->max_batch);
+  if (min_bucket == 0) min_bucket = 1024;
+  if (max_bucket == 0) {
+    max_bucket = 32768;
+    if (const char *e = std::getenv("FD_AUTOTUNE_SEQ_LEN")) {
+      const int v = atoi(e);
+      if (v > 0) max_bucket = next_pow2(v);
+    }
+  }
+  if (!is_pow2(min_bucket) || !is_pow2(max_bucket) || min_bucket > max_bucket)
+    return fail(FD_ERR_INVALID_ARG, "buckets must be powers of two with min <= max");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!plan->timer) {
+    if (plan->device < 0) return fail(FD_ERR_WORKSPACE, "host-only plan cannot time kernels");
+    fd::DeviceGuard guard(plan->device);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess)
+      return fail(FD_ERR_CUDA, "cudaStreamIsCapturing failed");
+    if (cs != cudaStreamCaptureStatusNone)
+      return fail(FD_ERR_CAPTURING, "autotuning cannot run inside CUDA graph capture");
+  }
+  if (!plan->cache_loaded) {
+    fd_status s = fd::autotune_load(plan);
+    if (s != FD_OK) return s;
+  }
+  const char *force_env = std::getenv("FD_FORCE_AUTOTUNE");
+  const bool force = force_env && force_env[0] == '1';
+
+  std::vector<std::pair<int, int>> todo;
+  for (int i = 0; i < n_batch; ++i)
+    for (int k = min_bucket; k <= max_bucket; k <<= 1) {
+      const std::pair<int, int> key{batch_sizes[i], k};
+      if (!force && plan->table.count(key)) {
+        ++plan->cache_hits;
+        continue;
+      }
+      if (std::find(todo.begin(), todo.end(), key) == todo.end()) todo.push_back(key);
+    }
+  if (todo.empty()) return FD_OK;
+
+  fd::DeviceGuard guard(plan->device);
+  TuneBuffers tb;
+  if (!plan->timer) {
+    int bmax = 0;
+    for (auto &k : todo) bmax = std::max(bmax, k.first);
+    fd_status s = tune_alloc(plan, tb, bmax, max_bucket, st);
+    if (s != FD_OK) return s;
+  }
+  for (auto &key : todo) {
+    ++plan->searches;
+    int best = 1;
+    double best_t = 0.0;
+    for (int S = 1; S <= plan->max_splits; S <<= 1) {
+      double t = 0.0;
+      if (plan->timer) {
+        t = plan->timer(plan->timer_user, key.first, key.second, S);
+      } else {
+        fd_status s = tune_time(plan, tb, key.first, key.second, S, st, &t);
+        if (s != FD_OK) return s;
+      }
+      if (S == 1 || t < best_t) {
+        best = S;
+        best_t = t;
+      }
+    }
+    plan->table[key] = best;
+    plan->table_time[key] = best_t;
+  }
+  return fd::autotune_save(plan);
+}
+
+}  // extern "C"

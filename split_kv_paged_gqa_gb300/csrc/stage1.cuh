@@ -1,0 +1,625 @@
+// stage1.cuh - split-KV paged GQA flash decode, stage 1 (sm_103a).
+//
+// Computes, for one (request b, KV head h, KV split s, tile of 16 query rows),
+// the softmax-normalised partial output and log-sum-exp of the tile's rows
+// over the split's keys: "Triton GQA flash decode stage 1" and its INT8 /
+// INT4 KV variants in "feat(autotune): separate general and decode attention
+// warmup" (LightLLM PR 1549), section "Covered decode kernels". The query rows
+// of a tile are the G query heads of KV head h times the Tq query tokens
+// (row r = t * G + g), so K and V are read once per group ("GQA").
+//
+// Structure of one CTA (NUM_CW consumer warps + 1 producer warp):
+//  * split range: chunk = P * ceil(ceil(L_b / S) / P); split s owns keys
+//    [s * chunk, min(L_b, (s + 1) * chunk)), derived here from cache_seqlens.
+//  * producer warp: reads page ids from the page table one stage ahead, and
+//    lane 0 issues 4-D TMA loads (d, head, slot, page) of whole page segments
+//    of K and V into a STAGES-deep shared-memory ring, 128-byte swizzled,
+//    completing on a per-stage mbarrier. Quantised caches also copy their
+//    per-row fp32 scales with cp.async (one arrival per lane on the barrier).
+//  * consumer warps: warp w takes keys [16w, 16w + 16) of each 64-key stage.
+//    Quantised rows are first converted to bf16 in a per-warp staging tile
+//    (int8 / int4 codes are exact in bf16). QK^T and PV run on mma.sync
+//    m16n8k16 (bf16 in, fp32 accumulate) with the 16 query rows as M; the
+//    online softmax keeps a running max / sum per row in the log2 domain with
+//    quad shuffles. K scales multiply the fp32 scores (per 32-channel group
+//    for int4, from separate per-group accumulators); V scales are folded into
+//    the probabilities before they are rounded to bf16 for PV.
+//  * epilogue: the consumer warps merge their (max, sum, O) through shared
+//    memory and write either fp32 partial O + LSE to the split workspace, or
+//    (num_splits == 1) the final bf16/fp32 output and LSE.
+//
+// Keys at or past a row's limit are masked by selection (-inf score, zero
+// probability), and V rows past the split end are zeroed in shared memory
+// before PV, so stale or poisoned cache slots (NaN, huge values) never reach
+// a result.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace fd {
+
+template <int KIND, int D_>
+struct S1Cfg {
+  static constexpr int D = D_;
+  static constexpr bool QUANT = KIND != KV_BF16;
+  static constexpr int ROW_BYTES = KIND == KV_BF16 ? 2 * D : (KIND == KV_I8 ? D : D / 2);
+  static constexpr int BOX_BYTES = ROW_BYTES < 128 ? ROW_BYTES : 128;  // TMA box inner extent
+  static constexpr int N_BOX = ROW_BYTES / BOX_BYTES;
+  static constexpr int BOX_ELEMS = KIND == KV_BF16 ? BOX_BYTES / 2 : BOX_BYTES;
+  static constexpr int NG = KIND == KV_I4 ? D / 32 : 1;  // fp32 scales per cache row
+  static constexpr int BLOCK_N = 64;                     // keys per pipeline stage
+  static constexpr int NUM_CW = 4;                       // consumer warps (16 keys each)
+  static constexpr int THREADS = (NUM_CW + 1) * 32;
+  static constexpr int STAGES = KIND == KV_BF16 ? 3 : (KIND == KV_I8 ? 4 : 6);
+  static constexpr int TILE = BLOCK_N * ROW_BYTES;       // K (or V) bytes of one stage
+  static constexpr int SC = QUANT ? BLOCK_N * NG * 4 : 0;
+  static constexpr int STAGE = ((2 * TILE + 2 * SC) + 1023) / 1024 * 1024;
+  static constexpr int RING = STAGES * STAGE;
+  static constexpr int STG_HALF = 16 * 128;              // 16 rows x 64 bf16
+  static constexpr int STG_TILE = (D / 64) * STG_HALF;   // one K or V staging tile of a warp
+  static constexpr int STG = QUANT ? NUM_CW * 2 * STG_TILE : 0;
+  static constexpr int QROW = D * 2 + 16;                // padded bf16 row of the Q tile
+  static constexpr int QB = 16 * QROW;
+  static constexpr int CROW = D + 8;                     // padded fp32 row of the combine tile
+  static constexpr int CMB_O = NUM_CW * 16 * CROW * 4;
+  static constexpr int CMB = CMB_O + NUM_CW * 16 * 2 * 4;
+  static constexpr int OFF_STG = RING;
+  static constexpr int OFF_Q = OFF_STG + STG;
+  static constexpr int OFF_BAR = (OFF_Q + QB + 7) / 8 * 8;
+  static constexpr int SMEM = OFF_BAR + 2 * STAGES * 8;
+  static constexpr int SMEM_ALLOC = SMEM + 1024;         // slack to align the base to 1024
+  static constexpr int MIN_BLOCKS = SMEM_ALLOC * 2 <= 227 * 1024 ? 2 : 1;
+  static_assert(CMB <= RING, "combine tile must fit in the ring");
+  static_assert(TILE % 1024 == 0, "tiles must keep the 1024-byte swizzle alignment");
+  static_assert(D == 64 || D == 128, "head_dim");
+};
+
+// ----------------------------------------------------------------------------
+// In-register conversions of cache codes to bf16 (exact: |code| <= 128).
+
+// Four int8 codes (one 32-bit word, lowest byte = lowest channel) -> two
+// bf16x2 words. A biased byte u = code + 128 placed in the low mantissa bits
+// of 2^23 gives the float 2^23 + u exactly; subtracting 2^23 + 128 yields code.
+__device__ __forceinline__ void i8x4_to_bf16(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  const uint32_t x = w ^ 0x80808080u;
+  const float f0 = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7650)) - 8388736.0f;
+  const float f1 = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7651)) - 8388736.0f;
+  const float f2 = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7652)) - 8388736.0f;
+  const float f3 = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7653)) - 8388736.0f;
+  lo = pack_bf16x2(f0, f1);
+  hi = pack_bf16x2(f2, f3);
+}
+
+// One byte of two int4 codes (low nibble = even channel) -> one bf16x2 word.
+// A biased nibble u = code + 8 in the mantissa of bf16 128.0 gives 128 + u
+// exactly; subtracting 136 yields code.
+__device__ __forceinline__ uint32_t i4x2_to_bf16(uint32_t biased_byte) {
+  uint32_t r = 0x43004300u | (biased_byte & 0xFu) | ((biased_byte & 0xF0u) << 12);
+  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&r);
+  v = __hsub2(v, __floats2bfloat162_rn(136.0f, 136.0f));
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Convert this warp's 16 cache rows (tile rows row0..row0+15 of a raw stage
+// tile) into a bf16 staging tile laid out like a bf16 TMA tile (64-element
+// halves of 16 rows x 128 bytes, 128-byte swizzled). Rows whose token index is
+// >= zero_from are written as zeros.
+template <class C, int KIND>
+__device__ __forceinline__ void stage_rows_bf16(const uint8_t *raw, uint8_t *stg, int row0,
+                                                int tok_row0, int zero_from, int lane) {
+  constexpr int CHUNKS = C::ROW_BYTES / 16;     // 16-byte chunks per raw row
+  constexpr int JOBS = 16 * CHUNKS;
+  constexpr int VALS = KIND == KV_I8 ? 16 : 32;  // codes per raw chunk
+#pragma unroll
+  for (int job = lane; job < JOBS; job += 32) {
+    const int r = job / CHUNKS, cc = job % CHUNKS;
+    const uint32_t roff = swz<C::BOX_BYTES>((row0 + r) * C::ROW_BYTES + cc * 16);
+    const uint4 src = *reinterpret_cast<const uint4 *>(raw + roff);
+    const bool zero = tok_row0 + r >= zero_from;
+    uint32_t out[VALS / 2];
+    if (KIND == KV_I8) {
+      i8x4_to_bf16(src.x, out[0], out[1]);
+      i8x4_to_bf16(src.y, out[2], out[3]);
+      i8x4_to_bf16(src.z, out[4], out[5]);
+      i8x4_to_bf16(src.w, out[6], out[7]);
+    } else {
+      const uint32_t w[4] = {src.x ^ 0x88888888u, src.y ^ 0x88888888u, src.z ^ 0x88888888u,
+                             src.w ^ 0x88888888u};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+#pragma unroll
+        for (int bi = 0; bi < 4; ++bi) out[k * 4 + bi] = i4x2_to_bf16((w[k] >> (8 * bi)) & 0xFFu);
+      }
+    }
+    const int d0 = cc * VALS;
+#pragma unroll
+    for (int q = 0; q < VALS / 8; ++q) {
+      const int d = d0 + q * 8;
+      uint8_t *dst = stg + (d >> 6) * C::STG_HALF + swz<128>(r * 128 + (d & 63) * 2);
+      uint4 v;
+      v.x = zero ? 0u : out[q * 4 + 0];
+      v.y = zero ? 0u : out[q * 4 + 1];
+      v.z = zero ? 0u : out[q * 4 + 2];
+      v.w = zero ? 0u : out[q * 4 + 3];
+      *reinterpret_cast<uint4 *>(dst) = v;
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// One 16-key block of one warp: scores, online softmax update, PV.
+//
+// kbase / vbase: shared addresses of bf16 tiles laid out as 64-element halves
+// (half stride `half`) of 128-byte swizzled rows; the warp's keys are rows
+// row0..row0+15. ksc / vsc: per-row fp32 scales (NG per row) or null.
+template <class C>
+__device__ __forceinline__ void warp_block(uint32_t kbase, uint32_t vbase, uint32_t half, int row0,
+                                           const float *ksc, const float *vsc, int sc_row0,
+                                           const uint32_t (&qa)[C::D / 16][4],
+                                           float (&o)[C::D / 8][4], float (&m)[2], float (&l)[2],
+                                           int tok_row0, int lim0, int lim1, float scale_log2,
+                                           int lane) {
+  constexpr int D = C::D;
+  constexpr int NG = C::NG;
+  const int c = lane & 3;
+  const int mi = lane >> 3, ri = lane & 7;
+
+  // ---- S = Q K^T (16 rows x 16 keys), one accumulator per scale group
+  float acc[NG][2][4];
+#pragma unroll
+  for (int gi = 0; gi < NG; ++gi)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[gi][nt][e] = 0.f;
+
+  const int krow = row0 + ((mi >> 1) << 3) + ri;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    const int d = ks * 16 + ((mi & 1) << 3);
+    uint32_t bk[4];
+    ldsm_x4(bk, kbase + (d >> 6) * half + swz<128>(krow * 128 + (d & 63) * 2));
+    const int gi = NG == 1 ? 0 : ks / 2;
+    mma_bf16_16816(acc[gi][0], qa[ks], bk[0], bk[1]);
+    mma_bf16_16816(acc[gi][1], qa[ks], bk[2], bk[3]);
+  }
+
+  // ---- scale, mask (by selection), running max
+  float s[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int key = nt * 8 + 2 * c + (e & 1);
+      float v;
+      if constexpr (C::QUANT) {
+        const float *sc = ksc + (sc_row0 + key) * NG;
+        v = 0.f;
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) v = fmaf(acc[gi][nt][e], sc[gi], v);
+      } else {
+        v = acc[0][nt][e];
+      }
+      const int lim = (e < 2) ? lim0 : lim1;
+      s[nt][e] = (tok_row0 + key < lim) ? v * scale_log2 : -INFINITY;
+    }
+  }
+  float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+  float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+  const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+  const float b0 = mn0 == -INFINITY ? 0.f : mn0;
+  const float b1 = mn1 == -INFINITY ? 0.f : mn1;
+  const float al0 = exp2f(m[0] - b0), al1 = exp2f(m[1] - b1);
+  m[0] = mn0;
+  m[1] = mn1;
+
+  float p[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    p[nt][0] = exp2f(s[nt][0] - b0);
+    p[nt][1] = exp2f(s[nt][1] - b0);
+    p[nt][2] = exp2f(s[nt][2] - b1);
+    p[nt][3] = exp2f(s[nt][3] - b1);
+  }
+  l[0] = l[0] * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+  l[1] = l[1] * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+
+  if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j) {
+      o[j][0] *= al0;
+      o[j][1] *= al0;
+      o[j][2] *= al1;
+      o[j][3] *= al1;
+    }
+  }
+
+  // ---- P (bf16, V scales folded per group) as the A operand of PV
+  constexpr int NGV = NG;
+  uint32_t pa[NGV][4];
+#pragma unroll
+  for (int gv = 0; gv < NGV; ++gv) {
+    float pv[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if constexpr (C::QUANT) {
+          const int key = nt * 8 + 2 * c + (e & 1);
+          const float vs = vsc[(sc_row0 + key) * NG + gv];
+          pv[nt][e] = p[nt][e] == 0.f ? 0.f : p[nt][e] * vs;
+        } else {
+          pv[nt][e] = p[nt][e];
+        }
+      }
+    }
+    pa[gv][0] = pack_bf16x2(pv[0][0], pv[0][1]);
+    pa[gv][1] = pack_bf16x2(pv[0][2], pv[0][3]);
+    pa[gv][2] = pack_bf16x2(pv[1][0], pv[1][1]);
+    pa[gv][3] = pack_bf16x2(pv[1][2], pv[1][3]);
+  }
+
+  // ---- O += P V
+  const int vrow = row0 + ((mi & 1) << 3) + ri;
+#pragma unroll
+  for (int dp = 0; dp < D / 16; ++dp) {
+    const int d = dp * 16 + ((mi >> 1) << 3);
+    uint32_t bv[4];
+    ldsm_x4_t(bv, vbase + (d >> 6) * half + swz<128>(vrow * 128 + (d & 63) * 2));
+    const int gv = NGV == 1 ? 0 : dp / 2;
+    mma_bf16_16816(o[2 * dp], pa[gv], bv[0], bv[1]);
+    mma_bf16_16816(o[2 * dp + 1], pa[gv], bv[2], bv[3]);
+  }
+}
+
+// ----------------------------------------------------------------------------
+
+template <class C>
+__device__ __forceinline__ void write_row_outputs(const Stage1Params &p, bool fused, int b, int h,
+                                                  int s, int row_glob, int d0, const float *vals,
+                                                  int nvals, float lse_nat, bool write_lse) {
+  const int t = row_glob / p.G, g = row_glob - t * p.G;
+  const int hq = h * p.G + g;
+  if (fused) {
+    if (p.out_f32) {
+      float *dst = reinterpret_cast<float *>(p.out) + b * p.o_sb + t * p.o_st + hq * p.o_sh + d0;
+      for (int i = 0; i < nvals; i += 4)
+        *reinterpret_cast<float4 *>(dst + i) = make_float4(vals[i], vals[i + 1], vals[i + 2], vals[i + 3]);
+    } else {
+      __nv_bfloat16 *dst =
+          reinterpret_cast<__nv_bfloat16 *>(p.out) + b * p.o_sb + t * p.o_st + hq * p.o_sh + d0;
+      for (int i = 0; i < nvals; i += 8) {
+        uint4 v;
+        v.x = pack_bf16x2(vals[i + 0], vals[i + 1]);
+        v.y = pack_bf16x2(vals[i + 2], vals[i + 3]);
+        v.z = pack_bf16x2(vals[i + 4], vals[i + 5]);
+        v.w = pack_bf16x2(vals[i + 6], vals[i + 7]);
+        *reinterpret_cast<uint4 *>(dst + i) = v;
+      }
+    }
+    if (write_lse && p.lse) p.lse[b * p.l_sb + t * p.l_st + hq * p.l_sh] = lse_nat;
+  } else {
+    const int64_t rowi = ((static_cast<int64_t>(b) * p.Tq + t) * p.Hq + hq) * p.num_splits + s;
+    float *dst = p.o_part + rowi * C::D + d0;
+    for (int i = 0; i < nvals; i += 4)
+      *reinterpret_cast<float4 *>(dst + i) = make_float4(vals[i], vals[i + 1], vals[i + 2], vals[i + 3]);
+    if (write_lse) p.lse_part[rowi] = lse_nat;
+  }
+}
+
+template <int KIND, int D, bool FUSED>
+__global__ void __launch_bounds__(S1Cfg<KIND, D>::THREADS, S1Cfg<KIND, D>::MIN_BLOCKS)
+    fd_stage1_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                     const __grid_constant__ Stage1Params p) {
+  using C = S1Cfg<KIND, D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+  uint64_t *empty = full + C::STAGES;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rt = blockIdx.x % p.row_tiles, s = blockIdx.x / p.row_tiles;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int P = p.page_size;
+
+  // ---- split range from cache_seqlens (on the device; no host metadata)
+  int L = p.seqlens[b * p.sl_s];
+  const int cap = p.max_pages * P;
+  if (L < 0 || L > cap) {
+    if (threadIdx.x == 0) atomicOr(p.status, FD_DEVSTAT_SEQLEN_OVERFLOW);
+    L = L < 0 ? 0 : cap;
+  }
+  const int per = (L + p.num_splits - 1) / p.num_splits;
+  const int chunk = ((per + P - 1) >> p.log2_page) << p.log2_page;
+  const int c0 = s * chunk;
+  const int c1 = min(L, c0 + chunk);
+
+  if (c0 >= c1) {  // empty split: zero partial (weight 0 in the merge) or empty final rows
+    const int ntile_rows = min(16, p.R - rt * 16);
+    for (int i = threadIdx.x; i < ntile_rows * (D / 8); i += C::THREADS) {
+      const int r = i / (D / 8), d0 = (i % (D / 8)) * 8;
+      const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      write_row_outputs<C>(p, FUSED, b, h, s, rt * 16 + r, d0, z, 8, -INFINITY, d0 == 0);
+    }
+    griddep_launch_dependents();
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::STAGES; ++i) {
+      mbar_init(&full[i], C::QUANT ? 1 + 32 : 1);
+      mbar_init(&empty[i], C::NUM_CW);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int n_iters = (c1 - c0 + C::BLOCK_N - 1) / C::BLOCK_N;
+
+  if (warp == C::NUM_CW) {
+    // ======================= producer warp =======================
+    if (lane == 0) {
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+    }
+    const uint64_t pol = l2_policy_evict_first();
+    const int *pt = p.page_table + b * p.pt_sb;
+    const int SEG = P < C::BLOCK_N ? P : C::BLOCK_N;  // slots per TMA box
+    const unsigned seg_bytes = static_cast<unsigned>(SEG * C::ROW_BYTES);
+
+    auto load_pids = [&](int it, int &q0, int &q1) {
+      const int tok0 = c0 + it * C::BLOCK_N;
+      const int first = tok0 >> p.log2_page;
+      const int np = ((min(tok0 + C::BLOCK_N, c1) - 1) >> p.log2_page) - first + 1;
+      q0 = lane < np ? pt[first + lane] : 0;
+      q1 = lane + 32 < np ? pt[first + 32 + lane] : 0;
+    };
+    int pn0, pn1;
+    load_pids(0, pn0, pn1);
+    int issued = 0;
+    for (int it = 0; it < n_iters; ++it) {
+      int p0 = pn0, p1 = pn1;
+      if (it + 1 < n_iters) load_pids(it + 1, pn0, pn1);
+      const int tok0 = c0 + it * C::BLOCK_N;
+      const int tend = min(tok0 + C::BLOCK_N, c1);
+      const int first = tok0 >> p.log2_page;
+      const int np = ((tend - 1) >> p.log2_page) - first + 1;
+      // page ids outside the pool: record and redirect past the end (TMA zero-fills)
+      const bool bad0 = lane < np && (p0 < 0 || p0 >= p.num_pages);
+      const bool bad1 = lane + 32 < np && (p1 < 0 || p1 >= p.num_pages);
+      if (__any_sync(0xffffffffu, bad0 || bad1) && lane == 0) atomicOr(p.status, FD_DEVSTAT_BAD_PAGE);
+      if (bad0) p0 = p.num_pages;
+      if (bad1) p1 = p.num_pages;
+
+      const int stage = it % C::STAGES;
+      const unsigned ph = (it / C::STAGES) & 1;
+      if (!mbar_wait_warp(&empty[stage], ph ^ 1, p.status)) break;
+
+      uint8_t *kt = smem + stage * C::STAGE;
+      uint8_t *vt = kt + C::TILE;
+      if (lane == 0) mbar_arrive_expect_tx(&full[stage], static_cast<unsigned>(np) * seg_bytes * 2u);
+      for (int i = 0; i < np; ++i) {
+        const int a0 = __shfl_sync(0xffffffffu, p0, i & 31);
+        const int a1 = __shfl_sync(0xffffffffu, p1, i & 31);
+        if (lane == 0) {
+          const int pid = i < 32 ? a0 : a1;
+          const int slot0 = P > C::BLOCK_N ? (tok0 & (P - 1)) : 0;
+          const int row0 = P > C::BLOCK_N ? 0 : i * P;
+#pragma unroll
+          for (int bx = 0; bx < C::N_BOX; ++bx) {
+            const int off = bx * C::BLOCK_N * C::BOX_BYTES + row0 * C::BOX_BYTES;
+            tma_load_4d(kt + off, &tmk, bx * C::BOX_ELEMS, h, slot0, pid, &full[stage], pol);
+            tma_load_4d(vt + off, &tmv, bx * C::BOX_ELEMS, h, slot0, pid, &full[stage], pol);
+          }
+        }
+      }
+      if constexpr (C::QUANT) {
+        float *ksc = reinterpret_cast<float *>(vt + C::TILE);
+        float *vsc = ksc + C::BLOCK_N * C::NG;
+#pragma unroll
+        for (int i = lane; i < C::BLOCK_N; i += 32) {
+          const int tok = tok0 + i;
+          const int pi = (tok >> p.log2_page) - first;
+          const int a0 = __shfl_sync(0xffffffffu, p0, pi & 31);
+          const int a1 = __shfl_sync(0xffffffffu, p1, pi & 31);
+          const int pid = pi < 32 ? a0 : a1;
+          if (tok < tend && pid < p.num_pages) {
+            const float *src = p.kv_scales + static_cast<int64_t>(pid) * p.sc_sp +
+                               static_cast<int64_t>(tok & (P - 1)) * p.sc_ss +
+                               static_cast<int64_t>(h) * p.sc_sh;
+            cp_async_ca<C::NG * 4>(ksc + i * C::NG, src);
+            cp_async_ca<C::NG * 4>(vsc + i * C::NG, src + p.sc_sk);
+          }
+        }
+        cp_async_mbar_arrive_noinc(&full[stage]);
+      }
+      issued = it + 1;
+    }
+    // drain: the most recent phase of every stage this warp filled has landed
+    if (lane == 0) {
+      for (int k = issued > C::STAGES ? issued - C::STAGES : 0; k < issued; ++k)
+        mbar_wait(&full[k % C::STAGES], (k / C::STAGES) & 1, p.status);
+    }
+  } else {
+    // ======================= consumer warps =======================
+    const int g = lane >> 2;
+    // Q tile (16 rows; rows past R are zero) -> shared -> A fragments
+    uint8_t *qs = smem + C::OFF_Q;
+    for (int i = threadIdx.x; i < 16 * (D / 8); i += C::NUM_CW * 32) {
+      const int r = i / (D / 8), cc = i % (D / 8);
+      const int rg = rt * 16 + r;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (rg < p.R) {
+        const int t = rg / p.G, gq = rg - t * p.G;
+        const __nv_bfloat16 *src = p.q + b * p.q_sb + t * p.q_st + (h * p.G + gq) * p.q_sh + cc * 8;
+        v = *reinterpret_cast<const uint4 *>(src);
+      }
+      *reinterpret_cast<uint4 *>(qs + r * C::QROW + cc * 16) = v;
+    }
+    named_barrier(1, C::NUM_CW * 32);
+    uint32_t qa[D / 16][4];
+    {
+      const int mi = lane >> 3, ri = lane & 7;
+      const int row = ((mi & 1) << 3) + ri;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const int col = ks * 16 + ((mi >> 1) << 3);
+        ldsm_x4(qa[ks], smem_u32(qs + row * C::QROW + col * 2));
+      }
+    }
+    // causal limits of this thread's two rows (g and g + 8)
+    int lim[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int rg = rt * 16 + g + 8 * k;
+      if (rg < p.R) {
+        const int t = rg / p.G;
+        lim[k] = min(c1, L - (p.Tq - 1) + t);
+      } else {
+        lim[k] = c1;
+      }
+    }
+
+    float o[D / 8][4];
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    float m[2] = {-INFINITY, -INFINITY};
+    float l[2] = {0.f, 0.f};
+    const int row0 = warp * 16;
+
+    for (int it = 0; it < n_iters; ++it) {
+      const int stage = it % C::STAGES;
+      const unsigned ph = (it / C::STAGES) & 1;
+      if (!mbar_wait_warp(&full[stage], ph, p.status)) break;
+      const int tok0 = c0 + it * C::BLOCK_N;
+      const int tok_row0 = tok0 + row0;
+      uint8_t *kt = smem + stage * C::STAGE;
+      uint8_t *vt = kt + C::TILE;
+      if (tok_row0 < c1) {
+        if constexpr (C::QUANT) {
+          uint8_t *ks = smem + C::OFF_STG + warp * 2 * C::STG_TILE;
+          uint8_t *vs = ks + C::STG_TILE;
+          stage_rows_bf16<C, KIND>(kt, ks, row0, tok_row0, 0x7fffffff, lane);
+          stage_rows_bf16<C, KIND>(vt, vs, row0, tok_row0, c1, lane);
+          __syncwarp();
+          const float *ksc = reinterpret_cast<const float *>(vt + C::TILE);
+          const float *vsc = ksc + C::BLOCK_N * C::NG;
+          warp_block<C>(smem_u32(ks), smem_u32(vs), C::STG_HALF, 0, ksc, vsc, row0, qa, o, m, l,
+                        tok_row0, lim[0], lim[1], p.scale_log2, lane);
+        } else {
+          if (tok_row0 + 16 > c1) {  // zero V rows past the split end before PV
+            constexpr int CH = C::N_BOX * (C::BOX_BYTES / 16);
+            for (int job = lane; job < 16 * CH; job += 32) {
+              const int r = job / CH, k = job % CH;
+              if (tok_row0 + r >= c1) {
+                const int bx = k / (C::BOX_BYTES / 16), cc = k % (C::BOX_BYTES / 16);
+                *reinterpret_cast<uint4 *>(vt + bx * C::BLOCK_N * C::BOX_BYTES +
+                                           swz<C::BOX_BYTES>((row0 + r) * C::BOX_BYTES + cc * 16)) =
+                    make_uint4(0u, 0u, 0u, 0u);
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          warp_block<C>(smem_u32(kt), smem_u32(vt), C::BLOCK_N * 128, row0, nullptr, nullptr, 0,
+                        qa, o, m, l, tok_row0, lim[0], lim[1], p.scale_log2, lane);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+    }
+
+    // ---- merge the consumer warps' (max, sum, O) through shared memory
+    l[0] += __shfl_xor_sync(0xffffffffu, l[0], 1);
+    l[0] += __shfl_xor_sync(0xffffffffu, l[0], 2);
+    l[1] += __shfl_xor_sync(0xffffffffu, l[1], 1);
+    l[1] += __shfl_xor_sync(0xffffffffu, l[1], 2);
+    named_barrier(1, C::NUM_CW * 32);  // every consumer is done with the ring
+    float *co = reinterpret_cast<float *>(smem);
+    float *cm = reinterpret_cast<float *>(smem + C::CMB_O);
+    float *cl = cm + C::NUM_CW * 16;
+    {
+      const int c = lane & 3;
+      float *w0 = co + (warp * 16 + g) * C::CROW;
+      float *w1 = co + (warp * 16 + g + 8) * C::CROW;
+#pragma unroll
+      for (int j = 0; j < D / 8; ++j) {
+        *reinterpret_cast<float2 *>(w0 + j * 8 + 2 * c) = make_float2(o[j][0], o[j][1]);
+        *reinterpret_cast<float2 *>(w1 + j * 8 + 2 * c) = make_float2(o[j][2], o[j][3]);
+      }
+      if (c == 0) {
+        cm[warp * 16 + g] = m[0];
+        cm[warp * 16 + g + 8] = m[1];
+        cl[warp * 16 + g] = l[0];
+        cl[warp * 16 + g + 8] = l[1];
+      }
+    }
+    named_barrier(1, C::NUM_CW * 32);
+    {
+      constexpr int TPR = (C::NUM_CW * 32) / 16;  // threads per row
+      constexpr int DPT = D / TPR;                // columns per thread
+      const int tid = threadIdx.x;
+      const int row = tid / TPR;
+      const int d0 = (tid % TPR) * DPT;
+      const int rg = rt * 16 + row;
+      float mw[C::NUM_CW], wt[C::NUM_CW];
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < C::NUM_CW; ++w) {
+        mw[w] = cm[w * 16 + row];
+        M = fmaxf(M, mw[w]);
+      }
+      float Lsum = 0.f;
+#pragma unroll
+      for (int w = 0; w < C::NUM_CW; ++w) {
+        wt[w] = mw[w] == -INFINITY ? 0.f : exp2f(mw[w] - M);
+        Lsum = fmaf(wt[w], cl[w * 16 + row], Lsum);
+      }
+      const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+      const float lse_nat = Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
+      float vals[DPT];
+#pragma unroll
+      for (int i = 0; i < DPT; ++i) {
+        float a = 0.f;
+#pragma unroll
+        for (int w = 0; w < C::NUM_CW; ++w) a = fmaf(wt[w], co[(w * 16 + row) * C::CROW + d0 + i], a);
+        vals[i] = a * inv;
+      }
+      if (rg < p.R) write_row_outputs<C>(p, FUSED, b, h, s, rg, d0, vals, DPT, lse_nat, d0 == 0);
+    }
+  }
+  griddep_launch_dependents();
+}
+
+template <int KIND, int D>
+cudaError_t stage1_prepare_t() {
+  using C = S1Cfg<KIND, D>;
+  cudaError_t e = cudaFuncSetAttribute(fd_stage1_kernel<KIND, D, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(fd_stage1_kernel<KIND, D, true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+}
+
+template <int KIND, int D>
+cudaError_t launch_stage1_t(bool fused, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                            const Stage1Params &p, dim3 grid, cudaStream_t stream) {
+  using C = S1Cfg<KIND, D>;
+  if (fused)
+    fd_stage1_kernel<KIND, D, true><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tmk, tmv, p);
+  else
+    fd_stage1_kernel<KIND, D, false><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tmk, tmv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace fd

@@ -1,0 +1,19 @@
+// stage1_i8.cu - stage-1 instantiations for one KV cache format (KV_I8).
+#include "stage1.cuh"
+
+namespace fd {
+
+cudaError_t stage1_prepare_i8(int head_dim) {
+  if (head_dim == 128) return stage1_prepare_t<KV_I8, 128>();
+  if (head_dim == 64) return stage1_prepare_t<KV_I8, 64>();
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_stage1_i8(int head_dim, bool fused, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                           const Stage1Params &p, dim3 grid, cudaStream_t stream) {
+  if (head_dim == 128) return launch_stage1_t<KV_I8, 128>(fused, tmk, tmv, p, grid, stream);
+  if (head_dim == 64) return launch_stage1_t<KV_I8, 64>(fused, tmk, tmv, p, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fd

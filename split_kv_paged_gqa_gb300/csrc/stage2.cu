@@ -1,0 +1,123 @@
+// stage2.cu - merge of the KV splits by log-sum-exp (sm_103a).
+//
+// The stage-2 kernel of "feat(autotune): separate general and decode attention
+// warmup" (LightLLM PR 1549), section "Covered decode kernels" (MTP attention
+// stages 1 and 2; section "Validation": stage-2 inputs reused). For one output
+// row (request, query token, query head) with split partials (o_s, lse_s):
+//   M = max_s lse_s,  w_s = exp(lse_s - M),  out = sum_s w_s o_s / sum_s w_s,
+//   lse = M + ln(sum_s w_s).
+// Splits with lse_s = -inf carry weight 0 and are skipped by selection; a row
+// whose splits are all empty gets out = 0, lse = -inf. One warp per row; the
+// split partials of a row are contiguous (S x D fp32) and read coalesced.
+// Launched with programmatic dependent launch: the grid may start while stage 1
+// drains and waits on griddepcontrol before touching the workspace.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace fd {
+
+constexpr int kS2Warps = 8;
+
+template <int D>
+__global__ void __launch_bounds__(kS2Warps * 32) fd_stage2_kernel(const __grid_constant__ Stage2Params p) {
+  griddep_wait();
+  constexpr int VPL = D / 32;  // values per lane
+  const int row = blockIdx.x * kS2Warps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= p.B * p.Tq * p.Hq) return;
+  const int S = p.num_splits;
+  const float *lp = p.lse_part + static_cast<int64_t>(row) * S;
+  const float l0 = lane < S ? lp[lane] : -INFINITY;
+  const float l1 = lane + 32 < S ? lp[lane + 32] : -INFINITY;
+  float M = fmaxf(l0, l1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float w0 = (l0 == -INFINITY) ? 0.f : expf(l0 - M);
+  const float w1 = (l1 == -INFINITY) ? 0.f : expf(l1 - M);
+  float Z = w0 + w1;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
+
+  float acc[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) acc[i] = 0.f;
+  const float *op = p.o_part + static_cast<int64_t>(row) * S * D + lane * VPL;
+  for (int s = 0; s < S; ++s) {
+    const float wa = __shfl_sync(0xffffffffu, w0, s & 31);
+    const float wb = __shfl_sync(0xffffffffu, w1, s & 31);
+    const float w = s < 32 ? wa : wb;
+    if (w > 0.f) {
+      if constexpr (VPL == 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(op + s * D);
+        acc[0] = fmaf(w, v.x, acc[0]);
+        acc[1] = fmaf(w, v.y, acc[1]);
+        acc[2] = fmaf(w, v.z, acc[2]);
+        acc[3] = fmaf(w, v.w, acc[3]);
+      } else {
+        const float2 v = *reinterpret_cast<const float2 *>(op + s * D);
+        acc[0] = fmaf(w, v.x, acc[0]);
+        acc[1] = fmaf(w, v.y, acc[1]);
+      }
+    }
+  }
+  const float inv = Z > 0.f ? 1.f / Z : 0.f;
+  const int hq = row % p.Hq;
+  const int t = (row / p.Hq) % p.Tq;
+  const int b = row / (p.Hq * p.Tq);
+  const int64_t base = b * p.o_sb + t * p.o_st + hq * p.o_sh + lane * VPL;
+  if (p.out_f32) {
+    float *dst = reinterpret_cast<float *>(p.out) + base;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) dst[i] = acc[i] * inv;
+  } else {
+    __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + base;
+#pragma unroll
+    for (int i = 0; i < VPL; i += 2)
+      *reinterpret_cast<uint32_t *>(dst + i) = pack_bf16x2(acc[i] * inv, acc[i + 1] * inv);
+  }
+  if (lane == 0 && p.lse) p.lse[b * p.l_sb + t * p.l_st + hq * p.l_sh] = Z > 0.f ? M + logf(Z) : -INFINITY;
+}
+
+cudaError_t launch_stage2(const Stage2Params &p, cudaStream_t stream, bool pdl) {
+  const int rows = p.B * p.Tq * p.Hq;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((rows + kS2Warps - 1) / kS2Warps);
+  cfg.blockDim = dim3(kS2Warps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (p.D == 128) return cudaLaunchKernelEx(&cfg, fd_stage2_kernel<128>, p);
+  if (p.D == 64) return cudaLaunchKernelEx(&cfg, fd_stage2_kernel<64>, p);
+  return cudaErrorInvalidValue;
+}
+
+int stage1_block_n(int, int) { return 64; }
+
+cudaError_t stage1_prepare(int kind, int head_dim) {
+  switch (kind) {
+    case KV_BF16: return stage1_prepare_bf16(head_dim);
+    case KV_I8: return stage1_prepare_i8(head_dim);
+    case KV_I4: return stage1_prepare_i4(head_dim);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_stage1(int kind, int head_dim, bool fused, const CUtensorMap &tmk,
+                          const CUtensorMap &tmv, const Stage1Params &p, dim3 grid,
+                          cudaStream_t stream) {
+  switch (kind) {
+    case KV_BF16: return launch_stage1_bf16(head_dim, fused, tmk, tmv, p, grid, stream);
+    case KV_I8: return launch_stage1_i8(head_dim, fused, tmk, tmv, p, grid, stream);
+    case KV_I4: return launch_stage1_i4(head_dim, fused, tmk, tmv, p, grid, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fd

@@ -1,0 +1,78 @@
+"""Helpers shared by the GPU parity tests (calls go through the C ABI binding)."""
+import numpy as np
+import torch
+
+import split_kv_paged_gqa_gb300 as fd
+from split_kv_paged_gqa_gb300 import workloads as wl
+
+# Parity bar for this operation: max |err| on bf16 out and on fp32 LSE, and
+# the agreement required between different num_splits.
+OUT_ATOL = 8e-3
+LSE_ATOL = 1e-3
+SPLIT_ATOL = 2e-3
+# Tighter gates that a dropped page cannot pass at long context.
+LSE_TIGHT = 1e-4
+REL_ROW = 1e-2       # max|err| <= REL_ROW * max|ref| per (request, token, head) row
+REL_L2 = 5e-3        # ||err||_2 / ||ref||_2 over the whole output
+
+_PLANS = {}
+
+
+def plan_for(shape: wl.DecodeShape, max_batch=None, max_splits=64):
+    key = (shape.num_q_heads, shape.num_kv_heads, shape.head_dim, shape.page_size, shape.kv_dtype,
+           max_batch or shape.batch, shape.q_per_req, max_splits)
+    if key not in _PLANS:
+        _PLANS[key] = fd.fd_plan_create(0, max_batch or shape.batch, shape.q_per_req, shape.num_q_heads,
+                                        shape.num_kv_heads, shape.head_dim, shape.page_size, shape.kv_dtype,
+                                        max_splits)
+    return _PLANS[key]
+
+
+def run(w: wl.Workload, num_splits: int, out_dtype=torch.bfloat16, plan=None, stream=None):
+    plan = plan or plan_for(w.shape)
+    fd.fd_set_plan(plan)
+    out = torch.empty(w.q.shape, dtype=out_dtype, device=w.q.device)
+    lse = torch.empty(w.q.shape[:3], dtype=torch.float32, device=w.q.device)
+    fd.fd_decode_paged(w.q, w.k_cache, w.v_cache, w.kv_scales, w.page_table, w.cache_seqlens,
+                       w.shape.q_per_req, num_splits, out, lse, stream)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def assert_parity(out, lse, ref_out, ref_lse, requests=None, tight=True, label=""):
+    o = out.float().cpu().numpy()
+    l = lse.cpu().numpy()
+    if requests is not None:
+        o, l = o[requests], l[requests]
+    assert np.array_equal(np.isneginf(l), np.isneginf(ref_lse)), f"{label}: -inf LSE pattern differs"
+    fin = np.isfinite(ref_lse)
+    err = np.abs(o - ref_out)
+    assert np.all(np.isfinite(o)), f"{label}: non-finite output"
+    assert err.max() <= OUT_ATOL, f"{label}: max|out err| {err.max():.3e} > {OUT_ATOL}"
+    lerr = np.abs(l[fin] - ref_lse[fin]).max() if fin.any() else 0.0
+    assert lerr <= LSE_ATOL, f"{label}: max|lse err| {lerr:.3e} > {LSE_ATOL}"
+    if tight:
+        assert lerr <= LSE_TIGHT, f"{label}: max|lse err| {lerr:.3e} > {LSE_TIGHT}"
+        row_ref = np.abs(ref_out).max(axis=-1)
+        row_err = err.max(axis=-1)
+        bad = row_err > REL_ROW * np.maximum(row_ref, 1e-6) + 2e-5
+        assert not bad.any(), f"{label}: {bad.sum()} rows fail the per-row relative gate"
+        nrm = np.linalg.norm(ref_out)
+        if nrm > 0:
+            assert np.linalg.norm(o - ref_out) / nrm <= REL_L2, f"{label}: relative L2 error too large"
+    return float(err.max()), float(lerr)
+
+
+def assert_needles(w: wl.Workload, out, inp):
+    """Needle rows must return the needle's V row (to bf16 rounding)."""
+    from oracle import gather_kv
+    sc = inp["kv_scales"]
+    G = w.shape.group
+    o = out.float().cpu().numpy()
+    for b, h, j in w.needles:
+        L = int(inp["cache_seqlens"][b])
+        V = gather_kv(inp["v_cache"], None if sc is None else sc[1], inp["page_table"][b], L,
+                      w.shape.page_size, w.shape.kv_dtype)
+        got = o[b, w.shape.q_per_req - 1, h * G]
+        np.testing.assert_allclose(got, V[j, h], rtol=2 ** -7, atol=1e-4,
+                                   err_msg=f"needle request {b} head {h} key {j}")

@@ -1,0 +1,230 @@
+"""GPU parity of the CUDA path (through the C ABI) against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import split_kv_paged_gqa_gb300 as fd
+from oracle import decode_ref_inputs
+from split_kv_paged_gqa_gb300 import workloads as wl
+from tests.gpu_common import (OUT_ATOL, SPLIT_ATOL, assert_needles, assert_parity, plan_for, run)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _shape(kind, B, Tq, Hq, Hkv, D, P, lengths):
+    return wl.DecodeShape("case", B, Hq, Hkv, D, P, Tq, kind, "fixed:" + ",".join(map(str, lengths)))
+
+
+# ---------------------------------------------------------------------------
+# the tiny workload, both split counts, bf16 and fp32 outputs
+
+
+@pytest.mark.parametrize("S", [1, 4])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_tiny_bf16(S, out_dtype):
+    shape = wl.CONFIGS["tiny_bf16"]
+    w = wl.make_workload(shape, wl.CONFIG_SEEDS["tiny_bf16"], "cuda", poison=True)
+    ref_out, ref_lse = decode_ref_inputs(wl.oracle_inputs(w))
+    out, lse = run(w, S, out_dtype)
+    assert_parity(out, lse, ref_out, ref_lse, label=f"tiny S={S}")
+
+
+# ---------------------------------------------------------------------------
+# several tiles, ragged tails, every cache format, GQA groups, MTP, page sizes
+
+CASES = [
+    # kind, B, Tq, Hq, Hkv, D, P, lengths
+    ("bf16", 3, 1, 8, 2, 64, 16, (1, 300, 1023)),
+    ("bf16", 2, 1, 40, 8, 128, 16, (777, 2050)),
+    ("bf16", 2, 1, 64, 8, 128, 64, (4096, 1000)),
+    ("bf16", 2, 4, 32, 8, 128, 16, (517, 1290)),
+    ("bf16", 2, 1, 16, 1, 128, 256, (600, 129)),        # G=16, sub-page stages
+    ("bf16", 2, 4, 32, 4, 128, 32, (99, 400)),          # R = 32 rows: two row tiles
+    ("bf16", 2, 1, 4, 4, 64, 8, (70, 3)),               # smallest page size
+    ("bf16", 2, 2, 12, 2, 64, 8, (45, 200)),
+    ("int8", 3, 1, 32, 8, 128, 16, (16, 900, 2500)),
+    ("int8", 2, 1, 8, 2, 64, 64, (300, 130)),
+    ("int8", 2, 4, 32, 8, 128, 16, (1000, 67)),
+    ("int4", 2, 4, 32, 8, 128, 16, (4096, 1111)),
+    ("int4", 3, 1, 8, 2, 128, 64, (70, 640, 2000)),
+    ("int4", 2, 1, 16, 4, 64, 16, (333, 48)),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-B{c[1]}-T{c[2]}-H{c[3]}/{c[4]}-D{c[5]}-P{c[6]}")
+@pytest.mark.parametrize("S", [1, 3, 8])
+def test_parity_cases(case, S):
+    shape = _shape(*case)
+    w = wl.make_workload(shape, 100 + CASES.index(case), "cuda", poison=True, needles=True, extra_pages=3)
+    inp = wl.oracle_inputs(w)
+    ref_out, ref_lse = decode_ref_inputs(inp)
+    out, lse = run(w, S)
+    assert_parity(out, lse, ref_out, ref_lse, label=f"{case} S={S}")
+    assert_needles(w, out, inp)
+
+
+# ---------------------------------------------------------------------------
+# results for different num_splits agree
+
+
+@pytest.mark.parametrize("kind", ["bf16", "int8", "int4"])
+def test_cross_split_agreement(kind):
+    shape = _shape(kind, 3, 1, 32, 8, 128, 16, (3000, 5000, 129))
+    w = wl.make_workload(shape, 7, "cuda", poison=True)
+    base_f, base_l = run(w, 1, torch.float32)
+    base_b, _ = run(w, 1, torch.bfloat16)
+    for S in (2, 4, 8, 16, 32, 64):
+        of, lf = run(w, S, torch.float32)
+        assert (of - base_f).abs().max().item() <= SPLIT_ATOL, f"fp32 out S={S}"
+        assert (lf - base_l).abs().max().item() <= SPLIT_ATOL, f"lse S={S}"
+        ob, _ = run(w, S, torch.bfloat16)
+        d = (ob.float() - base_b.float()).abs()
+        ulp = torch.where(base_b.float().abs() >= 0.5, 2.0 ** -7, 0.0)   # one bf16 rounding flip
+        assert (d <= SPLIT_ATOL + ulp).all(), f"bf16 out S={S}: {d.max().item()}"
+
+
+# ---------------------------------------------------------------------------
+# edge cases
+
+
+def test_rows_without_keys():
+    # L = 0 and L < Tq: rows with no visible key get out = 0, lse = -inf
+    shape = _shape("bf16", 3, 4, 8, 2, 64, 16, (0, 2, 17))
+    w = wl.make_workload(shape, 3, "cuda", poison=True, capacity_pages=2)
+    ref_out, ref_lse = decode_ref_inputs(wl.oracle_inputs(w))
+    for S in (1, 4):
+        out, lse = run(w, S)
+        assert_parity(out, lse, ref_out, ref_lse, label=f"empty S={S}")
+        assert torch.isneginf(lse[0]).all() and (out[0] == 0).all()
+
+
+def test_more_splits_than_pages():
+    shape = _shape("bf16", 2, 1, 8, 2, 64, 16, (20, 33))
+    w = wl.make_workload(shape, 5, "cuda", poison=True)
+    ref_out, ref_lse = decode_ref_inputs(wl.oracle_inputs(w))
+    out, lse = run(w, 64)
+    assert_parity(out, lse, ref_out, ref_lse, label="S=64 on 2-3 pages")
+
+
+def test_strided_outputs_and_queries():
+    shape = _shape("bf16", 2, 1, 16, 4, 128, 16, (500, 901))
+    w = wl.make_workload(shape, 9, "cuda")
+    ref_out, ref_lse = decode_ref_inputs(wl.oracle_inputs(w))
+    big_q = torch.zeros((2, 1, 16, 256), dtype=torch.bfloat16, device="cuda")
+    big_q[..., 64:192] = w.q
+    q_view = big_q[..., 64:192]                      # non-contiguous query rows
+    out_big = torch.full((2, 1, 16, 136), 7.0, dtype=torch.bfloat16, device="cuda")
+    out_view = out_big[..., :128]
+    lse_big = torch.zeros((2, 1, 16, 2), dtype=torch.float32, device="cuda")
+    lse_view = lse_big[..., 0]
+    fd.fd_set_plan(plan_for(shape))
+    for S in (1, 4):
+        fd.fd_decode_paged(q_view, w.k_cache, w.v_cache, None, w.page_table, w.cache_seqlens, 1, S,
+                           out_view, lse_view)
+        torch.cuda.synchronize()
+        assert_parity(out_view, lse_view, ref_out, ref_lse, label=f"strided S={S}")
+        assert (out_big[..., 128:] == 7.0).all()       # padding untouched
+
+
+def test_deterministic():
+    shape = _shape("int4", 2, 4, 32, 8, 128, 16, (3000, 1700))
+    w = wl.make_workload(shape, 13, "cuda")
+    a, la = run(w, 8)
+    for _ in range(5):
+        b, lb = run(w, 8)
+        assert torch.equal(a, b) and torch.equal(la, lb)
+
+
+# ---------------------------------------------------------------------------
+# bad metadata is reported, not faulted on
+
+
+def test_bad_page_id_sets_status():
+    shape = _shape("bf16", 2, 1, 8, 2, 64, 16, (100, 40))
+    w = wl.make_workload(shape, 21, "cuda")
+    plan = plan_for(shape)
+    fd.fd_read_device_status(plan)                     # clear
+    pt = w.page_table.clone()
+    pt[0, 2] = w.k_cache.shape[0] + 5                   # outside the pool
+    w.page_table = pt
+    out, lse = run(w, 2)
+    assert fd.fd_read_device_status(plan) & fd.FD_DEVSTAT_BAD_PAGE
+    assert fd.fd_read_device_status(plan) == 0          # reading cleared it
+    assert torch.isfinite(out.float()).all()
+
+
+def test_seqlen_over_capacity_sets_status():
+    shape = _shape("bf16", 2, 1, 8, 2, 64, 16, (100, 40))
+    w = wl.make_workload(shape, 22, "cuda")
+    plan = plan_for(shape)
+    fd.fd_read_device_status(plan)
+    w.cache_seqlens = torch.tensor([100, 40 + 10 * 16 * 7], dtype=torch.int32, device="cuda")
+    run(w, 1)
+    assert fd.fd_read_device_status(plan) & fd.FD_DEVSTAT_SEQLEN_OVERFLOW
+
+
+# ---------------------------------------------------------------------------
+# CUDA graph capture and replay with new metadata contents
+
+
+def test_graph_capture_replay_picks_up_new_metadata():
+    shape = _shape("bf16", 2, 1, 16, 4, 128, 16, (700, 1500))
+    w = wl.make_workload(shape, 31, "cuda", extra_pages=200, capacity_pages=110)
+    plan = plan_for(shape)
+    fd.fd_set_plan(plan)
+    out = torch.empty_like(w.q)
+    lse = torch.empty(w.q.shape[:3], dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):            # warm-up outside capture
+        fd.fd_decode_paged(w.q, w.k_cache, w.v_cache, None, w.page_table, w.cache_seqlens, 1, 4, out, lse)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fd.fd_decode_paged(w.q, w.k_cache, w.v_cache, None, w.page_table, w.cache_seqlens, 1, 4, out, lse)
+    rng = np.random.default_rng(4)
+    for trial in range(3):
+        lens = rng.integers(1, 1600, size=2)
+        n_pages = w.k_cache.shape[0]
+        new_pt = torch.full_like(w.page_table, -1)
+        for b in range(2):
+            need = -(-int(lens[b]) // 16)
+            new_pt[b, :need] = torch.from_numpy(rng.choice(n_pages, need, replace=False).astype(np.int32))
+        w.page_table.copy_(new_pt)
+        w.cache_seqlens.copy_(torch.from_numpy(lens.astype(np.int32)))
+        w.lengths = lens
+        g.replay()
+        torch.cuda.synchronize()
+        ref_out, ref_lse = decode_ref_inputs(wl.oracle_inputs(w))
+        assert_parity(out, lse, ref_out, ref_lse, label=f"graph replay {trial}")
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, in the launch configuration the bench times, on sampled requests
+
+
+FULL = ["mixed_bf16", "long_bf16_b64", "int8_lognormal", "int4_mtp"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(name):
+    shape = wl.CONFIGS[name]
+    w = wl.make_workload(shape, wl.CONFIG_SEEDS[name], "cuda")
+    plan = plan_for(shape, max_splits=64)
+    fd.fd_set_max_seqlen_hint(plan, int(w.lengths.max()))
+    out, lse = run(w, 0, plan=plan)                    # num_splits from the plan (bench setting)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    rng = np.random.default_rng(0)
+    sample = sorted(set([int(np.argmax(w.lengths)), int(np.argmin(w.lengths))] +
+                        rng.choice(shape.batch, 2, replace=False).tolist()))
+    inp = wl.oracle_inputs(w, requests=sample)
+    ref_out, ref_lse = decode_ref_inputs(inp)
+    assert_parity(out, lse, ref_out, ref_lse, requests=sample, label=name)
+    del w
+    torch.cuda.empty_cache()
