@@ -17,7 +17,8 @@ __all__ = [
     "FdError", "load_library", "fd_plan_create", "fd_plan_destroy", "fd_set_plan", "fd_get_plan",
     "fd_decode_paged", "fd_set_max_seqlen_hint", "fd_autotune", "fd_query_splits",
     "fd_autotune_set_timer", "fd_autotune_set_cache_dir", "fd_autotune_stats",
-    "fd_read_device_status", "fd_plan_workspace_bytes", "fd_status_string", "fd_last_error",
+    "fd_read_device_status", "fd_plan_workspace_bytes", "fd_profile_begin", "fd_profile_end",
+    "fd_status_string", "fd_last_error",
     "FD_OK", "FD_ERR_INVALID_ARG", "FD_ERR_UNSUPPORTED", "FD_ERR_WORKSPACE", "FD_ERR_CAPTURING",
     "FD_ERR_CUDA", "FD_ERR_DEVICE_STATUS", "FD_ERR_TIMEOUT", "FD_ERR_NO_PLAN", "FD_ERR_IO",
     "FD_BF16", "FD_FP32", "FD_INT8", "FD_INT4X2", "FD_INT32",
@@ -81,6 +82,9 @@ def load_library(path: Optional[str] = None):
         "fd_autotune_stats": (I, [P, ctypes.POINTER(I), ctypes.POINTER(I)]),
         "fd_read_device_status": (I, [P, ctypes.POINTER(I)]),
         "fd_plan_workspace_bytes": (I, [P, ctypes.POINTER(ctypes.c_size_t)]),
+        "fd_profile_begin": (I, [P]),
+        "fd_profile_end": (I, [P, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double),
+                               ctypes.POINTER(ctypes.c_double)]),
         "fd_status_string": (ctypes.c_char_p, [I]),
         "fd_last_error": (ctypes.c_char_p, []),
     }
@@ -239,3 +243,14 @@ def fd_plan_workspace_bytes(plan: int) -> int:
     v = ctypes.c_size_t()
     _check(load_library().fd_plan_workspace_bytes(plan, ctypes.byref(v)))
     return v.value
+
+
+def fd_profile_begin(plan: int) -> None:
+    _check(load_library().fd_profile_begin(plan))
+
+
+def fd_profile_end(plan: int) -> Tuple[int, float, float]:
+    """(calls, summed stage-1 ms, summed stage-2 ms) since fd_profile_begin."""
+    n, a, b = ctypes.c_int(), ctypes.c_double(), ctypes.c_double()
+    _check(load_library().fd_profile_end(plan, ctypes.byref(n), ctypes.byref(a), ctypes.byref(b)))
+    return n.value, a.value, b.value

@@ -236,7 +236,7 @@ fd_status fd_read_device_status(fd_plan *plan, int *code) {
 
 namespace {
 
-fd_status check_tensor(const fd_tensor *t, const char *name, int ndim) {
+fd_status check_tensor(const fd_tensor *t, const char *name, int ndim, bool unit_inner = true) {
   if (!t) return fail(FD_ERR_INVALID_ARG, "%s descriptor is NULL", name);
   if (!t->data) return fail(FD_ERR_INVALID_ARG, "%s data pointer is NULL", name);
   if (t->ndim != ndim) return fail(FD_ERR_INVALID_ARG, "%s has ndim %d, expected %d", name, t->ndim, ndim);
@@ -244,7 +244,7 @@ fd_status check_tensor(const fd_tensor *t, const char *name, int ndim) {
     if (t->shape[i] < 0) return fail(FD_ERR_INVALID_ARG, "%s shape[%d] < 0", name, i);
     if (t->stride[i] < 0) return fail(FD_ERR_UNSUPPORTED, "%s stride[%d] < 0", name, i);
   }
-  if (t->stride[ndim - 1] != 1 && t->shape[ndim - 1] > 1)
+  if (unit_inner && t->stride[ndim - 1] != 1 && t->shape[ndim - 1] > 1)
     return fail(FD_ERR_UNSUPPORTED, "%s innermost stride must be 1", name);
   return FD_OK;
 }
@@ -361,7 +361,7 @@ extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cach
       return fail(FD_ERR_UNSUPPORTED, "out rows must be 16-byte aligned");
   }
   if (lse && lse->data) {
-    FD_TRY(check_tensor(lse, "lse", 3));
+    FD_TRY(check_tensor(lse, "lse", 3, false));
     if (lse->dtype != FD_FP32 || lse->shape[0] != B || lse->shape[1] != Tq || lse->shape[2] != pl->hq)
       return fail(FD_ERR_INVALID_ARG, "lse must be fp32 [B, Tq, Hq]");
   }
@@ -425,8 +425,15 @@ extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cach
   p.status = pl->status;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+  if (pl->profiling) {
+    for (auto &x : ev) FD_CUDA_TRY(cudaEventCreate(&x));
+    for (auto &x : ev) pl->prof_events.push_back(x);
+    FD_CUDA_TRY(cudaEventRecord(ev[0], st));
+  }
   dim3 grid(p.row_tiles * S, pl->hkv, B);
   cudaError_t e = fd::launch_stage1(pl->kind, D, S == 1, tmk, tmv, p, grid, st);
+  if (pl->profiling) FD_CUDA_TRY(cudaEventRecord(ev[1], st));
   if (e != cudaSuccess) return fail(FD_ERR_CUDA, "stage-1 launch failed: %s (%d)", cudaGetErrorString(e), (int)e);
   if (S > 1) {
     fd::Stage2Params p2;
@@ -446,8 +453,40 @@ extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cach
     p2.l_sb = p.l_sb;
     p2.l_st = p.l_st;
     p2.l_sh = p.l_sh;
-    e = fd::launch_stage2(p2, st, true);
+    e = fd::launch_stage2(p2, st, !pl->profiling);
     if (e != cudaSuccess) return fail(FD_ERR_CUDA, "stage-2 launch failed: %s (%d)", cudaGetErrorString(e), (int)e);
   }
+  if (pl->profiling) FD_CUDA_TRY(cudaEventRecord(ev[2], st));
   return FD_OK;
+}
+
+extern "C" fd_status fd_profile_begin(fd_plan *plan) {
+  if (!plan) return fail(FD_ERR_INVALID_ARG, "plan is NULL");
+  if (plan->device < 0) return fail(FD_ERR_WORKSPACE, "host-only plan cannot profile");
+  plan->profiling = true;
+  return FD_OK;
+}
+
+extern "C" fd_status fd_profile_end(fd_plan *plan, int *calls, double *stage1_ms, double *stage2_ms) {
+  if (!plan) return fail(FD_ERR_INVALID_ARG, "plan is NULL");
+  fd::DeviceGuard guard(plan->device);
+  plan->profiling = false;
+  double t1 = 0.0, t2 = 0.0;
+  fd_status st = FD_OK;
+  const size_t n = plan->prof_events.size() / 3;
+  for (size_t i = 0; i < n; ++i) {
+    cudaEvent_t *e = &plan->prof_events[3 * i];
+    float a = 0.f, b = 0.f;
+    if (st == FD_OK && (cudaEventSynchronize(e[2]) != cudaSuccess || cudaEventElapsedTime(&a, e[0], e[1]) != cudaSuccess ||
+                        cudaEventElapsedTime(&b, e[1], e[2]) != cudaSuccess))
+      st = fail(FD_ERR_CUDA, "profiling events failed");
+    t1 += a;
+    t2 += b;
+  }
+  for (cudaEvent_t e : plan->prof_events) cudaEventDestroy(e);
+  plan->prof_events.clear();
+  if (calls) *calls = static_cast<int>(n);
+  if (stage1_ms) *stage1_ms = t1;
+  if (stage2_ms) *stage2_ms = t2;
+  return st;
 }

@@ -6,6 +6,7 @@
 #include <map>
 #include <string>
 #include <utility>
+#include <vector>
 
 #include "fd.h"
 
@@ -36,6 +37,10 @@ struct fd_plan {
   fd_timer_fn timer = nullptr;
   void *timer_user = nullptr;
   int searches = 0, cache_hits = 0;
+
+  // per-stage timing events (fd_profile_begin / fd_profile_end)
+  bool profiling = false;
+  std::vector<cudaEvent_t> prof_events;  // 3 per call: start, after stage 1, after stage 2
 };
 
 namespace fd {

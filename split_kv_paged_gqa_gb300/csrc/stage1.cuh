@@ -17,13 +17,14 @@
 //    completing on a per-stage mbarrier. Quantised caches also copy their
 //    per-row fp32 scales with cp.async (one arrival per lane on the barrier).
 //  * consumer warps: warp w takes keys [16w, 16w + 16) of each 64-key stage.
-//    Quantised rows are first converted to bf16 in a per-warp staging tile
-//    (int8 / int4 codes are exact in bf16). QK^T and PV run on mma.sync
-//    m16n8k16 (bf16 in, fp32 accumulate) with the 16 query rows as M; the
-//    online softmax keeps a running max / sum per row in the log2 domain with
-//    quad shuffles. K scales multiply the fp32 scores (per 32-channel group
-//    for int4, from separate per-group accumulators); V scales are folded into
-//    the probabilities before they are rounded to bf16 for PV.
+//    Quantised rows are first converted in a per-warp staging tile, K codes
+//    to bf16 and V codes to fp16 (both exact). QK^T and PV run on mma.sync
+//    m16n8k16 (fp32 accumulate) with the 16 query rows as M; the online
+//    softmax keeps a running max / sum per row in the log2 domain with quad
+//    shuffles. K scales multiply the fp32 scores (per 32-channel group for
+//    int4, from separate per-group accumulators); V scales are folded into the
+//    probabilities, which are then rounded to fp16 (11-bit mantissa) for an
+//    fp16 PV product; the bf16 cache path rounds probabilities to bf16.
 //  * epilogue: the consumer warps merge their (max, sum, O) through shared
 //    memory and write either fp32 partial O + LSE to the split workspace, or
 //    (num_splits == 1) the final bf16/fp32 output and LSE.
@@ -105,13 +106,34 @@ __device__ __forceinline__ uint32_t i4x2_to_bf16(uint32_t biased_byte) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Four int8 codes -> two f16x2 words. A biased byte u = code + 128 in the low
+// mantissa bits of fp16 1024.0 gives 1024 + u exactly; subtracting 1152
+// yields code.
+__device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  const uint32_t x = w ^ 0x80808080u;
+  uint32_t a = __byte_perm(x, 0x64646464u, 0x5140);
+  uint32_t b = __byte_perm(x, 0x64646464u, 0x7362);
+  const __half2 bias = __floats2half2_rn(1152.0f, 1152.0f);
+  __half2 ha = __hsub2(*reinterpret_cast<__half2 *>(&a), bias);
+  __half2 hb = __hsub2(*reinterpret_cast<__half2 *>(&b), bias);
+  lo = *reinterpret_cast<uint32_t *>(&ha);
+  hi = *reinterpret_cast<uint32_t *>(&hb);
+}
+
+// One byte of two int4 codes -> one f16x2 word (fp16 1024 + u, minus 1032).
+__device__ __forceinline__ uint32_t i4x2_to_f16(uint32_t biased_byte) {
+  uint32_t r = 0x64006400u | (biased_byte & 0xFu) | ((biased_byte & 0xF0u) << 12);
+  __half2 v = __hsub2(*reinterpret_cast<__half2 *>(&r), __floats2half2_rn(1032.0f, 1032.0f));
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
 // Convert this warp's 16 cache rows (tile rows row0..row0+15 of a raw stage
-// tile) into a bf16 staging tile laid out like a bf16 TMA tile (64-element
-// halves of 16 rows x 128 bytes, 128-byte swizzled). Rows whose token index is
-// >= zero_from are written as zeros.
-template <class C, int KIND>
-__device__ __forceinline__ void stage_rows_bf16(const uint8_t *raw, uint8_t *stg, int row0,
-                                                int tok_row0, int zero_from, int lane) {
+// tile) into a 16-bit staging tile (bf16, or fp16 when F16) laid out like a
+// bf16 TMA tile (64-element halves of 16 rows x 128 bytes, 128-byte
+// swizzled). Rows whose token index is >= zero_from are written as zeros.
+template <class C, int KIND, bool F16>
+__device__ __forceinline__ void stage_rows(const uint8_t *raw, uint8_t *stg, int row0, int tok_row0,
+                                           int zero_from, int lane) {
   constexpr int CHUNKS = C::ROW_BYTES / 16;     // 16-byte chunks per raw row
   constexpr int JOBS = 16 * CHUNKS;
   constexpr int VALS = KIND == KV_I8 ? 16 : 32;  // codes per raw chunk
@@ -122,18 +144,25 @@ __device__ __forceinline__ void stage_rows_bf16(const uint8_t *raw, uint8_t *stg
     const uint4 src = *reinterpret_cast<const uint4 *>(raw + roff);
     const bool zero = tok_row0 + r >= zero_from;
     uint32_t out[VALS / 2];
-    if (KIND == KV_I8) {
-      i8x4_to_bf16(src.x, out[0], out[1]);
-      i8x4_to_bf16(src.y, out[2], out[3]);
-      i8x4_to_bf16(src.z, out[4], out[5]);
-      i8x4_to_bf16(src.w, out[6], out[7]);
+    if constexpr (KIND == KV_I8) {
+      const uint32_t w[4] = {src.x, src.y, src.z, src.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if constexpr (F16)
+          i8x4_to_f16(w[k], out[2 * k], out[2 * k + 1]);
+        else
+          i8x4_to_bf16(w[k], out[2 * k], out[2 * k + 1]);
+      }
     } else {
       const uint32_t w[4] = {src.x ^ 0x88888888u, src.y ^ 0x88888888u, src.z ^ 0x88888888u,
                              src.w ^ 0x88888888u};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
 #pragma unroll
-        for (int bi = 0; bi < 4; ++bi) out[k * 4 + bi] = i4x2_to_bf16((w[k] >> (8 * bi)) & 0xFFu);
+        for (int bi = 0; bi < 4; ++bi) {
+          const uint32_t byte = (w[k] >> (8 * bi)) & 0xFFu;
+          out[k * 4 + bi] = F16 ? i4x2_to_f16(byte) : i4x2_to_bf16(byte);
+        }
       }
     }
     const int d0 = cc * VALS;
@@ -262,10 +291,17 @@ __device__ __forceinline__ void warp_block(uint32_t kbase, uint32_t vbase, uint3
         }
       }
     }
-    pa[gv][0] = pack_bf16x2(pv[0][0], pv[0][1]);
-    pa[gv][1] = pack_bf16x2(pv[0][2], pv[0][3]);
-    pa[gv][2] = pack_bf16x2(pv[1][0], pv[1][1]);
-    pa[gv][3] = pack_bf16x2(pv[1][2], pv[1][3]);
+    if constexpr (C::QUANT) {
+      pa[gv][0] = pack_f16x2(pv[0][0], pv[0][1]);
+      pa[gv][1] = pack_f16x2(pv[0][2], pv[0][3]);
+      pa[gv][2] = pack_f16x2(pv[1][0], pv[1][1]);
+      pa[gv][3] = pack_f16x2(pv[1][2], pv[1][3]);
+    } else {
+      pa[gv][0] = pack_bf16x2(pv[0][0], pv[0][1]);
+      pa[gv][1] = pack_bf16x2(pv[0][2], pv[0][3]);
+      pa[gv][2] = pack_bf16x2(pv[1][0], pv[1][1]);
+      pa[gv][3] = pack_bf16x2(pv[1][2], pv[1][3]);
+    }
   }
 
   // ---- O += P V
@@ -276,8 +312,13 @@ __device__ __forceinline__ void warp_block(uint32_t kbase, uint32_t vbase, uint3
     uint32_t bv[4];
     ldsm_x4_t(bv, vbase + (d >> 6) * half + swz<128>(vrow * 128 + (d & 63) * 2));
     const int gv = NGV == 1 ? 0 : dp / 2;
-    mma_bf16_16816(o[2 * dp], pa[gv], bv[0], bv[1]);
-    mma_bf16_16816(o[2 * dp + 1], pa[gv], bv[2], bv[3]);
+    if constexpr (C::QUANT) {
+      mma_f16_16816(o[2 * dp], pa[gv], bv[0], bv[1]);
+      mma_f16_16816(o[2 * dp + 1], pa[gv], bv[2], bv[3]);
+    } else {
+      mma_bf16_16816(o[2 * dp], pa[gv], bv[0], bv[1]);
+      mma_bf16_16816(o[2 * dp + 1], pa[gv], bv[2], bv[3]);
+    }
   }
 }
 
@@ -509,8 +550,8 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D>::THREADS, S1Cfg<KIND, D>::MIN_B
         if constexpr (C::QUANT) {
           uint8_t *ks = smem + C::OFF_STG + warp * 2 * C::STG_TILE;
           uint8_t *vs = ks + C::STG_TILE;
-          stage_rows_bf16<C, KIND>(kt, ks, row0, tok_row0, 0x7fffffff, lane);
-          stage_rows_bf16<C, KIND>(vt, vs, row0, tok_row0, c1, lane);
+          stage_rows<C, KIND, false>(kt, ks, row0, tok_row0, 0x7fffffff, lane);
+          stage_rows<C, KIND, true>(vt, vs, row0, tok_row0, c1, lane);
           __syncwarp();
           const float *ksc = reinterpret_cast<const float *>(vt + C::TILE);
           const float *vsc = ksc + C::BLOCK_N * C::NG;

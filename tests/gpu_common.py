@@ -39,7 +39,19 @@ def run(w: wl.Workload, num_splits: int, out_dtype=torch.bfloat16, plan=None, st
     return out, lse
 
 
-def assert_parity(out, lse, ref_out, ref_lse, requests=None, tight=True, label=""):
+def bf16_half_ulp(x):
+    """Half a bf16 unit in the last place at |x| (8 significant bits)."""
+    ax = np.maximum(np.abs(x), 1e-30)
+    return np.exp2(np.floor(np.log2(ax)) - 8)
+
+
+def assert_parity(out, lse, ref_out, ref_lse, requests=None, tight=True, label="", bf16_rounding=False):
+    """max|out err| <= OUT_ATOL and max|lse err| <= LSE_ATOL (plus tighter gates).
+
+    bf16_rounding: the output was rounded to bf16 and rows can reach |out| >= 2
+    (needle rows return a V row); there rounding alone can take half a bf16 ulp
+    (up to 7.8e-3 on [2, 4)), so that much is allowed on top of the bar.
+    """
     o = out.float().cpu().numpy()
     l = lse.cpu().numpy()
     if requests is not None:
@@ -48,7 +60,8 @@ def assert_parity(out, lse, ref_out, ref_lse, requests=None, tight=True, label="
     fin = np.isfinite(ref_lse)
     err = np.abs(o - ref_out)
     assert np.all(np.isfinite(o)), f"{label}: non-finite output"
-    assert err.max() <= OUT_ATOL, f"{label}: max|out err| {err.max():.3e} > {OUT_ATOL}"
+    tol = OUT_ATOL + (np.where(np.abs(ref_out) >= 2.0, bf16_half_ulp(ref_out), 0.0) if bf16_rounding else 0.0)
+    assert np.all(err <= tol), f"{label}: max|out err| {err.max():.3e} > {OUT_ATOL}"
     lerr = np.abs(l[fin] - ref_lse[fin]).max() if fin.any() else 0.0
     assert lerr <= LSE_ATOL, f"{label}: max|lse err| {lerr:.3e} > {LSE_ATOL}"
     if tight:

@@ -64,8 +64,10 @@ def test_parity_cases(case, S):
     w = wl.make_workload(shape, 100 + CASES.index(case), "cuda", poison=True, needles=True, extra_pages=3)
     inp = wl.oracle_inputs(w)
     ref_out, ref_lse = decode_ref_inputs(inp)
+    out32, lse32 = run(w, S, torch.float32)
+    assert_parity(out32, lse32, ref_out, ref_lse, label=f"{case} S={S} fp32 out")
     out, lse = run(w, S)
-    assert_parity(out, lse, ref_out, ref_lse, label=f"{case} S={S}")
+    assert_parity(out, lse, ref_out, ref_lse, label=f"{case} S={S} bf16 out", bf16_rounding=True)
     assert_needles(w, out, inp)
 
 
