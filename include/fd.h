@@ -164,6 +164,38 @@ FD_API fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cache, c
                           const fd_tensor *cache_seqlens, int q_per_req, int num_splits,
                           fd_tensor *out, fd_tensor *lse, fd_stream_t stream);
 
+/*
+ * fd_decode_paged_static - fd_decode_paged for callers that cannot allocate
+ * device memory. The reference pages have no counterpart; it exists because
+ * some callers cannot call cudaMalloc: a serving engine that has already
+ * reserved all GPU memory for its own pool, or a plugin inside a process
+ * that forbids foreign device allocations. It needs no plan and allocates
+ * nothing.
+ *
+ * The split workspace is a fixed 32 MiB array inside the library, held on
+ * every GPU that loads it until the process exits. A call needing more,
+ * B*Tq*Hq*num_splits*(D+1)*4 bytes when num_splits > 1, fails with
+ * FD_ERR_WORKSPACE.
+ *
+ * Arguments are those of fd_decode_paged, with these differences:
+ *  - num_splits must be 1..64 (there is no tuning table);
+ *  - softmax_scale is explicit (0 = 1/sqrt(D));
+ *  - the device is the current one.
+ *
+ * The first call on a device does a one-time set-up: it looks up the array's
+ * address and raises the kernels' shared-memory limit. Make that first call
+ * before any stream capture.
+ *
+ * All calls share the array. Calls that overlap on the GPU race on it, so
+ * serialise them on one stream. Kernel status bits go to an internal word
+ * that this entry point does not report.
+ */
+FD_API fd_status fd_decode_paged_static(const fd_tensor *q, const fd_tensor *k_cache,
+                                        const fd_tensor *v_cache, const fd_tensor *kv_scales,
+                                        const fd_tensor *page_table, const fd_tensor *cache_seqlens,
+                                        int q_per_req, int num_splits, float softmax_scale,
+                                        fd_tensor *out, fd_tensor *lse, fd_stream_t stream);
+
 /* fd_set_max_seqlen_hint - host-known upper bound of cache_seqlens for the
  * next calls with num_splits = 0; picks the KV-length bucket of the tuning
  * table without reading device memory ("feat(autotune): ...", section

@@ -15,7 +15,7 @@ from typing import Optional, Sequence, Tuple
 
 __all__ = [
     "FdError", "load_library", "fd_plan_create", "fd_plan_destroy", "fd_set_plan", "fd_get_plan",
-    "fd_decode_paged", "fd_set_max_seqlen_hint", "fd_autotune", "fd_query_splits",
+    "fd_decode_paged", "fd_decode_paged_static", "fd_set_max_seqlen_hint", "fd_autotune", "fd_query_splits",
     "fd_autotune_set_timer", "fd_autotune_set_cache_dir", "fd_autotune_stats",
     "fd_read_device_status", "fd_plan_workspace_bytes", "fd_profile_begin", "fd_profile_end",
     "fd_status_string", "fd_last_error",
@@ -74,6 +74,7 @@ def load_library(path: Optional[str] = None):
         "fd_set_plan": (I, [P]),
         "fd_get_plan": (P, []),
         "fd_decode_paged": (I, [T, T, T, T, T, T, I, I, T, T, P]),
+        "fd_decode_paged_static": (I, [T, T, T, T, T, T, I, I, F, T, T, P]),
         "fd_set_max_seqlen_hint": (I, [P, I]),
         "fd_autotune": (I, [P, ctypes.POINTER(I), I, I, I, P]),
         "fd_query_splits": (I, [P, I, I, ctypes.POINTER(I)]),
@@ -187,6 +188,21 @@ def fd_decode_paged(q, k_cache, v_cache, kv_scales, page_table, cache_seqlens, q
     descs = [make_descriptor(t) for t in (q, k_cache, v_cache, kv_scales, page_table, cache_seqlens, out, lse)]
     _check(load_library().fd_decode_paged(*(_ref(d) for d in descs[:6]), q_per_req, num_splits,
                                           _ref(descs[6]), _ref(descs[7]), _stream_handle(stream)))
+
+
+def fd_decode_paged_static(q, k_cache, v_cache, kv_scales, page_table, cache_seqlens, q_per_req: int,
+                           num_splits: int, softmax_scale: float, out, lse, stream=None) -> None:
+    """fd_decode_paged without a plan and without any device allocation.
+
+    For callers that cannot allocate GPU memory. The split workspace is a
+    fixed 32 MiB array inside the library; num_splits must be given (1..64).
+    The first call on a device does a one-time set-up, so make it before any
+    stream capture. Calls that overlap on the GPU race on the shared array.
+    """
+    descs = [make_descriptor(t) for t in (q, k_cache, v_cache, kv_scales, page_table, cache_seqlens, out, lse)]
+    _check(load_library().fd_decode_paged_static(*(_ref(d) for d in descs[:6]), q_per_req, num_splits,
+                                                 softmax_scale, _ref(descs[6]), _ref(descs[7]),
+                                                 _stream_handle(stream)))
 
 
 def fd_set_max_seqlen_hint(plan: int, max_seqlen: int) -> None:
