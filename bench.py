@@ -372,7 +372,7 @@ def run_fd(args):
     # CPU baseline: the oracle on a bounded sample of this workload, host cores
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        reqs = [0, 1]
+        reqs = list(range(min(2, B)))
         gbps, secs, nbytes = oracle_baseline(w, reqs)
         cpu = {"value": round(gbps, 4), "unit": "GB/s", "cores": len(os.sched_getaffinity(0)),
                "blas_threads": blas_threads(), "kind": "oracle",
