@@ -17,14 +17,23 @@
 //    completing on a per-stage mbarrier. Quantised caches also copy their
 //    per-row fp32 scales with cp.async (one arrival per lane on the barrier).
 //  * consumer warps: warp w takes keys [16w, 16w + 16) of each 64-key stage.
-//    Quantised rows are first converted in a per-warp staging tile, K codes
-//    to bf16 and V codes to fp16 (both exact). QK^T and PV run on mma.sync
-//    m16n8k16 (fp32 accumulate) with the 16 query rows as M; the online
-//    softmax keeps a running max / sum per row in the log2 domain with quad
-//    shuffles. K scales multiply the fp32 scores (per 32-channel group for
-//    int4, from separate per-group accumulators); V scales are folded into the
-//    probabilities, which are then rounded to fp16 (11-bit mantissa) for an
-//    fp16 PV product; the bf16 cache path rounds probabilities to bf16.
+//    QK^T and PV run on mma.sync m16n8k16 (fp32 accumulate) with the 16 query
+//    rows as M; the online softmax keeps a running max / sum per row in the
+//    log2 domain with quad shuffles. bf16 caches feed ldmatrix fragments
+//    straight from the TMA tile. Quantised caches are converted in registers
+//    from the raw tile, no staging copy:
+//      - K: ldmatrix of the raw rows as 16-bit elements hands each thread 4
+//        (int8) or 8 (int4) consecutive codes of one key; they become exact
+//        bf16 B fragments, and the Q A fragments are built once per CTA with
+//        the matching channel order (a dot product does not care about the
+//        order of its terms). K scales multiply the fp32 scores (per
+//        32-channel group for int4, from one accumulator per group).
+//      - V: thread (g, c) owns D/8 consecutive channels of its 4 keys; a
+//        byte permute pairs two keys' codes at one channel, giving exact fp16
+//        B fragments; PV output columns come out permuted and are put back in
+//        order by the epilogue. int8 folds the per-key V scale into the
+//        probabilities (fp16); int4 multiplies its per-group V scale into the
+//        fp16 V values.
 //  * epilogue: the consumer warps merge their (max, sum, O) through shared
 //    memory and write either fp32 partial O + LSE to the split workspace, or
 //    (num_splits == 1) the final bf16/fp32 output and LSE.
@@ -53,24 +62,21 @@ struct S1Cfg {
   static constexpr int N_BOX = ROW_BYTES / BOX_BYTES;
   static constexpr int BOX_ELEMS = KIND == KV_BF16 ? BOX_BYTES / 2 : BOX_BYTES;
   static constexpr int NG = KIND == KV_I4 ? D / 32 : 1;  // fp32 scales per cache row
+  static constexpr int NT = D / 8;                       // PV n-tiles (channels per thread, quantised V)
   static constexpr int BLOCK_N = 64;                     // keys per pipeline stage
   static constexpr int NUM_CW = 4;                       // consumer warps (16 keys each)
   static constexpr int THREADS = (NUM_CW + 1) * 32;
-  static constexpr int STAGES = KIND == KV_BF16 ? 3 : (KIND == KV_I8 ? 4 : 6);
+  static constexpr int STAGES = KIND == KV_BF16 ? 3 : (KIND == KV_I8 ? 6 : 8);
   static constexpr int TILE = BLOCK_N * ROW_BYTES;       // K (or V) bytes of one stage
   static constexpr int SC = QUANT ? BLOCK_N * NG * 4 : 0;
   static constexpr int STAGE = ((2 * TILE + 2 * SC) + 1023) / 1024 * 1024;
   static constexpr int RING = STAGES * STAGE;
-  static constexpr int STG_HALF = 16 * 128;              // 16 rows x 64 bf16
-  static constexpr int STG_TILE = (D / 64) * STG_HALF;   // one K or V staging tile of a warp
-  static constexpr int STG = QUANT ? NUM_CW * 2 * STG_TILE : 0;
   static constexpr int QROW = D * 2 + 16;                // padded bf16 row of the Q tile
   static constexpr int QB = 16 * QROW;
   static constexpr int CROW = D + 8;                     // padded fp32 row of the combine tile
   static constexpr int CMB_O = NUM_CW * 16 * CROW * 4;
   static constexpr int CMB = CMB_O + NUM_CW * 16 * 2 * 4;
-  static constexpr int OFF_STG = RING;
-  static constexpr int OFF_Q = OFF_STG + STG;
+  static constexpr int OFF_Q = RING;
   static constexpr int OFF_BAR = (OFF_Q + QB + 7) / 8 * 8;
   static constexpr int SMEM = OFF_BAR + 2 * STAGES * 8;
   static constexpr int SMEM_ALLOC = SMEM + 1024;         // slack to align the base to 1024
@@ -81,7 +87,7 @@ struct S1Cfg {
 };
 
 // ----------------------------------------------------------------------------
-// In-register conversions of cache codes to bf16 (exact: |code| <= 128).
+// In-register conversions of cache codes (exact: |code| <= 128).
 
 // Four int8 codes (one 32-bit word, lowest byte = lowest channel) -> two
 // bf16x2 words. A biased byte u = code + 128 placed in the low mantissa bits
@@ -96,105 +102,50 @@ __device__ __forceinline__ void i8x4_to_bf16(uint32_t w, uint32_t &lo, uint32_t 
   hi = pack_bf16x2(f2, f3);
 }
 
-// One byte of two int4 codes (low nibble = even channel) -> one bf16x2 word.
-// A biased nibble u = code + 8 in the mantissa of bf16 128.0 gives 128 + u
-// exactly; subtracting 136 yields code.
-__device__ __forceinline__ uint32_t i4x2_to_bf16(uint32_t biased_byte) {
-  uint32_t r = 0x43004300u | (biased_byte & 0xFu) | ((biased_byte & 0xF0u) << 12);
-  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&r);
-  v = __hsub2(v, __floats2bfloat162_rn(136.0f, 136.0f));
+// Two biased int4 codes u = code + 8 at bits 0-3 and 16-19 of x -> bf16x2.
+// In the mantissa of bf16 128.0 they read 128 + u exactly; minus 136 = code.
+__device__ __forceinline__ uint32_t i4pair_to_bf16(uint32_t x) {
+  uint32_t r = (x & 0x000F000Fu) | 0x43004300u;
+  __nv_bfloat162 v =
+      __hsub2(*reinterpret_cast<__nv_bfloat162 *>(&r), __floats2bfloat162_rn(136.0f, 136.0f));
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// Four int8 codes -> two f16x2 words. A biased byte u = code + 128 in the low
-// mantissa bits of fp16 1024.0 gives 1024 + u exactly; subtracting 1152
-// yields code.
-__device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
-  const uint32_t x = w ^ 0x80808080u;
-  uint32_t a = __byte_perm(x, 0x64646464u, 0x5140);
-  uint32_t b = __byte_perm(x, 0x64646464u, 0x7362);
-  const __half2 bias = __floats2half2_rn(1152.0f, 1152.0f);
-  __half2 ha = __hsub2(*reinterpret_cast<__half2 *>(&a), bias);
-  __half2 hb = __hsub2(*reinterpret_cast<__half2 *>(&b), bias);
-  lo = *reinterpret_cast<uint32_t *>(&ha);
-  hi = *reinterpret_cast<uint32_t *>(&hb);
+// f16x2 (1024 + u_lo, 1024 + u_hi) from biased bytes at bits 0-7 and 16-23.
+__device__ __forceinline__ uint32_t u8pair_to_f16_biased(uint32_t t) {
+  return (t & 0x00FF00FFu) | 0x64006400u;
 }
 
-// One byte of two int4 codes -> one f16x2 word (fp16 1024 + u, minus 1032).
-__device__ __forceinline__ uint32_t i4x2_to_f16(uint32_t biased_byte) {
-  uint32_t r = 0x64006400u | (biased_byte & 0xFu) | ((biased_byte & 0xF0u) << 12);
-  __half2 v = __hsub2(*reinterpret_cast<__half2 *>(&r), __floats2half2_rn(1032.0f, 1032.0f));
-  return *reinterpret_cast<uint32_t *>(&v);
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, float v) {
+  __half2 r = __hsub2(*reinterpret_cast<__half2 *>(&a), __floats2half2_rn(v, v));
+  return *reinterpret_cast<uint32_t *>(&r);
 }
 
-// Convert this warp's 16 cache rows (tile rows row0..row0+15 of a raw stage
-// tile) into a 16-bit staging tile (bf16, or fp16 when F16) laid out like a
-// bf16 TMA tile (64-element halves of 16 rows x 128 bytes, 128-byte
-// swizzled). Rows whose token index is >= zero_from are written as zeros.
-template <class C, int KIND, bool F16>
-__device__ __forceinline__ void stage_rows(const uint8_t *raw, uint8_t *stg, int row0, int tok_row0,
-                                           int zero_from, int lane) {
-  constexpr int CHUNKS = C::ROW_BYTES / 16;     // 16-byte chunks per raw row
-  constexpr int JOBS = 16 * CHUNKS;
-  constexpr int VALS = KIND == KV_I8 ? 16 : 32;  // codes per raw chunk
-#pragma unroll
-  for (int job = lane; job < JOBS; job += 32) {
-    const int r = job / CHUNKS, cc = job % CHUNKS;
-    const uint32_t roff = swz<C::BOX_BYTES>((row0 + r) * C::ROW_BYTES + cc * 16);
-    const uint4 src = *reinterpret_cast<const uint4 *>(raw + roff);
-    const bool zero = tok_row0 + r >= zero_from;
-    uint32_t out[VALS / 2];
-    if constexpr (KIND == KV_I8) {
-      const uint32_t w[4] = {src.x, src.y, src.z, src.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        if constexpr (F16)
-          i8x4_to_f16(w[k], out[2 * k], out[2 * k + 1]);
-        else
-          i8x4_to_bf16(w[k], out[2 * k], out[2 * k + 1]);
-      }
-    } else {
-      const uint32_t w[4] = {src.x ^ 0x88888888u, src.y ^ 0x88888888u, src.z ^ 0x88888888u,
-                             src.w ^ 0x88888888u};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-#pragma unroll
-        for (int bi = 0; bi < 4; ++bi) {
-          const uint32_t byte = (w[k] >> (8 * bi)) & 0xFFu;
-          out[k * 4 + bi] = F16 ? i4x2_to_f16(byte) : i4x2_to_bf16(byte);
-        }
-      }
-    }
-    const int d0 = cc * VALS;
-#pragma unroll
-    for (int q = 0; q < VALS / 8; ++q) {
-      const int d = d0 + q * 8;
-      uint8_t *dst = stg + (d >> 6) * C::STG_HALF + swz<128>(r * 128 + (d & 63) * 2);
-      uint4 v;
-      v.x = zero ? 0u : out[q * 4 + 0];
-      v.y = zero ? 0u : out[q * 4 + 1];
-      v.z = zero ? 0u : out[q * 4 + 2];
-      v.w = zero ? 0u : out[q * 4 + 3];
-      *reinterpret_cast<uint4 *>(dst) = v;
-    }
-  }
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
+  return *reinterpret_cast<uint32_t *>(&r);
+}
+
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, float mul, float add) {
+  __half2 r = __hfma2(*reinterpret_cast<__half2 *>(&a), __floats2half2_rn(mul, mul),
+                      __floats2half2_rn(add, add));
+  return *reinterpret_cast<uint32_t *>(&r);
 }
 
 // ----------------------------------------------------------------------------
-// One 16-key block of one warp: scores, online softmax update, PV.
+// One 16-key block of one warp, bf16 cache: scores, online softmax, PV.
 //
-// kbase / vbase: shared addresses of bf16 tiles laid out as 64-element halves
-// (half stride `half`) of 128-byte swizzled rows; the warp's keys are rows
-// row0..row0+15. ksc / vsc: per-row fp32 scales (NG per row) or null.
+// kbase / vbase: shared addresses of the stage's K / V tiles, laid out as
+// 64-element halves (half stride `half`) of 128-byte swizzled rows; the
+// warp's keys are rows row0..row0+15.
 template <class C>
 __device__ __forceinline__ void warp_block(uint32_t kbase, uint32_t vbase, uint32_t half, int row0,
-                                           const float *ksc, const float *vsc, int sc_row0,
                                            const uint32_t (&qa)[C::D / 16][4],
                                            float (&o)[C::D / 8][4], float (&m)[2], float (&l)[2],
                                            int tok_row0, int lim0, int lim1, float scale_log2,
                                            int lane) {
   constexpr int D = C::D;
-  constexpr int NG = C::NG;
+  constexpr int NG = 1;
   const int c = lane & 3;
   const int mi = lane >> 3, ri = lane & 7;
 
@@ -225,15 +176,7 @@ __device__ __forceinline__ void warp_block(uint32_t kbase, uint32_t vbase, uint3
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int key = nt * 8 + 2 * c + (e & 1);
-      float v;
-      if constexpr (C::QUANT) {
-        const float *sc = ksc + (sc_row0 + key) * NG;
-        v = 0.f;
-#pragma unroll
-        for (int gi = 0; gi < NG; ++gi) v = fmaf(acc[gi][nt][e], sc[gi], v);
-      } else {
-        v = acc[0][nt][e];
-      }
+      const float v = acc[0][nt][e];
       const int lim = (e < 2) ? lim0 : lim1;
       s[nt][e] = (tok_row0 + key < lim) ? v * scale_log2 : -INFINITY;
     }
@@ -272,37 +215,12 @@ __device__ __forceinline__ void warp_block(uint32_t kbase, uint32_t vbase, uint3
     }
   }
 
-  // ---- P (bf16, V scales folded per group) as the A operand of PV
-  constexpr int NGV = NG;
-  uint32_t pa[NGV][4];
-#pragma unroll
-  for (int gv = 0; gv < NGV; ++gv) {
-    float pv[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if constexpr (C::QUANT) {
-          const int key = nt * 8 + 2 * c + (e & 1);
-          const float vs = vsc[(sc_row0 + key) * NG + gv];
-          pv[nt][e] = p[nt][e] == 0.f ? 0.f : p[nt][e] * vs;
-        } else {
-          pv[nt][e] = p[nt][e];
-        }
-      }
-    }
-    if constexpr (C::QUANT) {
-      pa[gv][0] = pack_f16x2(pv[0][0], pv[0][1]);
-      pa[gv][1] = pack_f16x2(pv[0][2], pv[0][3]);
-      pa[gv][2] = pack_f16x2(pv[1][0], pv[1][1]);
-      pa[gv][3] = pack_f16x2(pv[1][2], pv[1][3]);
-    } else {
-      pa[gv][0] = pack_bf16x2(pv[0][0], pv[0][1]);
-      pa[gv][1] = pack_bf16x2(pv[0][2], pv[0][3]);
-      pa[gv][2] = pack_bf16x2(pv[1][0], pv[1][1]);
-      pa[gv][3] = pack_bf16x2(pv[1][2], pv[1][3]);
-    }
-  }
+  // ---- P (bf16) as the A operand of PV
+  uint32_t pa[4];
+  pa[0] = pack_bf16x2(p[0][0], p[0][1]);
+  pa[1] = pack_bf16x2(p[0][2], p[0][3]);
+  pa[2] = pack_bf16x2(p[1][0], p[1][1]);
+  pa[3] = pack_bf16x2(p[1][2], p[1][3]);
 
   // ---- O += P V
   const int vrow = row0 + ((mi & 1) << 3) + ri;
@@ -311,13 +229,258 @@ __device__ __forceinline__ void warp_block(uint32_t kbase, uint32_t vbase, uint3
     const int d = dp * 16 + ((mi >> 1) << 3);
     uint32_t bv[4];
     ldsm_x4_t(bv, vbase + (d >> 6) * half + swz<128>(vrow * 128 + (d & 63) * 2));
-    const int gv = NGV == 1 ? 0 : dp / 2;
-    if constexpr (C::QUANT) {
-      mma_f16_16816(o[2 * dp], pa[gv], bv[0], bv[1]);
-      mma_f16_16816(o[2 * dp + 1], pa[gv], bv[2], bv[3]);
+    mma_bf16_16816(o[2 * dp], pa, bv[0], bv[1]);
+    mma_bf16_16816(o[2 * dp + 1], pa, bv[2], bv[3]);
+  }
+}
+
+// Online-softmax update in the log2 domain for a thread's two rows (g, g+8):
+// row max over the quad, alpha = 2^(m_old - m_new), p = 2^(s - m_new), running
+// sum rescaled by alpha. Rows that have seen no key keep m = -inf and p = 0.
+__device__ __forceinline__ void softmax_update(const float (&s)[2][4], float (&p)[2][4], float (&m)[2],
+                                               float (&l)[2], float (&al)[2]) {
+  float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+  float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+  const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+  const float b0 = mn0 == -INFINITY ? 0.f : mn0;
+  const float b1 = mn1 == -INFINITY ? 0.f : mn1;
+  al[0] = exp2f(m[0] - b0);
+  al[1] = exp2f(m[1] - b1);
+  m[0] = mn0;
+  m[1] = mn1;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    p[nt][0] = exp2f(s[nt][0] - b0);
+    p[nt][1] = exp2f(s[nt][1] - b0);
+    p[nt][2] = exp2f(s[nt][2] - b1);
+    p[nt][3] = exp2f(s[nt][3] - b1);
+  }
+  l[0] = l[0] * al[0] + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+  l[1] = l[1] * al[1] + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+}
+
+// ----------------------------------------------------------------------------
+// One 16-key block of one warp, quantised cache, straight from the raw tile.
+//
+// kt / vt: the stage's raw K / V tiles (rows of ROW_BYTES, TMA-swizzled with
+// span BOX_BYTES); ksc / vsc: the stage's per-row fp32 scales (NG per row).
+// qa: Q fragments in the channel order the K codes arrive in (see
+// build_q_fragments). O columns come out permuted: n-tile j, d-slot n holds
+// channel n * NT + j.
+template <class C, int KIND>
+__device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *vt, const float *ksc,
+                                             const float *vsc, int row0,
+                                             const uint32_t (&qa)[C::D / 16][4],
+                                             float (&o)[C::NT][4], float (&m)[2], float (&l)[2],
+                                             int tok_row0, int c1, int lim0, int lim1,
+                                             float scale_log2, int lane) {
+  constexpr int NG = C::NG, RB = C::ROW_BYTES, SW = C::BOX_BYTES, NT = C::NT;
+  constexpr int CH = RB / 16;  // 16-byte chunks per cache row
+  const int g = lane >> 2, c = lane & 3;
+  const int mi = lane >> 3, ri = lane & 7;
+  const uint32_t kbase = smem_u32(kt);
+
+  // ---- S = Q K^T; one accumulator per scale group (int4), else one
+  float acc[NG][2][4];
+#pragma unroll
+  for (int gi = 0; gi < NG; ++gi)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[gi][nt][e] = 0.f;
+  const int krow = row0 + ((mi >> 1) << 3) + ri;
+#pragma unroll
+  for (int kc = 0; kc < CH; kc += 2) {
+    uint32_t r[4];  // (n-tile 0, chunk kc), (n-tile 0, kc+1), (n-tile 1, kc), (n-tile 1, kc+1)
+    ldsm_x4(r, kbase + swz<SW>(krow * RB + (kc + (mi & 1)) * 16));
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int ch = kc + hh;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const uint32_t w = r[nt * 2 + hh];
+        if constexpr (KIND == KV_I8) {
+          uint32_t b0, b1;  // channels 16ch+4c+{0,1} and 16ch+4c+{2,3}
+          i8x4_to_bf16(w, b0, b1);
+          mma_bf16_16816(acc[0][nt], qa[ch], b0, b1);
+        } else {
+          const uint32_t x = w ^ 0x88888888u;  // nibble k = channel 32ch + 8c + k
+          mma_bf16_16816(acc[ch][nt], qa[2 * ch], i4pair_to_bf16(x), i4pair_to_bf16(x >> 4));
+          mma_bf16_16816(acc[ch][nt], qa[2 * ch + 1], i4pair_to_bf16(x >> 8),
+                         i4pair_to_bf16(x >> 12));
+        }
+      }
+    }
+  }
+
+  // ---- K scales, scale, mask by selection
+  float s[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int key = nt * 8 + 2 * c + (e & 1);
+      const float *sc = ksc + (row0 + key) * NG;
+      float v = 0.f;
+#pragma unroll
+      for (int gi = 0; gi < NG; ++gi) v = fmaf(acc[gi][nt][e], sc[gi], v);
+      const int lim = (e < 2) ? lim0 : lim1;
+      s[nt][e] = (tok_row0 + key < lim) ? v * scale_log2 : -INFINITY;
+    }
+  }
+  float p[2][4], al[2];
+  softmax_update(s, p, m, l, al);
+  if (__any_sync(0xffffffffu, al[0] != 1.f || al[1] != 1.f)) {
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      o[j][0] *= al[0];
+      o[j][1] *= al[0];
+      o[j][2] *= al[1];
+      o[j][3] *= al[1];
+    }
+  }
+
+  // ---- P as the fp16 A operand (int8: the per-key V scale folded in)
+  uint32_t pa[4];
+  if constexpr (KIND == KV_I8) {
+    float pv[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float vs = vsc[row0 + nt * 8 + 2 * c + (e & 1)];
+        pv[nt][e] = p[nt][e] == 0.f ? 0.f : p[nt][e] * vs;
+      }
+    pa[0] = pack_f16x2(pv[0][0], pv[0][1]);
+    pa[1] = pack_f16x2(pv[0][2], pv[0][3]);
+    pa[2] = pack_f16x2(pv[1][0], pv[1][1]);
+    pa[3] = pack_f16x2(pv[1][2], pv[1][3]);
+  } else {
+    pa[0] = pack_f16x2(p[0][0], p[0][1]);
+    pa[1] = pack_f16x2(p[0][2], p[0][3]);
+    pa[2] = pack_f16x2(p[1][0], p[1][1]);
+    pa[3] = pack_f16x2(p[1][2], p[1][3]);
+  }
+
+  // ---- V fragments: keys (2c, 2c+1) -> b0b1, (2c+8, 2c+9) -> b2b3, channels
+  // [g*NT, g*NT + NT), one channel per n-tile. Keys at or past c1 read as 0.
+  const int kA = row0 + 2 * c, kB = kA + 8;
+  const int vrows[4] = {kA, kA + 1, kB, kB + 1};
+  bool valid[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) valid[i] = tok_row0 + (vrows[i] - row0) < c1;
+  if constexpr (KIND == KV_I8) {
+    static_assert(NT % 4 == 0, "int8 V words");
+    constexpr int NW = NT / 4;  // 32-bit words per key
+    uint32_t w[4][NW];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint8_t *src = vt + swz<SW>(vrows[i] * RB + g * NT);
+      if constexpr (NW == 4) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(src);
+        w[i][0] = v.x;
+        w[i][1] = v.y;
+        w[i][2] = v.z;
+        w[i][3] = v.w;
+      } else {
+        const uint2 v = *reinterpret_cast<const uint2 *>(src);
+        w[i][0] = v.x;
+        w[i][1] = v.y;
+      }
+#pragma unroll
+      for (int k = 0; k < NW; ++k) w[i][k] = valid[i] ? (w[i][k] ^ 0x80808080u) : 0x80808080u;
+    }
+#pragma unroll
+    for (int k = 0; k < NW; ++k) {
+#pragma unroll
+      for (int bi = 0; bi < 4; ++bi) {
+        // byte bi of both keys -> bits 0-7 and 16-23: channel g*NT + 4k + bi
+        const uint32_t sel = (bi) | (bi << 4) | ((4u + bi) << 8) | ((4u + bi) << 12);
+        const uint32_t b0 =
+            hsub2_u32(u8pair_to_f16_biased(__byte_perm(w[0][k], w[1][k], sel)), 1152.0f);
+        const uint32_t b1 =
+            hsub2_u32(u8pair_to_f16_biased(__byte_perm(w[2][k], w[3][k], sel)), 1152.0f);
+        mma_f16_16816(o[4 * k + bi], pa, b0, b1);
+      }
+    }
+  } else {
+    static_assert(NT % 8 == 0, "int4 V words");
+    constexpr int NW = NT / 8;  // 32-bit words per key
+    const int grp = (g * NT) / 32;
+    uint32_t w[4][NW];
+    float vsf[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint8_t *src = vt + swz<SW>(vrows[i] * RB + g * (NT / 2));
+      if constexpr (NW == 2) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(src);
+        w[i][0] = v.x;
+        w[i][1] = v.y;
+      } else {
+        w[i][0] = *reinterpret_cast<const uint32_t *>(src);
+      }
+#pragma unroll
+      for (int k = 0; k < NW; ++k) w[i][k] ^= 0x88888888u;
+      vsf[i] = valid[i] ? vsc[vrows[i] * NG + grp] : 0.f;
+    }
+    const uint32_t sA = pack_f16x2(vsf[0], vsf[1]);
+    const uint32_t sB = pack_f16x2(vsf[2], vsf[3]);
+#pragma unroll
+    for (int k = 0; k < NW; ++k) {
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {  // bytes 0-1, then 2-3, of each key's word
+        const uint32_t sel = hb ? 0x7632u : 0x5410u;
+        const uint32_t tA = __byte_perm(w[0][k], w[1][k], sel);
+        const uint32_t tB = __byte_perm(w[2][k], w[3][k], sel);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // nibble q: channel g*NT + 8k + 4hb + q
+          uint32_t xa, xb;
+          if (q & 1) {  // high nibble reads 1024 + 16u: /16 - 72 = code
+            xa = hfma2_u32(((tA >> (4 * (q - 1))) & 0x00F000F0u) | 0x64006400u, 1.0f / 16.0f, -72.0f);
+            xb = hfma2_u32(((tB >> (4 * (q - 1))) & 0x00F000F0u) | 0x64006400u, 1.0f / 16.0f, -72.0f);
+          } else {
+            xa = hsub2_u32(((tA >> (4 * q)) & 0x000F000Fu) | 0x64006400u, 1032.0f);
+            xb = hsub2_u32(((tB >> (4 * q)) & 0x000F000Fu) | 0x64006400u, 1032.0f);
+          }
+          mma_f16_16816(o[8 * k + 4 * hb + q], pa, hmul2_u32(xa, sA), hmul2_u32(xb, sB));
+        }
+      }
+    }
+  }
+}
+
+// Q A fragments in the channel order warp_block_q feeds K codes in.
+//  int8, k-step ks (a 16-byte chunk of 16 codes): thread c's slots (2c, 2c+1)
+//    are channels 16ks+4c+{0,1} and slots (2c+8, 2c+9) are 16ks+4c+{2,3}.
+//  int4, k-steps 2ch / 2ch+1 (chunk ch of 32 codes, base 32ch+8c): slots
+//    (2c, 2c+1) = base+{0,4} / base+{2,6}; (2c+8, 2c+9) = base+{1,5} / base+{3,7}.
+template <class C, int KIND>
+__device__ __forceinline__ void build_q_fragments(const uint8_t *qs, uint32_t (&qa)[C::D / 16][4],
+                                                  int lane) {
+  const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const uint8_t *row = qs + (g + 8 * half) * C::QROW;
+    if constexpr (KIND == KV_I8) {
+#pragma unroll
+      for (int ks = 0; ks < C::D / 16; ++ks) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(row + (16 * ks + 4 * c) * 2);
+        qa[ks][half] = v.x;
+        qa[ks][2 + half] = v.y;
+      }
     } else {
-      mma_bf16_16816(o[2 * dp], pa[gv], bv[0], bv[1]);
-      mma_bf16_16816(o[2 * dp + 1], pa[gv], bv[2], bv[3]);
+#pragma unroll
+      for (int ch = 0; ch < C::D / 32; ++ch) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(row + (32 * ch + 8 * c) * 2);
+        qa[2 * ch][half] = __byte_perm(v.x, v.z, 0x5410);          // base+0, base+4
+        qa[2 * ch][2 + half] = __byte_perm(v.x, v.z, 0x7632);      // base+1, base+5
+        qa[2 * ch + 1][half] = __byte_perm(v.y, v.w, 0x5410);      // base+2, base+6
+        qa[2 * ch + 1][2 + half] = __byte_perm(v.y, v.w, 0x7632);  // base+3, base+7
+      }
     }
   }
 }
@@ -509,7 +672,9 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D>::THREADS, S1Cfg<KIND, D>::MIN_B
     }
     named_barrier(1, C::NUM_CW * 32);
     uint32_t qa[D / 16][4];
-    {
+    if constexpr (C::QUANT) {
+      build_q_fragments<C, KIND>(qs, qa, lane);
+    } else {
       const int mi = lane >> 3, ri = lane & 7;
       const int row = ((mi & 1) << 3) + ri;
 #pragma unroll
@@ -548,15 +713,10 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D>::THREADS, S1Cfg<KIND, D>::MIN_B
       uint8_t *vt = kt + C::TILE;
       if (tok_row0 < c1) {
         if constexpr (C::QUANT) {
-          uint8_t *ks = smem + C::OFF_STG + warp * 2 * C::STG_TILE;
-          uint8_t *vs = ks + C::STG_TILE;
-          stage_rows<C, KIND, false>(kt, ks, row0, tok_row0, 0x7fffffff, lane);
-          stage_rows<C, KIND, true>(vt, vs, row0, tok_row0, c1, lane);
-          __syncwarp();
           const float *ksc = reinterpret_cast<const float *>(vt + C::TILE);
           const float *vsc = ksc + C::BLOCK_N * C::NG;
-          warp_block<C>(smem_u32(ks), smem_u32(vs), C::STG_HALF, 0, ksc, vsc, row0, qa, o, m, l,
-                        tok_row0, lim[0], lim[1], p.scale_log2, lane);
+          warp_block_q<C, KIND>(kt, vt, ksc, vsc, row0, qa, o, m, l, tok_row0, c1, lim[0], lim[1],
+                                p.scale_log2, lane);
         } else {
           if (tok_row0 + 16 > c1) {  // zero V rows past the split end before PV
             constexpr int CH = C::N_BOX * (C::BOX_BYTES / 16);
@@ -572,8 +732,8 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D>::THREADS, S1Cfg<KIND, D>::MIN_B
             fence_proxy_async_smem();
             __syncwarp();
           }
-          warp_block<C>(smem_u32(kt), smem_u32(vt), C::BLOCK_N * 128, row0, nullptr, nullptr, 0,
-                        qa, o, m, l, tok_row0, lim[0], lim[1], p.scale_log2, lane);
+          warp_block<C>(smem_u32(kt), smem_u32(vt), C::BLOCK_N * 128, row0, qa, o, m, l, tok_row0,
+                        lim[0], lim[1], p.scale_log2, lane);
         }
       }
       __syncwarp();
@@ -595,8 +755,15 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D>::THREADS, S1Cfg<KIND, D>::MIN_B
       float *w1 = co + (warp * 16 + g + 8) * C::CROW;
 #pragma unroll
       for (int j = 0; j < D / 8; ++j) {
-        *reinterpret_cast<float2 *>(w0 + j * 8 + 2 * c) = make_float2(o[j][0], o[j][1]);
-        *reinterpret_cast<float2 *>(w1 + j * 8 + 2 * c) = make_float2(o[j][2], o[j][3]);
+        if constexpr (C::QUANT) {  // n-tile j, d-slot n holds channel n * NT + j
+          w0[(2 * c) * C::NT + j] = o[j][0];
+          w0[(2 * c + 1) * C::NT + j] = o[j][1];
+          w1[(2 * c) * C::NT + j] = o[j][2];
+          w1[(2 * c + 1) * C::NT + j] = o[j][3];
+        } else {
+          *reinterpret_cast<float2 *>(w0 + j * 8 + 2 * c) = make_float2(o[j][0], o[j][1]);
+          *reinterpret_cast<float2 *>(w1 + j * 8 + 2 * c) = make_float2(o[j][2], o[j][3]);
+        }
       }
       if (c == 0) {
         cm[warp * 16 + g] = m[0];
