@@ -77,7 +77,9 @@ struct S1Cfg {
   static constexpr int CMB_O = NUM_CW * 16 * CROW * 4;
   static constexpr int CMB = CMB_O + NUM_CW * 16 * 2 * 4;
   static constexpr int OFF_Q = RING;
-  static constexpr int OFF_BAR = (OFF_Q + QB + 7) / 8 * 8;
+  static constexpr int OFF_QI = OFF_Q + QB;              // per row: 2^e, then NG bias constants
+  static constexpr int QI = QUANT ? 16 * (1 + NG) * 4 : 0;
+  static constexpr int OFF_BAR = (OFF_QI + QI + 7) / 8 * 8;
   static constexpr int SMEM = OFF_BAR + 2 * STAGES * 8;
   static constexpr int SMEM_ALLOC = SMEM + 1024;         // slack to align the base to 1024
   static constexpr int MIN_BLOCKS = SMEM_ALLOC * 2 <= 227 * 1024 ? 2 : 1;
@@ -87,29 +89,7 @@ struct S1Cfg {
 };
 
 // ----------------------------------------------------------------------------
-// In-register conversions of cache codes (exact: |code| <= 128).
-
-// Four int8 codes (one 32-bit word, lowest byte = lowest channel) -> two
-// bf16x2 words. A biased byte u = code + 128 placed in the low mantissa bits
-// of 2^23 gives the float 2^23 + u exactly; subtracting 2^23 + 128 yields code.
-__device__ __forceinline__ void i8x4_to_bf16(uint32_t w, uint32_t &lo, uint32_t &hi) {
-  const uint32_t x = w ^ 0x80808080u;
-  const float f0 = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7650)) - 8388736.0f;
-  const float f1 = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7651)) - 8388736.0f;
-  const float f2 = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7652)) - 8388736.0f;
-  const float f3 = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7653)) - 8388736.0f;
-  lo = pack_bf16x2(f0, f1);
-  hi = pack_bf16x2(f2, f3);
-}
-
-// Two biased int4 codes u = code + 8 at bits 0-3 and 16-19 of x -> bf16x2.
-// In the mantissa of bf16 128.0 they read 128 + u exactly; minus 136 = code.
-__device__ __forceinline__ uint32_t i4pair_to_bf16(uint32_t x) {
-  uint32_t r = (x & 0x000F000Fu) | 0x43004300u;
-  __nv_bfloat162 v =
-      __hsub2(*reinterpret_cast<__nv_bfloat162 *>(&r), __floats2bfloat162_rn(136.0f, 136.0f));
-  return *reinterpret_cast<uint32_t *>(&v);
-}
+// In-register conversions of cache codes to fp16 (exact: |code| <= 128).
 
 // f16x2 (1024 + u_lo, 1024 + u_hi) from biased bytes at bits 0-7 and 16-23.
 __device__ __forceinline__ uint32_t u8pair_to_f16_biased(uint32_t t) {
@@ -190,17 +170,17 @@ __device__ __forceinline__ void warp_block(uint32_t kbase, uint32_t vbase, uint3
   const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
   const float b0 = mn0 == -INFINITY ? 0.f : mn0;
   const float b1 = mn1 == -INFINITY ? 0.f : mn1;
-  const float al0 = exp2f(m[0] - b0), al1 = exp2f(m[1] - b1);
+  const float al0 = fast_exp2(m[0] - b0), al1 = fast_exp2(m[1] - b1);
   m[0] = mn0;
   m[1] = mn1;
 
   float p[2][4];
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
-    p[nt][0] = exp2f(s[nt][0] - b0);
-    p[nt][1] = exp2f(s[nt][1] - b0);
-    p[nt][2] = exp2f(s[nt][2] - b1);
-    p[nt][3] = exp2f(s[nt][3] - b1);
+    p[nt][0] = fast_exp2(s[nt][0] - b0);
+    p[nt][1] = fast_exp2(s[nt][1] - b0);
+    p[nt][2] = fast_exp2(s[nt][2] - b1);
+    p[nt][3] = fast_exp2(s[nt][3] - b1);
   }
   l[0] = l[0] * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
   l[1] = l[1] * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
@@ -248,16 +228,16 @@ __device__ __forceinline__ void softmax_update(const float (&s)[2][4], float (&p
   const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
   const float b0 = mn0 == -INFINITY ? 0.f : mn0;
   const float b1 = mn1 == -INFINITY ? 0.f : mn1;
-  al[0] = exp2f(m[0] - b0);
-  al[1] = exp2f(m[1] - b1);
+  al[0] = fast_exp2(m[0] - b0);
+  al[1] = fast_exp2(m[1] - b1);
   m[0] = mn0;
   m[1] = mn1;
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
-    p[nt][0] = exp2f(s[nt][0] - b0);
-    p[nt][1] = exp2f(s[nt][1] - b0);
-    p[nt][2] = exp2f(s[nt][2] - b1);
-    p[nt][3] = exp2f(s[nt][3] - b1);
+    p[nt][0] = fast_exp2(s[nt][0] - b0);
+    p[nt][1] = fast_exp2(s[nt][1] - b0);
+    p[nt][2] = fast_exp2(s[nt][2] - b1);
+    p[nt][3] = fast_exp2(s[nt][3] - b1);
   }
   l[0] = l[0] * al[0] + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
   l[1] = l[1] * al[1] + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
@@ -275,16 +255,16 @@ template <class C, int KIND>
 __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *vt, const float *ksc,
                                              const float *vsc, int row0,
                                              const uint32_t (&qa)[C::D / 16][4],
+                                             const float (&qc)[2][C::NG], const float (&rs)[2],
                                              float (&o)[C::NT][4], float (&m)[2], float (&l)[2],
-                                             int tok_row0, int c1, int lim0, int lim1,
-                                             float scale_log2, int lane) {
+                                             int tok_row0, int c1, int lim0, int lim1, int lane) {
   constexpr int NG = C::NG, RB = C::ROW_BYTES, SW = C::BOX_BYTES, NT = C::NT;
   constexpr int CH = RB / 16;  // 16-byte chunks per cache row
   const int g = lane >> 2, c = lane & 3;
   const int mi = lane >> 3, ri = lane & 7;
   const uint32_t kbase = smem_u32(kt);
 
-  // ---- S = Q K^T; one accumulator per scale group (int4), else one
+  // ---- S = Q K^T in fp16 with biased K codes; one accumulator per scale group
   float acc[NG][2][4];
 #pragma unroll
   for (int gi = 0; gi < NG; ++gi)
@@ -304,32 +284,35 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
       for (int nt = 0; nt < 2; ++nt) {
         const uint32_t w = r[nt * 2 + hh];
         if constexpr (KIND == KV_I8) {
-          uint32_t b0, b1;  // channels 16ch+4c+{0,1} and 16ch+4c+{2,3}
-          i8x4_to_bf16(w, b0, b1);
-          mma_bf16_16816(acc[0][nt], qa[ch], b0, b1);
+          const uint32_t x = w ^ 0x80808080u;  // bytes u = code + 128
+          mma_f16_16816(acc[0][nt], qa[ch], __byte_perm(x, 0x64646464u, 0x5140),
+                        __byte_perm(x, 0x64646464u, 0x7362));
         } else {
-          const uint32_t x = w ^ 0x88888888u;  // nibble k = channel 32ch + 8c + k
-          mma_bf16_16816(acc[ch][nt], qa[2 * ch], i4pair_to_bf16(x), i4pair_to_bf16(x >> 4));
-          mma_bf16_16816(acc[ch][nt], qa[2 * ch + 1], i4pair_to_bf16(x >> 8),
-                         i4pair_to_bf16(x >> 12));
+          const uint32_t x = w ^ 0x88888888u;  // nibble k = channel 32ch + 8c + k, u = code + 8
+          const uint32_t y = x >> 8;
+          mma_f16_16816(acc[ch][nt], qa[2 * ch], (x & 0x000F000Fu) | 0x64006400u,
+                        (y & 0x000F000Fu) | 0x64006400u);
+          mma_f16_16816(acc[ch][nt], qa[2 * ch + 1], (x & 0x00F000F0u) | 0x64006400u,
+                        (y & 0x00F000F0u) | 0x64006400u);
         }
       }
     }
   }
 
-  // ---- K scales, scale, mask by selection
+  // ---- remove the bias, apply K scales and the row scale, mask by selection
   float s[2][4];
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int key = nt * 8 + 2 * c + (e & 1);
+      const int hr = e >> 1;
       const float *sc = ksc + (row0 + key) * NG;
       float v = 0.f;
 #pragma unroll
-      for (int gi = 0; gi < NG; ++gi) v = fmaf(acc[gi][nt][e], sc[gi], v);
-      const int lim = (e < 2) ? lim0 : lim1;
-      s[nt][e] = (tok_row0 + key < lim) ? v * scale_log2 : -INFINITY;
+      for (int gi = 0; gi < NG; ++gi) v = fmaf(acc[gi][nt][e] - qc[hr][gi], sc[gi], v);
+      const int lim = hr ? lim1 : lim0;
+      s[nt][e] = (tok_row0 + key < lim) ? v * rs[hr] : -INFINITY;
     }
   }
   float p[2][4], al[2];
@@ -453,33 +436,89 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
   }
 }
 
-// Q A fragments in the channel order warp_block_q feeds K codes in.
-//  int8, k-step ks (a 16-byte chunk of 16 codes): thread c's slots (2c, 2c+1)
-//    are channels 16ks+4c+{0,1} and slots (2c+8, 2c+9) are 16ks+4c+{2,3}.
-//  int4, k-steps 2ch / 2ch+1 (chunk ch of 32 codes, base 32ch+8c): slots
-//    (2c, 2c+1) = base+{0,4} / base+{2,6}; (2c+8, 2c+9) = base+{1,5} / base+{3,7}.
+// Quantised caches run Q K^T in fp16. Each query row is scaled by an exact
+// power of two, 2^-e, so that its largest |q| lies in [2^14, 2^15): every bf16
+// value then converts to fp16 exactly (8 significant bits fit 11; values below
+// 2^-28 of the row max, which round, cannot move an fp32 dot product). The
+// K codes enter the product biased (see warp_block_q), and the bias is taken
+// back out of the fp32 scores with per-(row, group) constants:
+//   int8: K = 1024 + u, u = code + 128       -> c = 1152 * sum_d q'_d
+//   int4: even channels K = 1024 + u, odd channels K = 1024 + 16u with Q/16
+//         (u = code + 8)                      -> c_g = 1032 * sum_even q' + 72 * sum_odd q'
+// qinfo[r] = 2^e, qinfo[16 + r * NG + g] = c_g (fp32). 128 consumer threads,
+// 8 per row.
 template <class C, int KIND>
-__device__ __forceinline__ void build_q_fragments(const uint8_t *qs, uint32_t (&qa)[C::D / 16][4],
-                                                  int lane) {
+__device__ __forceinline__ void prepare_q_rows(const uint8_t *qs, float *qinfo, int tid) {
+  constexpr int D = C::D, NG = C::NG, PER = D / 8;  // channels per thread
+  const int row = tid >> 3, k = tid & 7;
+  const __nv_bfloat16 *q = reinterpret_cast<const __nv_bfloat16 *>(qs + row * C::QROW) + k * PER;
+  float v[PER];
+  float mx = 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    v[i] = __bfloat162float(q[i]);
+    mx = fmaxf(mx, fabsf(v[i]));
+  }
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+  int E = 0;
+  if (mx > 0.f && mx <= 3.0e38f) frexpf(mx, &E);
+  E = max(E, -100);  // keep 2^(15-E) finite for rows of tiny values
+  const float down = ldexpf(1.0f, 15 - E);  // exact power of two
+  float se = 0.f, so = 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    if (i & 1) so += v[i] * down;
+    else se += v[i] * down;
+  }
+  if constexpr (KIND == KV_I8) {
+    float c = 1152.0f * (se + so);
+    c += __shfl_xor_sync(0xffffffffu, c, 1);
+    c += __shfl_xor_sync(0xffffffffu, c, 2);
+    c += __shfl_xor_sync(0xffffffffu, c, 4);
+    if (k == 0) qinfo[16 + row] = c;
+  } else {
+    constexpr int TPG = 32 / PER;  // threads per 32-channel group
+    float c = 1032.0f * se + 72.0f * so;
+#pragma unroll
+    for (int o = 1; o < TPG; o <<= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if (k % TPG == 0) qinfo[16 + row * NG + k / TPG] = c;
+  }
+  if (k == 0) qinfo[row] = ldexpf(1.0f, E - 15);
+}
+
+// Q A fragments (fp16, prescaled) in the channel order warp_block_q feeds K in.
+//  int8, k-step ks (16-byte chunk of 16 codes): slots (2c, 2c+1) are channels
+//    16ks+4c+{0,1}, slots (2c+8, 2c+9) are 16ks+4c+{2,3}.
+//  int4, chunk ch of 32 codes, base = 32ch+8c: k-step 2ch has slots
+//    (2c, 2c+1) = base+{0,4}, (2c+8, 2c+9) = base+{2,6}; k-step 2ch+1 has
+//    base+{1,5} and base+{3,7}, divided by 16.
+template <class C, int KIND>
+__device__ __forceinline__ void build_q_fragments(const uint8_t *qs, const float *qinfo,
+                                                  uint32_t (&qa)[C::D / 16][4], int lane) {
   const int g = lane >> 2, c = lane & 3;
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
-    const uint8_t *row = qs + (g + 8 * half) * C::QROW;
+    const int row = g + 8 * half;
+    const __nv_bfloat16 *q = reinterpret_cast<const __nv_bfloat16 *>(qs + row * C::QROW);
+    const float down = 1.0f / qinfo[row];  // exact: qinfo[row] is a power of two
+    auto qv = [&](int d) { return __bfloat162float(q[d]) * down; };
     if constexpr (KIND == KV_I8) {
 #pragma unroll
       for (int ks = 0; ks < C::D / 16; ++ks) {
-        const uint2 v = *reinterpret_cast<const uint2 *>(row + (16 * ks + 4 * c) * 2);
-        qa[ks][half] = v.x;
-        qa[ks][2 + half] = v.y;
+        const int d = 16 * ks + 4 * c;
+        qa[ks][half] = pack_f16x2(qv(d), qv(d + 1));
+        qa[ks][2 + half] = pack_f16x2(qv(d + 2), qv(d + 3));
       }
     } else {
 #pragma unroll
       for (int ch = 0; ch < C::D / 32; ++ch) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(row + (32 * ch + 8 * c) * 2);
-        qa[2 * ch][half] = __byte_perm(v.x, v.z, 0x5410);          // base+0, base+4
-        qa[2 * ch][2 + half] = __byte_perm(v.x, v.z, 0x7632);      // base+1, base+5
-        qa[2 * ch + 1][half] = __byte_perm(v.y, v.w, 0x5410);      // base+2, base+6
-        qa[2 * ch + 1][2 + half] = __byte_perm(v.y, v.w, 0x7632);  // base+3, base+7
+        const int d = 32 * ch + 8 * c;
+        qa[2 * ch][half] = pack_f16x2(qv(d), qv(d + 4));
+        qa[2 * ch][2 + half] = pack_f16x2(qv(d + 2), qv(d + 6));
+        qa[2 * ch + 1][half] = pack_f16x2(qv(d + 1) * 0.0625f, qv(d + 5) * 0.0625f);
+        qa[2 * ch + 1][2 + half] = pack_f16x2(qv(d + 3) * 0.0625f, qv(d + 7) * 0.0625f);
       }
     }
   }
@@ -672,8 +711,18 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D>::THREADS, S1Cfg<KIND, D>::MIN_B
     }
     named_barrier(1, C::NUM_CW * 32);
     uint32_t qa[D / 16][4];
+    float qc[2][C::NG], rs[2];
     if constexpr (C::QUANT) {
-      build_q_fragments<C, KIND>(qs, qa, lane);
+      float *qinfo = reinterpret_cast<float *>(smem + C::OFF_QI);
+      prepare_q_rows<C, KIND>(qs, qinfo, threadIdx.x);
+      named_barrier(1, C::NUM_CW * 32);
+      build_q_fragments<C, KIND>(qs, qinfo, qa, lane);
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        rs[hr] = qinfo[g + 8 * hr] * p.scale_log2;
+#pragma unroll
+        for (int gi = 0; gi < C::NG; ++gi) qc[hr][gi] = qinfo[16 + (g + 8 * hr) * C::NG + gi];
+      }
     } else {
       const int mi = lane >> 3, ri = lane & 7;
       const int row = ((mi & 1) << 3) + ri;
@@ -715,8 +764,8 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D>::THREADS, S1Cfg<KIND, D>::MIN_B
         if constexpr (C::QUANT) {
           const float *ksc = reinterpret_cast<const float *>(vt + C::TILE);
           const float *vsc = ksc + C::BLOCK_N * C::NG;
-          warp_block_q<C, KIND>(kt, vt, ksc, vsc, row0, qa, o, m, l, tok_row0, c1, lim[0], lim[1],
-                                p.scale_log2, lane);
+          warp_block_q<C, KIND>(kt, vt, ksc, vsc, row0, qa, qc, rs, o, m, l, tok_row0, c1, lim[0],
+                                lim[1], lane);
         } else {
           if (tok_row0 + 16 > c1) {  // zero V rows past the split end before PV
             constexpr int CH = C::N_BOX * (C::BOX_BYTES / 16);
@@ -790,7 +839,7 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D>::THREADS, S1Cfg<KIND, D>::MIN_B
       float Lsum = 0.f;
 #pragma unroll
       for (int w = 0; w < C::NUM_CW; ++w) {
-        wt[w] = mw[w] == -INFINITY ? 0.f : exp2f(mw[w] - M);
+        wt[w] = mw[w] == -INFINITY ? 0.f : fast_exp2(mw[w] - M);
         Lsum = fmaf(wt[w], cl[w * 16 + row], Lsum);
       }
       const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;

@@ -45,23 +45,38 @@ __global__ void __launch_bounds__(kS2Warps * 32) fd_stage2_kernel(const __grid_c
 #pragma unroll
   for (int i = 0; i < VPL; ++i) acc[i] = 0.f;
   const float *op = p.o_part + static_cast<int64_t>(row) * S * D + lane * VPL;
-  for (int s = 0; s < S; ++s) {
-    const float wa = __shfl_sync(0xffffffffu, w0, s & 31);
-    const float wb = __shfl_sync(0xffffffffu, w1, s & 31);
-    const float w = s < 32 ? wa : wb;
-    if (w > 0.f) {
-      if constexpr (VPL == 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(op + s * D);
-        acc[0] = fmaf(w, v.x, acc[0]);
-        acc[1] = fmaf(w, v.y, acc[1]);
-        acc[2] = fmaf(w, v.z, acc[2]);
-        acc[3] = fmaf(w, v.w, acc[3]);
-      } else {
-        const float2 v = *reinterpret_cast<const float2 *>(op + s * D);
-        acc[0] = fmaf(w, v.x, acc[0]);
-        acc[1] = fmaf(w, v.y, acc[1]);
+  // Partials in groups of 8 splits, all loads of a group issued before use.
+  // Splits with weight 0 (empty, or far below the max) are not read.
+  constexpr int U = 8;
+  for (int s0 = 0; s0 < S; s0 += U) {
+    float w[U];
+    float v[U][VPL];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int s = s0 + u;
+      const float wa = __shfl_sync(0xffffffffu, w0, s & 31);
+      const float wb = __shfl_sync(0xffffffffu, w1, s & 31);
+      w[u] = s < S ? (s < 32 ? wa : wb) : 0.f;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) v[u][i] = 0.f;
+      if (w[u] > 0.f) {
+        if constexpr (VPL == 4) {
+          const float4 t = *reinterpret_cast<const float4 *>(op + s * D);
+          v[u][0] = t.x;
+          v[u][1] = t.y;
+          v[u][2] = t.z;
+          v[u][3] = t.w;
+        } else {
+          const float2 t = *reinterpret_cast<const float2 *>(op + s * D);
+          v[u][0] = t.x;
+          v[u][1] = t.y;
+        }
       }
     }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) acc[i] = fmaf(w[u], v[u][i], acc[i]);
   }
   const float inv = Z > 0.f ? 1.f / Z : 0.f;
   const int hq = row % p.Hq;
