@@ -25,6 +25,8 @@
  *  - Pointers inside fd_tensor are device pointers unless stated otherwise;
  *    the caller owns every tensor. The library never frees caller memory.
  *  - Work is enqueued on the given stream only (NULL = legacy default stream).
+ *  - A plan is not thread-safe: calls that use one plan from several host
+ *    threads at once must be serialised by the caller.
  */
 #ifndef FD_H_
 #define FD_H_

@@ -53,6 +53,23 @@ int heuristic_splits(const fd_plan *pl, int batch, int max_seqlen) {
   return std::min(s, pl->max_splits);
 }
 
+// Candidates: powers of two up to max_splits, plus the split counts that
+// fill one or two waves of one CTA per SM for this batch (e.g. 19 for one
+// request of 8 KV heads on 152 SMs), where a power of two leaves SMs idle.
+std::vector<int> candidate_splits(const fd_plan *pl, int batch) {
+  std::vector<int> c;
+  for (int S = 1; S <= pl->max_splits; S <<= 1) c.push_back(S);
+  const int G = pl->hq / pl->hkv;
+  const long base = static_cast<long>(batch) * pl->hkv * ((G * pl->max_q + 15) / 16);
+  for (int k = 1; k <= 2; ++k) {
+    const long sw = k * static_cast<long>(pl->num_sms) / base;
+    if (sw >= 2 && sw <= pl->max_splits && !is_pow2(static_cast<int>(sw))) c.push_back(static_cast<int>(sw));
+  }
+  std::sort(c.begin(), c.end());
+  c.erase(std::unique(c.begin(), c.end()), c.end());
+  return c;
+}
+
 const char *kv_name(fd_dtype t) {
   return t == FD_BF16 ? "bf16" : t == FD_INT8 ? "int8" : t == FD_INT4X2 ? "int4" : "x";
 }
@@ -404,7 +421,7 @@ fd_status fd_autotune(fd_plan *plan, const int *batch_sizes, int n_batch, int mi
     ++plan->searches;
     int best = 1;
     double best_t = 0.0;
-    for (int S = 1; S <= plan->max_splits; S <<= 1) {
+    for (int S : candidate_splits(plan, key.first)) {
       double t = 0.0;
       if (plan->timer) {
         t = plan->timer(plan->timer_user, key.first, key.second, S);

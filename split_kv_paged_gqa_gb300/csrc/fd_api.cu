@@ -280,6 +280,26 @@ fd_status encode_cache_map(CUtensorMap *map, const fd_tensor *c, const fd_plan *
   return FD_OK;
 }
 
+// The descriptor of a cache depends only on its pointer, shape and strides,
+// which a serving loop keeps fixed; re-encode only when they change.
+fd_status cached_cache_map(CUtensorMap *map, const fd_tensor *c, fd_plan *pl, int which) {
+  static_assert(sizeof(CUtensorMap) <= sizeof(pl->map_cache[0].map), "map cache slot");
+  fd_plan::MapEntry &e = pl->map_cache[which];
+  bool hit = e.valid && e.data == c->data;
+  for (int i = 0; hit && i < 4; ++i) hit = e.shape[i] == c->shape[i] && e.stride[i] == c->stride[i];
+  if (!hit) {
+    FD_TRY(encode_cache_map(reinterpret_cast<CUtensorMap *>(e.map), c, pl));
+    e.valid = true;
+    e.data = c->data;
+    for (int i = 0; i < 4; ++i) {
+      e.shape[i] = c->shape[i];
+      e.stride[i] = c->stride[i];
+    }
+  }
+  std::memcpy(map, e.map, sizeof(CUtensorMap));
+  return FD_OK;
+}
+
 }  // namespace
 
 extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cache,
@@ -377,8 +397,8 @@ extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cach
   if (!guard.ok) return fail(FD_ERR_CUDA, "cannot make device %d current", pl->device);
 
   CUtensorMap tmk, tmv;
-  FD_TRY(encode_cache_map(&tmk, k_cache, pl));
-  FD_TRY(encode_cache_map(&tmv, v_cache, pl));
+  FD_TRY(cached_cache_map(&tmk, k_cache, pl, 0));
+  FD_TRY(cached_cache_map(&tmv, v_cache, pl, 1));
 
   fd::Stage1Params p;
   std::memset(&p, 0, sizeof(p));
@@ -432,7 +452,9 @@ extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cach
     FD_CUDA_TRY(cudaEventRecord(ev[0], st));
   }
   dim3 grid(p.row_tiles * S, pl->hkv, B);
-  cudaError_t e = fd::launch_stage1(pl->kind, D, S == 1, tmk, tmv, p, grid, st);
+  const long ctas = static_cast<long>(grid.x) * grid.y * grid.z;
+  const bool deep = ctas <= pl->num_sms;  // one wave: one CTA per SM with a deeper ring
+  cudaError_t e = fd::launch_stage1(pl->kind, D, S == 1, deep, tmk, tmv, p, grid, st);
   if (pl->profiling) FD_CUDA_TRY(cudaEventRecord(ev[1], st));
   if (e != cudaSuccess) return fail(FD_ERR_CUDA, "stage-1 launch failed: %s (%d)", cudaGetErrorString(e), (int)e);
   if (S > 1) {

@@ -58,7 +58,8 @@ int stage1_block_n(int kind, int head_dim);
 // Raise the dynamic shared-memory limit of every stage-1 variant of (kind, D).
 cudaError_t stage1_prepare(int kind, int head_dim);
 
-cudaError_t launch_stage1(int kind, int head_dim, bool fused, const CUtensorMap &tmk,
+// deep: the one-CTA-per-SM deep-ring variant (bf16 cache; ignored otherwise).
+cudaError_t launch_stage1(int kind, int head_dim, bool fused, bool deep, const CUtensorMap &tmk,
                           const CUtensorMap &tmv, const Stage1Params &p, dim3 grid,
                           cudaStream_t stream);
 
@@ -68,13 +69,13 @@ cudaError_t launch_stage2(const Stage2Params &p, cudaStream_t stream, bool pdl);
 cudaError_t stage1_prepare_bf16(int head_dim);
 cudaError_t stage1_prepare_i8(int head_dim);
 cudaError_t stage1_prepare_i4(int head_dim);
-cudaError_t launch_stage1_bf16(int head_dim, bool fused, const CUtensorMap &tmk,
+cudaError_t launch_stage1_bf16(int head_dim, bool fused, bool deep, const CUtensorMap &tmk,
                                const CUtensorMap &tmv, const Stage1Params &p, dim3 grid,
                                cudaStream_t stream);
-cudaError_t launch_stage1_i8(int head_dim, bool fused, const CUtensorMap &tmk,
+cudaError_t launch_stage1_i8(int head_dim, bool fused, bool deep, const CUtensorMap &tmk,
                              const CUtensorMap &tmv, const Stage1Params &p, dim3 grid,
                              cudaStream_t stream);
-cudaError_t launch_stage1_i4(int head_dim, bool fused, const CUtensorMap &tmk,
+cudaError_t launch_stage1_i4(int head_dim, bool fused, bool deep, const CUtensorMap &tmk,
                              const CUtensorMap &tmv, const Stage1Params &p, dim3 grid,
                              cudaStream_t stream);
 

@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 
+#include <cstdint>
 #include <map>
 #include <string>
 #include <utility>
@@ -37,6 +38,17 @@ struct fd_plan {
   fd_timer_fn timer = nullptr;
   void *timer_user = nullptr;
   int searches = 0, cache_hits = 0;
+
+  // last encoded TMA descriptors of the K and V caches (host-side cache:
+  // encoding costs microseconds of CPU per call otherwise)
+  struct MapEntry {
+    bool valid = false;
+    const void *data = nullptr;
+    int64_t shape[4] = {0, 0, 0, 0};
+    int64_t stride[4] = {0, 0, 0, 0};
+    alignas(64) unsigned char map[128];
+  };
+  MapEntry map_cache[2];
 
   // per-stage timing events (fd_profile_begin / fd_profile_end)
   bool profiling = false;

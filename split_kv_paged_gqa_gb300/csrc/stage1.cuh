@@ -11,8 +11,8 @@
 // Structure of one CTA (NUM_CW consumer warps + 1 producer warp):
 //  * split range: chunk = P * ceil(ceil(L_b / S) / P); split s owns keys
 //    [s * chunk, min(L_b, (s + 1) * chunk)), derived here from cache_seqlens.
-//  * producer warp: reads page ids from the page table one stage ahead, and
-//    lane 0 issues 4-D TMA loads (d, head, slot, page) of whole page segments
+//  * producer warp: keeps page ids in a register window filled 32 pages
+//    ahead of use, and lane 0 issues 4-D TMA loads (d, head, slot, page) of whole page segments
 //    of K and V into a STAGES-deep shared-memory ring, 128-byte swizzled,
 //    completing on a per-stage mbarrier. Quantised caches also copy their
 //    per-row fp32 scales with cp.async (one arrival per lane on the barrier).
@@ -53,7 +53,7 @@
 
 namespace fd {
 
-template <int KIND, int D_>
+template <int KIND, int D_, bool DEEP = false>
 struct S1Cfg {
   static constexpr int D = D_;
   static constexpr bool QUANT = KIND != KV_BF16;
@@ -66,7 +66,9 @@ struct S1Cfg {
   static constexpr int BLOCK_N = 64;                     // keys per pipeline stage
   static constexpr int NUM_CW = 4;                       // consumer warps (16 keys each)
   static constexpr int THREADS = (NUM_CW + 1) * 32;
-  static constexpr int STAGES = KIND == KV_BF16 ? 3 : (KIND == KV_I8 ? 6 : 8);
+  // DEEP: one CTA per SM with a deeper ring, for grids that fit in one wave
+  // (small batches), where a single CTA must keep enough bytes in flight.
+  static constexpr int STAGES = KIND == KV_BF16 ? (DEEP ? 6 : 3) : (KIND == KV_I8 ? 6 : 8);
   static constexpr int TILE = BLOCK_N * ROW_BYTES;       // K (or V) bytes of one stage
   static constexpr int SC = QUANT ? BLOCK_N * NG * 4 : 0;
   static constexpr int STAGE = ((2 * TILE + 2 * SC) + 1023) / 1024 * 1024;
@@ -559,11 +561,11 @@ __device__ __forceinline__ void write_row_outputs(const Stage1Params &p, bool fu
   }
 }
 
-template <int KIND, int D, bool FUSED>
-__global__ void __launch_bounds__(S1Cfg<KIND, D>::THREADS, S1Cfg<KIND, D>::MIN_BLOCKS)
+template <int KIND, int D, bool FUSED, bool DEEP>
+__global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, DEEP>::MIN_BLOCKS)
     fd_stage1_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                      const __grid_constant__ Stage1Params p) {
-  using C = S1Cfg<KIND, D>;
+  using C = S1Cfg<KIND, D, DEEP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -620,29 +622,31 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D>::THREADS, S1Cfg<KIND, D>::MIN_B
     const int SEG = P < C::BLOCK_N ? P : C::BLOCK_N;  // slots per TMA box
     const unsigned seg_bytes = static_cast<unsigned>(SEG * C::ROW_BYTES);
 
-    auto load_pids = [&](int it, int &q0, int &q1) {
-      const int tok0 = c0 + it * C::BLOCK_N;
-      const int first = tok0 >> p.log2_page;
-      const int np = ((min(tok0 + C::BLOCK_N, c1) - 1) >> p.log2_page) - first + 1;
-      q0 = lane < np ? pt[first + lane] : 0;
-      q1 = lane + 32 < np ? pt[first + 32 + lane] : 0;
+    // Page ids live in a two-window register cache: lane i holds the id of
+    // page w0 + i (cur) and of page w0 + 32 + i (nxt, loaded 32 pages ahead),
+    // so the page-table latency stays off the critical path.
+    const int pg_end = (c1 + P - 1) >> p.log2_page;  // this split's pages: [c0 / P, pg_end)
+    auto load_win = [&](int base) { return base + lane < pg_end ? pt[base + lane] : 0; };
+    int w0 = c0 >> p.log2_page;
+    int cur = load_win(w0);
+    int nxt = load_win(w0 + 32);
+    auto pid_at = [&](int page) {  // page in [w0, w0 + 64); every lane must call it
+      const int idx = page - w0;
+      const int a0 = __shfl_sync(0xffffffffu, cur, idx & 31);
+      const int a1 = __shfl_sync(0xffffffffu, nxt, idx & 31);
+      return idx < 32 ? a0 : a1;
     };
-    int pn0, pn1;
-    load_pids(0, pn0, pn1);
     int issued = 0;
     for (int it = 0; it < n_iters; ++it) {
-      int p0 = pn0, p1 = pn1;
-      if (it + 1 < n_iters) load_pids(it + 1, pn0, pn1);
       const int tok0 = c0 + it * C::BLOCK_N;
       const int tend = min(tok0 + C::BLOCK_N, c1);
       const int first = tok0 >> p.log2_page;
-      const int np = ((tend - 1) >> p.log2_page) - first + 1;
-      // page ids outside the pool: record and redirect past the end (TMA zero-fills)
-      const bool bad0 = lane < np && (p0 < 0 || p0 >= p.num_pages);
-      const bool bad1 = lane + 32 < np && (p1 < 0 || p1 >= p.num_pages);
-      if (__any_sync(0xffffffffu, bad0 || bad1) && lane == 0) atomicOr(p.status, FD_DEVSTAT_BAD_PAGE);
-      if (bad0) p0 = p.num_pages;
-      if (bad1) p1 = p.num_pages;
+      const int np = ((tend - 1) >> p.log2_page) - first + 1;  // <= BLOCK_N / 8
+      if (first - w0 >= 32) {
+        cur = nxt;
+        w0 += 32;
+        nxt = load_win(w0 + 32);
+      }
 
       const int stage = it % C::STAGES;
       const unsigned ph = (it / C::STAGES) & 1;
@@ -652,10 +656,14 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D>::THREADS, S1Cfg<KIND, D>::MIN_B
       uint8_t *vt = kt + C::TILE;
       if (lane == 0) mbar_arrive_expect_tx(&full[stage], static_cast<unsigned>(np) * seg_bytes * 2u);
       for (int i = 0; i < np; ++i) {
-        const int a0 = __shfl_sync(0xffffffffu, p0, i & 31);
-        const int a1 = __shfl_sync(0xffffffffu, p1, i & 31);
+        int pid = pid_at(first + i);
         if (lane == 0) {
-          const int pid = i < 32 ? a0 : a1;
+          // a page id outside the pool is recorded and redirected past the end,
+          // where TMA fills zeros
+          if (pid < 0 || pid >= p.num_pages) {
+            atomicOr(p.status, FD_DEVSTAT_BAD_PAGE);
+            pid = p.num_pages;
+          }
           const int slot0 = P > C::BLOCK_N ? (tok0 & (P - 1)) : 0;
           const int row0 = P > C::BLOCK_N ? 0 : i * P;
 #pragma unroll
@@ -672,11 +680,8 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D>::THREADS, S1Cfg<KIND, D>::MIN_B
 #pragma unroll
         for (int i = lane; i < C::BLOCK_N; i += 32) {
           const int tok = tok0 + i;
-          const int pi = (tok >> p.log2_page) - first;
-          const int a0 = __shfl_sync(0xffffffffu, p0, pi & 31);
-          const int a1 = __shfl_sync(0xffffffffu, p1, pi & 31);
-          const int pid = pi < 32 ? a0 : a1;
-          if (tok < tend && pid < p.num_pages) {
+          const int pid = pid_at(min(tok, tend - 1) >> p.log2_page);
+          if (tok < tend && pid >= 0 && pid < p.num_pages) {
             const float *src = p.kv_scales + static_cast<int64_t>(pid) * p.sc_sp +
                                static_cast<int64_t>(tok & (P - 1)) * p.sc_ss +
                                static_cast<int64_t>(h) * p.sc_sh;
@@ -858,25 +863,42 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D>::THREADS, S1Cfg<KIND, D>::MIN_B
   griddep_launch_dependents();
 }
 
-template <int KIND, int D>
-cudaError_t stage1_prepare_t() {
-  using C = S1Cfg<KIND, D>;
-  cudaError_t e = cudaFuncSetAttribute(fd_stage1_kernel<KIND, D, false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(fd_stage1_kernel<KIND, D, true>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+template <int KIND, int D, bool FUSED, bool DEEP>
+cudaError_t set_smem_limit() {
+  return cudaFuncSetAttribute(fd_stage1_kernel<KIND, D, FUSED, DEEP>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, S1Cfg<KIND, D, DEEP>::SMEM_ALLOC);
 }
 
 template <int KIND, int D>
-cudaError_t launch_stage1_t(bool fused, const CUtensorMap &tmk, const CUtensorMap &tmv,
-                            const Stage1Params &p, dim3 grid, cudaStream_t stream) {
-  using C = S1Cfg<KIND, D>;
+cudaError_t stage1_prepare_t() {
+  cudaError_t e = set_smem_limit<KIND, D, false, false>();
+  if (e == cudaSuccess) e = set_smem_limit<KIND, D, true, false>();
+  if constexpr (KIND == KV_BF16) {
+    if (e == cudaSuccess) e = set_smem_limit<KIND, D, false, true>();
+    if (e == cudaSuccess) e = set_smem_limit<KIND, D, true, true>();
+  }
+  return e;
+}
+
+template <int KIND, int D, bool DEEP>
+cudaError_t launch_variant(bool fused, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                           const Stage1Params &p, dim3 grid, cudaStream_t stream) {
+  using C = S1Cfg<KIND, D, DEEP>;
   if (fused)
-    fd_stage1_kernel<KIND, D, true><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tmk, tmv, p);
+    fd_stage1_kernel<KIND, D, true, DEEP><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tmk, tmv, p);
   else
-    fd_stage1_kernel<KIND, D, false><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tmk, tmv, p);
+    fd_stage1_kernel<KIND, D, false, DEEP><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tmk, tmv, p);
   return cudaGetLastError();
+}
+
+// deep: one-wave grids of the bf16 cache use the deep-ring variant.
+template <int KIND, int D>
+cudaError_t launch_stage1_t(bool fused, bool deep, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                            const Stage1Params &p, dim3 grid, cudaStream_t stream) {
+  if constexpr (KIND == KV_BF16) {
+    if (deep) return launch_variant<KIND, D, true>(fused, tmk, tmv, p, grid, stream);
+  }
+  return launch_variant<KIND, D, false>(fused, tmk, tmv, p, grid, stream);
 }
 
 }  // namespace fd

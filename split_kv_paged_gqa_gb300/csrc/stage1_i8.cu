@@ -9,10 +9,10 @@ cudaError_t stage1_prepare_i8(int head_dim) {
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_stage1_i8(int head_dim, bool fused, const CUtensorMap &tmk, const CUtensorMap &tmv,
+cudaError_t launch_stage1_i8(int head_dim, bool fused, bool deep, const CUtensorMap &tmk, const CUtensorMap &tmv,
                            const Stage1Params &p, dim3 grid, cudaStream_t stream) {
-  if (head_dim == 128) return launch_stage1_t<KV_I8, 128>(fused, tmk, tmv, p, grid, stream);
-  if (head_dim == 64) return launch_stage1_t<KV_I8, 64>(fused, tmk, tmv, p, grid, stream);
+  if (head_dim == 128) return launch_stage1_t<KV_I8, 128>(fused, deep, tmk, tmv, p, grid, stream);
+  if (head_dim == 64) return launch_stage1_t<KV_I8, 64>(fused, deep, tmk, tmv, p, grid, stream);
   return cudaErrorInvalidValue;
 }
 

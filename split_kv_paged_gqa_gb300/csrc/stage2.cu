@@ -124,13 +124,13 @@ cudaError_t stage1_prepare(int kind, int head_dim) {
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_stage1(int kind, int head_dim, bool fused, const CUtensorMap &tmk,
+cudaError_t launch_stage1(int kind, int head_dim, bool fused, bool deep, const CUtensorMap &tmk,
                           const CUtensorMap &tmv, const Stage1Params &p, dim3 grid,
                           cudaStream_t stream) {
   switch (kind) {
-    case KV_BF16: return launch_stage1_bf16(head_dim, fused, tmk, tmv, p, grid, stream);
-    case KV_I8: return launch_stage1_i8(head_dim, fused, tmk, tmv, p, grid, stream);
-    case KV_I4: return launch_stage1_i4(head_dim, fused, tmk, tmv, p, grid, stream);
+    case KV_BF16: return launch_stage1_bf16(head_dim, fused, deep, tmk, tmv, p, grid, stream);
+    case KV_I8: return launch_stage1_i8(head_dim, fused, deep, tmk, tmv, p, grid, stream);
+    case KV_I4: return launch_stage1_i4(head_dim, fused, deep, tmk, tmv, p, grid, stream);
   }
   return cudaErrorInvalidValue;
 }

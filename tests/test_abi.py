@@ -196,10 +196,16 @@ def test_autotune_buckets_nearest_and_persistence(tmp_path, monkeypatch):
         timer, calls = _fake_timer(best)
         fd.fd_autotune_set_timer(plan, timer)
         fd.fd_autotune(plan, [1, 16], 1024, 8192)
-        # 2 batches x 4 buckets, 7 candidates each
+        # 2 batches x 4 buckets; every power of two up to 64 is tried for each key,
+        # plus split counts that fill one or two waves of the SMs
         assert fd.fd_autotune_stats(plan) == (8, 0)
-        assert len(calls) == 8 * 7
-        assert sorted({c[2] for c in calls}) == [1, 2, 4, 8, 16, 32, 64]
+        per_key = {}
+        for b, k, S in calls:
+            per_key.setdefault((b, k), []).append(S)
+        assert len(per_key) == 8
+        for S_list in per_key.values():
+            assert {1, 2, 4, 8, 16, 32, 64} <= set(S_list) and max(S_list) <= 64
+            assert len(S_list) == len(set(S_list))
         for b in (1, 16):
             for k in (1024, 2048, 4096, 8192):
                 assert fd.fd_query_splits(plan, b, k) == best(b, k)
@@ -234,7 +240,7 @@ def test_autotune_buckets_nearest_and_persistence(tmp_path, monkeypatch):
         # FD_FORCE_AUTOTUNE re-searches even cached keys
         monkeypatch.setenv("FD_FORCE_AUTOTUNE", "1")
         fd.fd_autotune(plan2, [16], 1024, 1024)
-        assert len(calls2) == 7
+        assert {1, 2, 4, 8, 16, 32, 64} <= {c[2] for c in calls2} and len(calls2) >= 7
     finally:
         fd.fd_plan_destroy(plan2)
 
