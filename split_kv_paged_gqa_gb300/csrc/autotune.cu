@@ -419,8 +419,7 @@ fd_status fd_autotune(fd_plan *plan, const int *batch_sizes, int n_batch, int mi
   }
   for (auto &key : todo) {
     ++plan->searches;
-    int best = 1;
-    double best_t = 0.0;
+    std::vector<std::pair<int, double>> timed;
     for (int S : candidate_splits(plan, key.first)) {
       double t = 0.0;
       if (plan->timer) {
@@ -429,11 +428,20 @@ fd_status fd_autotune(fd_plan *plan, const int *batch_sizes, int n_batch, int mi
         fd_status s = tune_time(plan, tb, key.first, key.second, S, st, &t);
         if (s != FD_OK) return s;
       }
-      if (S == 1 || t < best_t) {
-        best = S;
-        best_t = t;
-      }
+      timed.emplace_back(S, t);
     }
+    // Among the candidates within 2% of the fastest, take the most splits:
+    // uniform-length tuning inputs cannot show the imbalance of a mixed batch,
+    // which more (balanced) splits absorb.
+    double fastest = timed[0].second;
+    for (auto &c : timed) fastest = std::min(fastest, c.second);
+    int best = 0;
+    double best_t = 0.0;
+    for (auto &c : timed)
+      if (c.second <= fastest * 1.02 && c.first > best) {
+        best = c.first;
+        best_t = c.second;
+      }
     plan->table[key] = best;
     plan->table_time[key] = best_t;
   }

@@ -428,6 +428,10 @@ extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cach
   p.R = p.G * Tq;
   p.row_tiles = (p.R + 15) / 16;
   p.num_splits = S;
+  // Equal splits per request. (A common chunk derived from the batch's max
+  // length measured slower on mixed-length batches: short requests' small
+  // splits already backfill the SMs, and a common chunk leaves empty CTAs.)
+  p.chunk_min = 0;
   p.scale_log2 = pl->scale * 1.4426950408889634f;
   p.o_part = pl->o_part;
   p.lse_part = pl->lse_part;
@@ -466,6 +470,11 @@ extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cach
     p2.Hq = pl->hq;
     p2.D = D;
     p2.num_splits = S;
+    p2.seqlens = p.seqlens;
+    p2.sl_s = p.sl_s;
+    p2.log2_page = p.log2_page;
+    p2.max_pages = p.max_pages;
+    p2.chunk_min = p.chunk_min;
     p2.out = p.out;
     p2.out_f32 = p.out_f32;
     p2.o_sb = p.o_sb;

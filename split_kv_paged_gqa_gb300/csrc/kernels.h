@@ -10,6 +10,25 @@ namespace fd {
 
 enum KvKind : int { KV_BF16 = 0, KV_I8 = 1, KV_I4 = 2 };
 
+// Keys per split of a request with L keys: equal page-aligned chunks
+// P * ceil(ceil(L / S) / P), but never fewer than chunk_min keys. With
+// chunk_min derived from the batch's max length, every non-empty split of
+// every request holds about the same number of keys (load balance across a
+// mixed-length batch); requests shorter than the max use fewer splits.
+__host__ __device__ inline int split_chunk(int L, int S, int log2_page, int chunk_min) {
+  const int per = (L + S - 1) / S;
+  const int c = ((per + (1 << log2_page) - 1) >> log2_page) << log2_page;
+  return c > chunk_min ? c : chunk_min;
+}
+
+// Non-empty splits of a request with L keys.
+__host__ __device__ inline int split_count(int L, int S, int log2_page, int chunk_min) {
+  if (L <= 0) return 0;
+  const int c = split_chunk(L, S, log2_page, chunk_min);
+  const int n = (L + c - 1) / c;
+  return n < S ? n : S;
+}
+
 // Stage 1: one CTA per (row tile, split, KV head, request).
 struct Stage1Params {
   const __nv_bfloat16 *q;          // [B, Tq, Hq, D]
@@ -26,6 +45,7 @@ struct Stage1Params {
   int max_pages;                   // W
   int Tq, Hq, Hkv, G, R, row_tiles;
   int num_splits;                  // S
+  int chunk_min;                   // minimum keys per split (0: equal splits per request)
   float scale_log2;                // softmax_scale * log2(e)
   // split outputs (num_splits > 1): workspace rows [B, Tq, Hq, S] of D floats
   float *o_part;
@@ -44,6 +64,10 @@ struct Stage2Params {
   const float *o_part;
   const float *lse_part;
   int B, Tq, Hq, D, num_splits;
+  // the split geometry of stage 1: only the non-empty splits of a request are read
+  const int *seqlens;
+  int64_t sl_s;
+  int log2_page, max_pages, chunk_min;
   void *out;
   int out_f32;
   int64_t o_sb, o_st, o_sh;

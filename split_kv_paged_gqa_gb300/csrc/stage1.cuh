@@ -9,10 +9,11 @@
 // (row r = t * G + g), so K and V are read once per group ("GQA").
 //
 // Structure of one CTA (NUM_CW consumer warps + 1 producer warp):
-//  * split range: chunk = P * ceil(ceil(L_b / S) / P); split s owns keys
-//    [s * chunk, min(L_b, (s + 1) * chunk)), derived here from cache_seqlens.
-//  * producer warp: keeps page ids in a register window filled 32 pages
-//    ahead of use, and lane 0 issues 4-D TMA loads (d, head, slot, page) of whole page segments
+//  * split range: chunk = split_chunk(L_b, S, ...) (equal page-aligned chunks,
+//    at least chunk_min keys); split s owns keys [s * chunk, min(L_b, (s + 1) *
+//    chunk)), derived here from cache_seqlens.
+//  * producer warp: reads page ids from the page table one stage ahead, and
+//    lane 0 issues 4-D TMA loads (d, head, slot, page) of whole page segments
 //    of K and V into a STAGES-deep shared-memory ring, 128-byte swizzled,
 //    completing on a per-stage mbarrier. Quantised caches also copy their
 //    per-row fp32 scales with cp.async (one arrival per lane on the barrier).
@@ -584,12 +585,18 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
     if (threadIdx.x == 0) atomicOr(p.status, FD_DEVSTAT_SEQLEN_OVERFLOW);
     L = L < 0 ? 0 : cap;
   }
-  const int per = (L + p.num_splits - 1) / p.num_splits;
-  const int chunk = ((per + P - 1) >> p.log2_page) << p.log2_page;
+  const int chunk = split_chunk(L, p.num_splits, p.log2_page, p.chunk_min);
   const int c0 = s * chunk;
   const int c1 = min(L, c0 + chunk);
 
-  if (c0 >= c1) {  // empty split: zero partial (weight 0 in the merge) or empty final rows
+  if (c0 >= c1) {
+    // An empty split of a split call writes nothing: stage 2 reads only the
+    // split_count() non-empty splits. A request with no keys in an unsplit
+    // call gets out = 0, lse = -inf here.
+    if (!FUSED) {
+      griddep_launch_dependents();
+      return;
+    }
     const int ntile_rows = min(16, p.R - rt * 16);
     for (int i = threadIdx.x; i < ntile_rows * (D / 8); i += C::THREADS) {
       const int r = i / (D / 8), d0 = (i % (D / 8)) * 8;
@@ -622,48 +629,40 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
     const int SEG = P < C::BLOCK_N ? P : C::BLOCK_N;  // slots per TMA box
     const unsigned seg_bytes = static_cast<unsigned>(SEG * C::ROW_BYTES);
 
-    // Page ids live in a two-window register cache: lane i holds the id of
-    // page w0 + i (cur) and of page w0 + 32 + i (nxt, loaded 32 pages ahead),
-    // so the page-table latency stays off the critical path.
-    const int pg_end = (c1 + P - 1) >> p.log2_page;  // this split's pages: [c0 / P, pg_end)
-    auto load_win = [&](int base) { return base + lane < pg_end ? pt[base + lane] : 0; };
-    int w0 = c0 >> p.log2_page;
-    int cur = load_win(w0);
-    int nxt = load_win(w0 + 32);
-    auto pid_at = [&](int page) {  // page in [w0, w0 + 64); every lane must call it
-      const int idx = page - w0;
-      const int a0 = __shfl_sync(0xffffffffu, cur, idx & 31);
-      const int a1 = __shfl_sync(0xffffffffu, nxt, idx & 31);
-      return idx < 32 ? a0 : a1;
+    auto load_pids = [&](int it, int &q0, int &q1) {
+      const int tok0 = c0 + it * C::BLOCK_N;
+      const int first = tok0 >> p.log2_page;
+      const int np = ((min(tok0 + C::BLOCK_N, c1) - 1) >> p.log2_page) - first + 1;
+      q0 = lane < np ? pt[first + lane] : 0;
+      q1 = lane + 32 < np ? pt[first + 32 + lane] : 0;
     };
+    int pn0, pn1;
+    load_pids(0, pn0, pn1);
     int issued = 0;
     for (int it = 0; it < n_iters; ++it) {
+      int p0 = pn0, p1 = pn1;
+      if (it + 1 < n_iters) load_pids(it + 1, pn0, pn1);
       const int tok0 = c0 + it * C::BLOCK_N;
       const int tend = min(tok0 + C::BLOCK_N, c1);
       const int first = tok0 >> p.log2_page;
-      const int np = ((tend - 1) >> p.log2_page) - first + 1;  // <= BLOCK_N / 8
-      if (first - w0 >= 32) {
-        cur = nxt;
-        w0 += 32;
-        nxt = load_win(w0 + 32);
-      }
-
+      const int np = ((tend - 1) >> p.log2_page) - first + 1;
+      // page ids outside the pool: record and redirect past the end (TMA zero-fills)
+      const bool bad0 = lane < np && (p0 < 0 || p0 >= p.num_pages);
+      const bool bad1 = lane + 32 < np && (p1 < 0 || p1 >= p.num_pages);
+      if (__any_sync(0xffffffffu, bad0 || bad1) && lane == 0) atomicOr(p.status, FD_DEVSTAT_BAD_PAGE);
+      if (bad0) p0 = p.num_pages;
+      if (bad1) p1 = p.num_pages;
       const int stage = it % C::STAGES;
       const unsigned ph = (it / C::STAGES) & 1;
       if (!mbar_wait_warp(&empty[stage], ph ^ 1, p.status)) break;
-
       uint8_t *kt = smem + stage * C::STAGE;
       uint8_t *vt = kt + C::TILE;
       if (lane == 0) mbar_arrive_expect_tx(&full[stage], static_cast<unsigned>(np) * seg_bytes * 2u);
       for (int i = 0; i < np; ++i) {
-        int pid = pid_at(first + i);
+        const int a0 = __shfl_sync(0xffffffffu, p0, i & 31);
+        const int a1 = __shfl_sync(0xffffffffu, p1, i & 31);
         if (lane == 0) {
-          // a page id outside the pool is recorded and redirected past the end,
-          // where TMA fills zeros
-          if (pid < 0 || pid >= p.num_pages) {
-            atomicOr(p.status, FD_DEVSTAT_BAD_PAGE);
-            pid = p.num_pages;
-          }
+          const int pid = i < 32 ? a0 : a1;
           const int slot0 = P > C::BLOCK_N ? (tok0 & (P - 1)) : 0;
           const int row0 = P > C::BLOCK_N ? 0 : i * P;
 #pragma unroll
@@ -680,8 +679,11 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
 #pragma unroll
         for (int i = lane; i < C::BLOCK_N; i += 32) {
           const int tok = tok0 + i;
-          const int pid = pid_at(min(tok, tend - 1) >> p.log2_page);
-          if (tok < tend && pid >= 0 && pid < p.num_pages) {
+          const int pi = (tok >> p.log2_page) - first;
+          const int a0 = __shfl_sync(0xffffffffu, p0, pi & 31);
+          const int a1 = __shfl_sync(0xffffffffu, p1, pi & 31);
+          const int pid = pi < 32 ? a0 : a1;
+          if (tok < tend && pid < p.num_pages) {
             const float *src = p.kv_scales + static_cast<int64_t>(pid) * p.sc_sp +
                                static_cast<int64_t>(tok & (P - 1)) * p.sc_ss +
                                static_cast<int64_t>(h) * p.sc_sh;

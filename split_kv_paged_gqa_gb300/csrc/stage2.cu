@@ -6,8 +6,9 @@
 // row (request, query token, query head) with split partials (o_s, lse_s):
 //   M = max_s lse_s,  w_s = exp(lse_s - M),  out = sum_s w_s o_s / sum_s w_s,
 //   lse = M + ln(sum_s w_s).
-// Splits with lse_s = -inf carry weight 0 and are skipped by selection; a row
-// whose splits are all empty gets out = 0, lse = -inf. One warp per row; the
+// Only the non-empty splits of the row's request (split_count of its length)
+// are read; splits with lse_s = -inf carry weight 0 and are skipped by
+// selection; a row whose splits are all empty gets out = 0, lse = -inf. One warp per row; the
 // split partials of a row are contiguous (S x D fp32) and read coalesced.
 // Launched with programmatic dependent launch: the grid may start while stage 1
 // drains and waits on griddepcontrol before touching the workspace.
@@ -29,9 +30,14 @@ __global__ void __launch_bounds__(kS2Warps * 32) fd_stage2_kernel(const __grid_c
   const int lane = threadIdx.x & 31;
   if (row >= p.B * p.Tq * p.Hq) return;
   const int S = p.num_splits;
+  const int b_row = row / (p.Hq * p.Tq);
+  int L = p.seqlens[b_row * p.sl_s];
+  const int cap = p.max_pages << p.log2_page;
+  L = L < 0 ? 0 : (L > cap ? cap : L);  // as stage 1 clamps it
+  const int nv = split_count(L, S, p.log2_page, p.chunk_min);  // splits stage 1 wrote
   const float *lp = p.lse_part + static_cast<int64_t>(row) * S;
-  const float l0 = lane < S ? lp[lane] : -INFINITY;
-  const float l1 = lane + 32 < S ? lp[lane + 32] : -INFINITY;
+  const float l0 = lane < nv ? lp[lane] : -INFINITY;
+  const float l1 = lane + 32 < nv ? lp[lane + 32] : -INFINITY;
   float M = fmaxf(l0, l1);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -48,7 +54,7 @@ __global__ void __launch_bounds__(kS2Warps * 32) fd_stage2_kernel(const __grid_c
   // Partials in groups of 8 splits, all loads of a group issued before use.
   // Splits with weight 0 (empty, or far below the max) are not read.
   constexpr int U = 8;
-  for (int s0 = 0; s0 < S; s0 += U) {
+  for (int s0 = 0; s0 < nv; s0 += U) {
     float w[U];
     float v[U][VPL];
 #pragma unroll
@@ -56,7 +62,7 @@ __global__ void __launch_bounds__(kS2Warps * 32) fd_stage2_kernel(const __grid_c
       const int s = s0 + u;
       const float wa = __shfl_sync(0xffffffffu, w0, s & 31);
       const float wb = __shfl_sync(0xffffffffu, w1, s & 31);
-      w[u] = s < S ? (s < 32 ? wa : wb) : 0.f;
+      w[u] = s < nv ? (s < 32 ? wa : wb) : 0.f;
 #pragma unroll
       for (int i = 0; i < VPL; ++i) v[u][i] = 0.f;
       if (w[u] > 0.f) {

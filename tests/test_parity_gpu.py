@@ -92,6 +92,28 @@ def test_cross_split_agreement(kind):
 
 
 # ---------------------------------------------------------------------------
+# mixed lengths with any max-length hint (exact, stale, loose) and many splits
+
+
+@pytest.mark.parametrize("kind", ["bf16", "int8", "int4"])
+def test_mixed_lengths_with_max_length_hints(kind):
+    Tq = 4 if kind == "int4" else 1
+    shape = _shape(kind, 5, Tq, 32, 8, 128, 16, (50, 3000, 12000, 700, 4))
+    w = wl.make_workload(shape, 77, "cuda", poison=True)
+    ref_out, ref_lse = decode_ref_inputs(wl.oracle_inputs(w))
+    plan = fd.fd_plan_create(0, 5, Tq, 32, 8, 128, 16, kind, 64)
+    try:
+        for hint in (12000, 1000, 16384):          # exact, stale (too small), loose
+            fd.fd_set_max_seqlen_hint(plan, hint)
+            for S in (4, 16, 64):
+                out32, lse32 = run(w, S, torch.float32, plan=plan)
+                assert_parity(out32, lse32, ref_out, ref_lse, label=f"{kind} hint={hint} S={S}")
+    finally:
+        fd.fd_set_plan(None)
+        fd.fd_plan_destroy(plan)
+
+
+# ---------------------------------------------------------------------------
 # edge cases
 
 
