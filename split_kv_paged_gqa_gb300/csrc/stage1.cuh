@@ -69,7 +69,13 @@ struct S1Cfg {
   static constexpr int THREADS = (NUM_CW + 1) * 32;
   // DEEP: one CTA per SM with a deeper ring, for grids that fit in one wave
   // (small batches), where a single CTA must keep enough bytes in flight.
-  static constexpr int STAGES = KIND == KV_BF16 ? (DEEP ? 6 : 3) : (KIND == KV_I8 ? 6 : 8);
+  // Quantised kinds are bound by the consumer warps' latency, not by bytes in
+  // flight: they run three CTAs per SM with shorter rings.
+  static constexpr int STAGES = KIND == KV_BF16 ? (DEEP ? 6 : 3) : (KIND == KV_I8 ? 3 : 6);
+  // Quantised kinds park the (identical) Q fragments of the consumer warps in
+  // shared memory and reload them per block, so they do not hold 32 registers
+  // through the PV half of the loop (three CTAs per SM allow 128 registers).
+  static constexpr bool QA_SMEM = QUANT;
   static constexpr int TILE = BLOCK_N * ROW_BYTES;       // K (or V) bytes of one stage
   static constexpr int SC = QUANT ? BLOCK_N * NG * 4 : 0;
   static constexpr int STAGE = ((2 * TILE + 2 * SC) + 1023) / 1024 * 1024;
@@ -82,10 +88,15 @@ struct S1Cfg {
   static constexpr int OFF_Q = RING;
   static constexpr int OFF_QI = OFF_Q + QB;              // per row: 2^e, then NG bias constants
   static constexpr int QI = QUANT ? 16 * (1 + NG) * 4 : 0;
-  static constexpr int OFF_BAR = (OFF_QI + QI + 7) / 8 * 8;
+  static constexpr int OFF_QA = (OFF_QI + QI + 15) / 16 * 16;  // [D/16][32 lanes] uint4
+  static constexpr int QAB = QA_SMEM ? (D / 16) * 32 * 16 : 0;
+  static constexpr int OFF_BAR = (OFF_QA + QAB + 7) / 8 * 8;
   static constexpr int SMEM = OFF_BAR + 2 * STAGES * 8;
   static constexpr int SMEM_ALLOC = SMEM + 1024;         // slack to align the base to 1024
-  static constexpr int MIN_BLOCKS = SMEM_ALLOC * 2 <= 227 * 1024 ? 2 : 1;
+  // CTAs per SM the shared memory allows (228 KB per SM, 1 KB reserved per CTA)
+  static constexpr int MIN_BLOCKS = 3 * (SMEM_ALLOC + 1024) <= 228 * 1024   ? 3
+                                    : 2 * (SMEM_ALLOC + 1024) <= 228 * 1024 ? 2
+                                                                             : 1;
   static_assert(CMB <= RING, "combine tile must fit in the ring");
   static_assert(TILE % 1024 == 0, "tiles must keep the 1024-byte swizzle alignment");
   static_assert(D == 64 || D == 128, "head_dim");
@@ -267,14 +278,19 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
   const int mi = lane >> 3, ri = lane & 7;
   const uint32_t kbase = smem_u32(kt);
 
-  // ---- S = Q K^T in fp16 with biased K codes; one accumulator per scale group
-  float acc[NG][2][4];
+  // ---- S = Q K^T in fp16 with biased K codes. Each 16-byte chunk of a K row
+  // is one scale group for int4 (32 channels); its accumulator is folded into
+  // the scores as soon as its products are done: sv = sum_g ks_g (acc_g - c_g).
+  float sv[2][4];
 #pragma unroll
-  for (int gi = 0; gi < NG; ++gi)
+  for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int e = 0; e < 4; ++e) sv[nt][e] = 0.f;
+  float acc8[2][4];  // int8: one accumulator over all chunks
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[gi][nt][e] = 0.f;
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc8[nt][e] = 0.f;
   const int krow = row0 + ((mi >> 1) << 3) + ri;
 #pragma unroll
   for (int kc = 0; kc < CH; kc += 2) {
@@ -283,26 +299,47 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int ch = kc + hh;
+      if constexpr (KIND == KV_I8) {
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const uint32_t w = r[nt * 2 + hh];
-        if constexpr (KIND == KV_I8) {
-          const uint32_t x = w ^ 0x80808080u;  // bytes u = code + 128
-          mma_f16_16816(acc[0][nt], qa[ch], __byte_perm(x, 0x64646464u, 0x5140),
+        for (int nt = 0; nt < 2; ++nt) {
+          const uint32_t x = r[nt * 2 + hh] ^ 0x80808080u;  // bytes u = code + 128
+          mma_f16_16816(acc8[nt], qa[ch], __byte_perm(x, 0x64646464u, 0x5140),
                         __byte_perm(x, 0x64646464u, 0x7362));
-        } else {
-          const uint32_t x = w ^ 0x88888888u;  // nibble k = channel 32ch + 8c + k, u = code + 8
+        }
+      } else {
+        float acc[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+          const uint32_t x = r[nt * 2 + hh] ^ 0x88888888u;  // nibble k = channel 32ch + 8c + k
           const uint32_t y = x >> 8;
-          mma_f16_16816(acc[ch][nt], qa[2 * ch], (x & 0x000F000Fu) | 0x64006400u,
+          mma_f16_16816(acc[nt], qa[2 * ch], (x & 0x000F000Fu) | 0x64006400u,
                         (y & 0x000F000Fu) | 0x64006400u);
-          mma_f16_16816(acc[ch][nt], qa[2 * ch + 1], (x & 0x00F000F0u) | 0x64006400u,
+          mma_f16_16816(acc[nt], qa[2 * ch + 1], (x & 0x00F000F0u) | 0x64006400u,
                         (y & 0x00F000F0u) | 0x64006400u);
         }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int key = nt * 8 + 2 * c + (e & 1);
+            sv[nt][e] = fmaf(acc[nt][e] - qc[e >> 1][ch], ksc[(row0 + key) * NG + ch], sv[nt][e]);
+          }
       }
     }
   }
+  if constexpr (KIND == KV_I8) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = nt * 8 + 2 * c + (e & 1);
+        sv[nt][e] = (acc8[nt][e] - qc[e >> 1][0]) * ksc[row0 + key];
+      }
+  }
 
-  // ---- remove the bias, apply K scales and the row scale, mask by selection
+  // ---- row scale, mask by selection
   float s[2][4];
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
@@ -310,12 +347,8 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
     for (int e = 0; e < 4; ++e) {
       const int key = nt * 8 + 2 * c + (e & 1);
       const int hr = e >> 1;
-      const float *sc = ksc + (row0 + key) * NG;
-      float v = 0.f;
-#pragma unroll
-      for (int gi = 0; gi < NG; ++gi) v = fmaf(acc[gi][nt][e] - qc[hr][gi], sc[gi], v);
       const int lim = hr ? lim1 : lim0;
-      s[nt][e] = (tok_row0 + key < lim) ? v * rs[hr] : -INFINITY;
+      s[nt][e] = (tok_row0 + key < lim) ? sv[nt][e] * rs[hr] : -INFINITY;
     }
   }
   float p[2][4], al[2];
@@ -724,6 +757,15 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
       prepare_q_rows<C, KIND>(qs, qinfo, threadIdx.x);
       named_barrier(1, C::NUM_CW * 32);
       build_q_fragments<C, KIND>(qs, qinfo, qa, lane);
+      if constexpr (C::QA_SMEM) {
+        if (warp == 0) {
+          uint4 *qa_s = reinterpret_cast<uint4 *>(smem + C::OFF_QA);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            qa_s[ks * 32 + lane] = make_uint4(qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+        }
+        named_barrier(1, C::NUM_CW * 32);
+      }
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         rs[hr] = qinfo[g + 8 * hr] * p.scale_log2;
@@ -771,8 +813,23 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
         if constexpr (C::QUANT) {
           const float *ksc = reinterpret_cast<const float *>(vt + C::TILE);
           const float *vsc = ksc + C::BLOCK_N * C::NG;
-          warp_block_q<C, KIND>(kt, vt, ksc, vsc, row0, qa, qc, rs, o, m, l, tok_row0, c1, lim[0],
-                                lim[1], lane);
+          if constexpr (C::QA_SMEM) {
+            uint32_t qb[D / 16][4];
+            const uint4 *qa_s = reinterpret_cast<const uint4 *>(smem + C::OFF_QA);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint4 v = qa_s[ks * 32 + lane];
+              qb[ks][0] = v.x;
+              qb[ks][1] = v.y;
+              qb[ks][2] = v.z;
+              qb[ks][3] = v.w;
+            }
+            warp_block_q<C, KIND>(kt, vt, ksc, vsc, row0, qb, qc, rs, o, m, l, tok_row0, c1, lim[0],
+                                  lim[1], lane);
+          } else {
+            warp_block_q<C, KIND>(kt, vt, ksc, vsc, row0, qa, qc, rs, o, m, l, tok_row0, c1, lim[0],
+                                  lim[1], lane);
+          }
         } else {
           if (tok_row0 + 16 > c1) {  // zero V rows past the split end before PV
             constexpr int CH = C::N_BOX * (C::BOX_BYTES / 16);
