@@ -152,6 +152,11 @@ fd_status fd_plan_create(int device, int max_batch, int max_q_per_req, int num_q
   pl->max_splits = max_splits;
   pl->scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
   if (const char *dir = std::getenv("FD_AUTOTUNE_CACHE_DIR")) pl->cache_dir = dir;
+  // Split merge: the stage-2 kernel (default) or, with FD_MERGE=fused, the
+  // last split CTA of each tile (measured slower on GB300: the tail merge
+  // lengthens the critical path more than the second launch costs).
+  const char *mg = std::getenv("FD_MERGE");
+  pl->merge_kernel = !(mg && std::strcmp(mg, "fused") == 0);
 
   if (device >= 0) {
     fd::DeviceGuard guard(device);
@@ -169,6 +174,10 @@ fd_status fd_plan_create(int device, int max_batch, int max_q_per_req, int num_q
     if (e == cudaSuccess && max_splits > 1) e = cudaMalloc(&pl->lse_part, pl->ws_rows * sizeof(float));
     if (e == cudaSuccess) e = cudaMalloc(&pl->status, sizeof(unsigned));
     if (e == cudaSuccess) e = cudaMemset(pl->status, 0, sizeof(unsigned));
+    pl->n_counters = static_cast<size_t>(max_batch) * num_kv_heads *
+                     ((num_q_heads / num_kv_heads * max_q_per_req + 15) / 16);
+    if (e == cudaSuccess && max_splits > 1) e = cudaMalloc(&pl->counters, pl->n_counters * sizeof(unsigned));
+    if (e == cudaSuccess && max_splits > 1) e = cudaMemset(pl->counters, 0, pl->n_counters * sizeof(unsigned));
     if (e == cudaSuccess) e = fd::stage1_prepare(kind, head_dim);
     if (e == cudaSuccess && !encode_fn()) e = cudaErrorSymbolNotFound;
     if (e != cudaSuccess) {
@@ -190,6 +199,7 @@ fd_status fd_plan_destroy(fd_plan *plan) {
     if (plan->o_part) cudaFree(plan->o_part);
     if (plan->lse_part) cudaFree(plan->lse_part);
     if (plan->status) cudaFree(plan->status);
+    if (plan->counters) cudaFree(plan->counters);
   }
   delete plan;
   return FD_OK;
@@ -204,7 +214,7 @@ fd_plan *fd_get_plan(void) { return g_plan; }
 
 fd_status fd_plan_workspace_bytes(fd_plan *plan, size_t *bytes) {
   if (!plan || !bytes) return fail(FD_ERR_INVALID_ARG, "NULL argument");
-  *bytes = plan->o_part ? plan->ws_rows * (plan->d + 1) * sizeof(float) : 0;
+  *bytes = plan->o_part ? plan->ws_rows * (plan->d + 1) * sizeof(float) + plan->n_counters * sizeof(unsigned) : 0;
   return FD_OK;
 }
 
@@ -224,6 +234,8 @@ fd_status fd_read_device_status(fd_plan *plan, int *code) {
   FD_CUDA_TRY(cudaDeviceSynchronize());
   FD_CUDA_TRY(cudaMemcpy(&v, plan->status, sizeof(v), cudaMemcpyDeviceToHost));
   FD_CUDA_TRY(cudaMemset(plan->status, 0, sizeof(unsigned)));
+  // after an abandoned call the merge counters may be mid-count: start over
+  if (v && plan->counters) FD_CUDA_TRY(cudaMemset(plan->counters, 0, plan->n_counters * sizeof(unsigned)));
   *code = static_cast<int>(v);
   if (v) return fail(FD_ERR_DEVICE_STATUS, "device status 0x%x", v);
   return FD_OK;
@@ -447,6 +459,7 @@ extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cach
     p.l_sh = lse->stride[2];
   }
   p.status = pl->status;
+  p.counters = (S > 1 && !pl->merge_kernel) ? pl->counters : nullptr;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
@@ -461,7 +474,7 @@ extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cach
   cudaError_t e = fd::launch_stage1(pl->kind, D, S == 1, deep, tmk, tmv, p, grid, st);
   if (pl->profiling) FD_CUDA_TRY(cudaEventRecord(ev[1], st));
   if (e != cudaSuccess) return fail(FD_ERR_CUDA, "stage-1 launch failed: %s (%d)", cudaGetErrorString(e), (int)e);
-  if (S > 1) {
+  if (S > 1 && !p.counters) {
     fd::Stage2Params p2;
     p2.o_part = pl->o_part;
     p2.lse_part = pl->lse_part;

@@ -3,8 +3,8 @@
 // Some callers cannot call cudaMalloc. A serving engine may have reserved all
 // of the GPU's memory for its own pool before it loads this library. A plugin
 // may live inside a host process that forbids foreign device allocations.
-// For such callers, fd_decode_paged_static runs the same stage-1 / stage-2
-// kernels as fd_decode_paged, but without a plan. The split workspace is a
+// For such callers, fd_decode_paged_static runs the same kernels as
+// fd_decode_paged, but without a plan. The split workspace is a
 // fixed array in this file (kStaticScratchBytes, 32 MiB). The library holds
 // that array on every GPU that loads it, until the process exits.
 //
@@ -13,6 +13,11 @@
 //  * it looks up the array's device address with cudaGetSymbolAddress;
 //  * it raises the kernels' shared-memory limit.
 // Make that first call before any stream capture.
+//
+// The array holds the fp32 split partials and, after them, one merge counter
+// per (request, KV head, tile of 16 query rows). The counters start at zero
+// (the array is zeroed when the library's device code loads) and every
+// completed call leaves them at zero.
 //
 // The call never allocates. It rejects a workspace need larger than the array
 // with FD_ERR_WORKSPACE. All calls share the array; calls that overlap on the
@@ -105,7 +110,9 @@ extern "C" fd_status fd_decode_paged_static(const fd_tensor *q, const fd_tensor 
   if (B < 1 || B > 65535 || Tq < 1 || Tq > 64 || Hkv < 1 || Hq < 1 || Hq % Hkv)
     return fd::fail(FD_ERR_INVALID_ARG, "bad batch / query tokens / head counts");
   const size_t rows = static_cast<size_t>(B) * Tq * Hq * num_splits;
-  const size_t need = num_splits > 1 ? rows * (static_cast<size_t>(D) + 1) * sizeof(float) : 0;
+  const size_t n_ctr = static_cast<size_t>(B) * Hkv * ((Hq / Hkv * Tq + 15) / 16);
+  const size_t need =
+      num_splits > 1 ? rows * (static_cast<size_t>(D) + 1) * sizeof(float) + n_ctr * sizeof(unsigned) : 0;
   if (need > kStaticScratchBytes)
     return fd::fail(FD_ERR_WORKSPACE,
                     "this call needs %zu bytes of split workspace (batch x tokens x heads x splits = %zu rows "
@@ -140,6 +147,10 @@ extern "C" fd_status fd_decode_paged_static(const fd_tensor *q, const fd_tensor 
   pl.lse_part = s.scratch + rows * D;
   pl.ws_rows = rows;
   pl.status = s.status;
+  // merge counters after the partials: zero when the array is loaded, and every
+  // call leaves them at zero again (the last split of a tile resets its counter)
+  pl.counters = reinterpret_cast<unsigned *>(s.scratch + rows * (D + 1));
+  pl.n_counters = n_ctr;
 
   fd_plan *prev = fd_get_plan();
   fd_set_plan(&pl);

@@ -57,6 +57,9 @@ struct Stage1Params {
   float *lse;
   int64_t l_sb, l_st, l_sh;
   unsigned *status;
+  // Fused merge (num_splits > 1): one counter per (request, KV head, row
+  // tile); the last split CTA to finish merges the tile. Null: stage 2 merges.
+  unsigned *counters;
 };
 
 // Stage 2: one warp per (request, query token, query head).
@@ -75,8 +78,8 @@ struct Stage2Params {
   int64_t l_sb, l_st, l_sh;
 };
 
-// Tokens per pipeline stage of the stage-1 kernel (the TMA box height is
-// min(page_size, this)).
+// Slots per TMA box of the stage-1 kernel: a box holds min(page_size, this)
+// rows of one page and head.
 int stage1_block_n(int kind, int head_dim);
 
 // Raise the dynamic shared-memory limit of every stage-1 variant of (kind, D).

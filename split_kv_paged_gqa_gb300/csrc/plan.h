@@ -27,6 +27,9 @@ struct fd_plan {
   float *lse_part = nullptr;  // [max_batch * max_q * hq * max_splits]
   size_t ws_rows = 0;
   unsigned *status = nullptr;
+  unsigned *counters = nullptr;  // [max_batch * hkv * max row tiles], fused split merge
+  size_t n_counters = 0;
+  bool merge_kernel = true;      // merge splits with the stage-2 kernel (FD_MERGE=fused: in stage 1)
 
   // num_splits selection
   int seqlen_hint = 0;

@@ -64,14 +64,18 @@ struct S1Cfg {
   static constexpr int BOX_ELEMS = KIND == KV_BF16 ? BOX_BYTES / 2 : BOX_BYTES;
   static constexpr int NG = KIND == KV_I4 ? D / 32 : 1;  // fp32 scales per cache row
   static constexpr int NT = D / 8;                       // PV n-tiles (channels per thread, quantised V)
-  static constexpr int BLOCK_N = 64;                     // keys per pipeline stage
-  static constexpr int NUM_CW = 4;                       // consumer warps (16 keys each)
+  // keys per pipeline stage; the deep (one CTA per SM) variant doubles the
+  // consumer warps so a lone CTA has more blocks in flight
+  static constexpr int BLOCK_N = DEEP ? 128 : 64;
+  static constexpr int NUM_CW = BLOCK_N / 16;            // consumer warps (16 keys each)
+  static constexpr int SEG_MAX = 64;                     // slots per TMA box at most
   static constexpr int THREADS = (NUM_CW + 1) * 32;
-  // DEEP: one CTA per SM with a deeper ring, for grids that fit in one wave
-  // (small batches), where a single CTA must keep enough bytes in flight.
+  // DEEP: one CTA per SM with 8 consumer warps and 64 KB stages, for grids
+  // that fit in one wave (small batches), where a single CTA must keep enough
+  // bytes and blocks in flight.
   // Quantised kinds are bound by the consumer warps' latency, not by bytes in
   // flight: they run three CTAs per SM with shorter rings.
-  static constexpr int STAGES = KIND == KV_BF16 ? (DEEP ? 6 : 3) : (KIND == KV_I8 ? 3 : 6);
+  static constexpr int STAGES = KIND == KV_BF16 ? 3 : (KIND == KV_I8 ? 3 : 6);
   // Quantised kinds park the (identical) Q fragments of the consumer warps in
   // shared memory and reload them per block, so they do not hold 32 registers
   // through the PV half of the loop (three CTAs per SM allow 128 registers).
@@ -91,7 +95,8 @@ struct S1Cfg {
   static constexpr int OFF_QA = (OFF_QI + QI + 15) / 16 * 16;  // [D/16][32 lanes] uint4
   static constexpr int QAB = QA_SMEM ? (D / 16) * 32 * 16 : 0;
   static constexpr int OFF_BAR = (OFF_QA + QAB + 7) / 8 * 8;
-  static constexpr int SMEM = OFF_BAR + 2 * STAGES * 8;
+  static constexpr int OFF_FLAG = OFF_BAR + 2 * STAGES * 8;  // "this CTA merges" flag
+  static constexpr int SMEM = OFF_FLAG + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;         // slack to align the base to 1024
   // CTAs per SM the shared memory allows (228 KB per SM, 1 KB reserved per CTA)
   static constexpr int MIN_BLOCKS = 3 * (SMEM_ALLOC + 1024) <= 228 * 1024   ? 3
@@ -595,6 +600,79 @@ __device__ __forceinline__ void write_row_outputs(const Stage1Params &p, bool fu
   }
 }
 
+// The merge of the last split CTA of a tile: for each of the tile's rows, the
+// nv non-empty split partials (o_s, lse_s) combine as
+//   M = max_s lse_s, w_s = exp(lse_s - M), out = sum w_s o_s / sum w_s,
+//   lse = M + ln(sum w_s)
+// (the stage-2 merge). One warp per row, lanes over the D columns, eight
+// partial loads in flight; partials written by other CTAs are read through L2.
+template <class C>
+__device__ __forceinline__ void merge_tile(const Stage1Params &p, int b, int h, int rt, int nv, int warp,
+                                           int nwarps, int lane) {
+  constexpr int D = C::D, VPL = D / 32;
+  const int nrows = min(16, p.R - rt * 16);
+  for (int r = warp; r < nrows; r += nwarps) {
+    const int rg = rt * 16 + r;
+    const int t = rg / p.G, hq = h * p.G + (rg - t * p.G);
+    const int64_t base = ((static_cast<int64_t>(b) * p.Tq + t) * p.Hq + hq) * p.num_splits;
+    const float l0 = lane < nv ? __ldcg(p.lse_part + base + lane) : -INFINITY;
+    const float l1 = lane + 32 < nv ? __ldcg(p.lse_part + base + lane + 32) : -INFINITY;
+    float M = fmaxf(l0, l1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float w0 = (l0 == -INFINITY) ? 0.f : expf(l0 - M);
+    const float w1 = (l1 == -INFINITY) ? 0.f : expf(l1 - M);
+    float Z = w0 + w1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const float *op = p.o_part + base * D + lane * VPL;
+    for (int s0 = 0; s0 < nv; s0 += 8) {
+      float w[8];
+      float v[8][VPL];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int sp = s0 + u;
+        const float wa = __shfl_sync(0xffffffffu, w0, sp & 31);
+        const float wb = __shfl_sync(0xffffffffu, w1, sp & 31);
+        w[u] = sp < nv ? (sp < 32 ? wa : wb) : 0.f;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) v[u][i] = 0.f;
+        if (w[u] > 0.f) {
+          if constexpr (VPL == 4) {
+            const float4 x = __ldcg(reinterpret_cast<const float4 *>(op + sp * D));
+            v[u][0] = x.x;
+            v[u][1] = x.y;
+            v[u][2] = x.z;
+            v[u][3] = x.w;
+          } else {
+            const float2 x = __ldcg(reinterpret_cast<const float2 *>(op + sp * D));
+            v[u][0] = x.x;
+            v[u][1] = x.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) acc[i] = fmaf(w[u], v[u][i], acc[i]);
+    }
+    const float inv = Z > 0.f ? 1.f / Z : 0.f;
+    const int64_t ob = b * p.o_sb + t * p.o_st + hq * p.o_sh + lane * VPL;
+    if (p.out_f32) {
+      float *dst = reinterpret_cast<float *>(p.out) + ob;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) dst[i] = acc[i] * inv;
+    } else {
+      __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + ob;
+#pragma unroll
+      for (int i = 0; i < VPL; i += 2)
+        *reinterpret_cast<uint32_t *>(dst + i) = pack_bf16x2(acc[i] * inv, acc[i + 1] * inv);
+    }
+    if (lane == 0 && p.lse) p.lse[b * p.l_sb + t * p.l_st + hq * p.l_sh] = Z > 0.f ? M + logf(Z) : -INFINITY;
+  }
+}
+
 template <int KIND, int D, bool FUSED, bool DEEP>
 __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, DEEP>::MIN_BLOCKS)
     fd_stage1_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -609,6 +687,10 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rt = blockIdx.x % p.row_tiles, s = blockIdx.x / p.row_tiles;
   const int h = blockIdx.y, b = blockIdx.z;
+  // Launched as a programmatic dependent of the previous kernel in the stream:
+  // everything that kernel wrote is visible after this wait, before any input
+  // is read.
+  griddep_wait();
   const int P = p.page_size;
 
   // ---- split range from cache_seqlens (on the device; no host metadata)
@@ -623,10 +705,12 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
   const int c1 = min(L, c0 + chunk);
 
   if (c0 >= c1) {
-    // An empty split of a split call writes nothing: stage 2 reads only the
+    // An empty split of a split call writes nothing: the merge reads only the
     // split_count() non-empty splits. A request with no keys in an unsplit
     // call gets out = 0, lse = -inf here.
-    if (!FUSED) {
+    // With the fused merge, a request with no keys has no split to merge
+    // it: its split-0 CTA writes the empty rows (out = 0, lse = -inf).
+    if (!FUSED && !(p.counters && L == 0 && s == 0)) {
       griddep_launch_dependents();
       return;
     }
@@ -634,7 +718,7 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
     for (int i = threadIdx.x; i < ntile_rows * (D / 8); i += C::THREADS) {
       const int r = i / (D / 8), d0 = (i % (D / 8)) * 8;
       const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      write_row_outputs<C>(p, FUSED, b, h, s, rt * 16 + r, d0, z, 8, -INFINITY, d0 == 0);
+      write_row_outputs<C>(p, true, b, h, s, rt * 16 + r, d0, z, 8, -INFINITY, d0 == 0);
     }
     griddep_launch_dependents();
     return;
@@ -659,7 +743,8 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
     }
     const uint64_t pol = l2_policy_evict_first();
     const int *pt = p.page_table + b * p.pt_sb;
-    const int SEG = P < C::BLOCK_N ? P : C::BLOCK_N;  // slots per TMA box
+    const int SEG = P < C::SEG_MAX ? P : C::SEG_MAX;  // slots per TMA box (within one page)
+    const int log2_seg = P < C::SEG_MAX ? p.log2_page : 6;
     const unsigned seg_bytes = static_cast<unsigned>(SEG * C::ROW_BYTES);
 
     auto load_pids = [&](int it, int &q0, int &q1) {
@@ -690,14 +775,18 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
       if (!mbar_wait_warp(&empty[stage], ph ^ 1, p.status)) break;
       uint8_t *kt = smem + stage * C::STAGE;
       uint8_t *vt = kt + C::TILE;
-      if (lane == 0) mbar_arrive_expect_tx(&full[stage], static_cast<unsigned>(np) * seg_bytes * 2u);
-      for (int i = 0; i < np; ++i) {
-        const int a0 = __shfl_sync(0xffffffffu, p0, i & 31);
-        const int a1 = __shfl_sync(0xffffffffu, p1, i & 31);
+      // segments of SEG slots starting at token tok0 + i * SEG, each inside one page
+      const int nseg = (tend - tok0 + SEG - 1) >> log2_seg;
+      if (lane == 0) mbar_arrive_expect_tx(&full[stage], static_cast<unsigned>(nseg) * seg_bytes * 2u);
+      for (int i = 0; i < nseg; ++i) {
+        const int ts = tok0 + (i << log2_seg);
+        const int pi = (ts >> p.log2_page) - first;
+        const int a0 = __shfl_sync(0xffffffffu, p0, pi & 31);
+        const int a1 = __shfl_sync(0xffffffffu, p1, pi & 31);
         if (lane == 0) {
-          const int pid = i < 32 ? a0 : a1;
-          const int slot0 = P > C::BLOCK_N ? (tok0 & (P - 1)) : 0;
-          const int row0 = P > C::BLOCK_N ? 0 : i * P;
+          const int pid = pi < 32 ? a0 : a1;
+          const int slot0 = ts & (P - 1);
+          const int row0 = i << log2_seg;
 #pragma unroll
           for (int bx = 0; bx < C::N_BOX; ++bx) {
             const int off = bx * C::BLOCK_N * C::BOX_BYTES + row0 * C::BOX_BYTES;
@@ -754,7 +843,7 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
     float qc[2][C::NG], rs[2];
     if constexpr (C::QUANT) {
       float *qinfo = reinterpret_cast<float *>(smem + C::OFF_QI);
-      prepare_q_rows<C, KIND>(qs, qinfo, threadIdx.x);
+      if (threadIdx.x < 128) prepare_q_rows<C, KIND>(qs, qinfo, threadIdx.x);  // 8 threads per row
       named_barrier(1, C::NUM_CW * 32);
       build_q_fragments<C, KIND>(qs, qinfo, qa, lane);
       if constexpr (C::QA_SMEM) {
@@ -886,9 +975,9 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
       }
     }
     named_barrier(1, C::NUM_CW * 32);
-    {
-      constexpr int TPR = (C::NUM_CW * 32) / 16;  // threads per row
-      constexpr int DPT = D / TPR;                // columns per thread
+    if (threadIdx.x < 128) {  // 8 threads per row of the tile
+      constexpr int TPR = 8;
+      constexpr int DPT = D / TPR;  // columns per thread
       const int tid = threadIdx.x;
       const int row = tid / TPR;
       const int d0 = (tid % TPR) * DPT;
@@ -918,6 +1007,28 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
       }
       if (rg < p.R) write_row_outputs<C>(p, FUSED, b, h, s, rg, d0, vals, DPT, lse_nat, d0 == 0);
     }
+    if constexpr (!FUSED) {
+      if (p.counters) {
+        // Fused merge: publish this split's partials, count it, and let the
+        // last split of the (request, KV head, row tile) merge them all.
+        volatile unsigned *flag = reinterpret_cast<volatile unsigned *>(smem + C::OFF_FLAG);
+        __threadfence();
+        named_barrier(1, C::NUM_CW * 32);
+        const int nv = split_count(L, p.num_splits, p.log2_page, p.chunk_min);
+        if (threadIdx.x == 0) {
+          unsigned *ctr = p.counters + (static_cast<int64_t>(b) * p.Hkv + h) * p.row_tiles + rt;
+          const unsigned done = atomicAdd(ctr, 1u) + 1u;
+          const bool last = done == static_cast<unsigned>(nv);
+          if (last) {
+            *ctr = 0u;  // ready for the next call (and graph replay)
+            __threadfence();
+          }
+          *flag = last ? 1u : 0u;
+        }
+        named_barrier(1, C::NUM_CW * 32);
+        if (*flag) merge_tile<C>(p, b, h, rt, nv, warp, C::NUM_CW, lane);
+      }
+    }
   }
   griddep_launch_dependents();
 }
@@ -939,15 +1050,26 @@ cudaError_t stage1_prepare_t() {
   return e;
 }
 
+// Stage 1 is launched with programmatic stream serialization: its CTAs may be
+// scheduled while the previous kernel drains (a previous kernel that never
+// triggers simply completes first), and griddepcontrol.wait at its start
+// orders it after that kernel's memory operations.
 template <int KIND, int D, bool DEEP>
 cudaError_t launch_variant(bool fused, const CUtensorMap &tmk, const CUtensorMap &tmv,
                            const Stage1Params &p, dim3 grid, cudaStream_t stream) {
   using C = S1Cfg<KIND, D, DEEP>;
-  if (fused)
-    fd_stage1_kernel<KIND, D, true, DEEP><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tmk, tmv, p);
-  else
-    fd_stage1_kernel<KIND, D, false, DEEP><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tmk, tmv, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (fused) return cudaLaunchKernelEx(&cfg, fd_stage1_kernel<KIND, D, true, DEEP>, tmk, tmv, p);
+  return cudaLaunchKernelEx(&cfg, fd_stage1_kernel<KIND, D, false, DEEP>, tmk, tmv, p);
 }
 
 // deep: one-wave grids of the bf16 cache use the deep-ring variant.

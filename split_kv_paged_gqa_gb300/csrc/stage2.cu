@@ -25,6 +25,9 @@ constexpr int kS2Warps = 8;
 template <int D>
 __global__ void __launch_bounds__(kS2Warps * 32) fd_stage2_kernel(const __grid_constant__ Stage2Params p) {
   griddep_wait();
+  // the next call's stage 1 may be scheduled now; it waits for this grid's
+  // writes before reading anything
+  griddep_launch_dependents();
   constexpr int VPL = D / 32;  // values per lane
   const int row = blockIdx.x * kS2Warps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;

@@ -114,6 +114,34 @@ def test_mixed_lengths_with_max_length_hints(kind):
 
 
 # ---------------------------------------------------------------------------
+# split merge: fused into stage 1 (default) and the separate stage-2 kernel
+
+
+@pytest.mark.parametrize("kind", ["bf16", "int4"])
+def test_fused_merge_matches_oracle_and_stage2_merge(kind, monkeypatch):
+    Tq = 4 if kind == "int4" else 1
+    shape = _shape(kind, 4, Tq, 32, 8, 128, 16, (2000, 37, 0, 5000))
+    w = wl.make_workload(shape, 88, "cuda", poison=True)
+    ref_out, ref_lse = decode_ref_inputs(wl.oracle_inputs(w))
+    monkeypatch.delenv("FD_MERGE", raising=False)
+    plan2 = fd.fd_plan_create(0, 4, Tq, 32, 8, 128, 16, kind, 64)
+    monkeypatch.setenv("FD_MERGE", "fused")
+    plan1 = fd.fd_plan_create(0, 4, Tq, 32, 8, 128, 16, kind, 64)
+    monkeypatch.delenv("FD_MERGE")
+    try:
+        for S in (2, 7, 64):   # plan2: stage-2 kernel; plan1: fused merge, including an empty request
+            o2, l2 = run(w, S, torch.float32, plan=plan2)
+            assert_parity(o2, l2, ref_out, ref_lse, label=f"stage-2 merge S={S}")
+            o1, l1 = run(w, S, torch.float32, plan=plan1)
+            assert_parity(o1, l1, ref_out, ref_lse, label=f"fused merge S={S}")
+            assert (o1 - o2).abs().max().item() <= 1e-5
+    finally:
+        fd.fd_set_plan(None)
+        fd.fd_plan_destroy(plan1)
+        fd.fd_plan_destroy(plan2)
+
+
+# ---------------------------------------------------------------------------
 # edge cases
 
 
