@@ -691,6 +691,26 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
   // everything that kernel wrote is visible after this wait, before any input
   // is read.
   griddep_wait();
+
+  // Consumers issue their query-tile loads now, so their latency overlaps the
+  // length load below (the tile is written to shared memory later).
+  constexpr int Q_JOBS = 16 * (D / 8);  // 16-byte pieces of the 16-row Q tile
+  constexpr int Q_PER = (Q_JOBS + C::NUM_CW * 32 - 1) / (C::NUM_CW * 32);
+  uint4 qv[Q_PER];
+  if (warp < C::NUM_CW) {
+#pragma unroll
+    for (int k = 0; k < Q_PER; ++k) {
+      const int i = threadIdx.x + k * C::NUM_CW * 32;
+      qv[k] = make_uint4(0u, 0u, 0u, 0u);
+      const int r = i / (D / 8), cc = i % (D / 8);
+      const int rg = rt * 16 + r;
+      if (i < Q_JOBS && rg < p.R) {
+        const int t = rg / p.G, gq = rg - t * p.G;
+        qv[k] = *reinterpret_cast<const uint4 *>(p.q + b * p.q_sb + t * p.q_st + (h * p.G + gq) * p.q_sh +
+                                                 cc * 8);
+      }
+    }
+  }
   const int P = p.page_size;
 
   // ---- split range from cache_seqlens (on the device; no host metadata)
@@ -827,16 +847,10 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
     const int g = lane >> 2;
     // Q tile (16 rows; rows past R are zero) -> shared -> A fragments
     uint8_t *qs = smem + C::OFF_Q;
-    for (int i = threadIdx.x; i < 16 * (D / 8); i += C::NUM_CW * 32) {
-      const int r = i / (D / 8), cc = i % (D / 8);
-      const int rg = rt * 16 + r;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (rg < p.R) {
-        const int t = rg / p.G, gq = rg - t * p.G;
-        const __nv_bfloat16 *src = p.q + b * p.q_sb + t * p.q_st + (h * p.G + gq) * p.q_sh + cc * 8;
-        v = *reinterpret_cast<const uint4 *>(src);
-      }
-      *reinterpret_cast<uint4 *>(qs + r * C::QROW + cc * 16) = v;
+#pragma unroll
+    for (int k = 0; k < Q_PER; ++k) {
+      const int i = threadIdx.x + k * C::NUM_CW * 32;
+      if (i < Q_JOBS) *reinterpret_cast<uint4 *>(qs + (i / (D / 8)) * C::QROW + (i % (D / 8)) * 16) = qv[k];
     }
     named_barrier(1, C::NUM_CW * 32);
     uint32_t qa[D / 16][4];

@@ -7,8 +7,9 @@
 //   M = max_s lse_s,  w_s = exp(lse_s - M),  out = sum_s w_s o_s / sum_s w_s,
 //   lse = M + ln(sum_s w_s).
 // Only the non-empty splits of the row's request (split_count of its length)
-// are read; splits with lse_s = -inf carry weight 0 and are skipped by
-// selection; a row whose splits are all empty gets out = 0, lse = -inf. One warp per row; the
+// are read; splits with lse_s = -inf (a row with no visible key in them) carry
+// weight 0 (their partial is a finite 0); a row whose splits are all empty gets
+// out = 0, lse = -inf. One warp per row; the
 // split partials of a row are contiguous (S x D fp32) and read coalesced.
 // Launched with programmatic dependent launch: the grid may start while stage 1
 // drains and waits on griddepcontrol before touching the workspace.
@@ -39,6 +40,29 @@ __global__ void __launch_bounds__(kS2Warps * 32) fd_stage2_kernel(const __grid_c
   L = L < 0 ? 0 : (L > cap ? cap : L);  // as stage 1 clamps it
   const int nv = split_count(L, S, p.log2_page, p.chunk_min);  // splits stage 1 wrote
   const float *lp = p.lse_part + static_cast<int64_t>(row) * S;
+  const float *op = p.o_part + static_cast<int64_t>(row) * S * D + lane * VPL;
+  // The LSEs and the first 16 partials are requested together (one round
+  // trip for up to 16 splits); the weights are applied once both are in.
+  constexpr int U = 16;
+  float v[U][VPL];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) v[u][i] = 0.f;
+    if (u < nv) {
+      if constexpr (VPL == 4) {
+        const float4 t = *reinterpret_cast<const float4 *>(op + u * D);
+        v[u][0] = t.x;
+        v[u][1] = t.y;
+        v[u][2] = t.z;
+        v[u][3] = t.w;
+      } else {
+        const float2 t = *reinterpret_cast<const float2 *>(op + u * D);
+        v[u][0] = t.x;
+        v[u][1] = t.y;
+      }
+    }
+  }
   const float l0 = lane < nv ? lp[lane] : -INFINITY;
   const float l1 = lane + 32 < nv ? lp[lane + 32] : -INFINITY;
   float M = fmaxf(l0, l1);
@@ -53,39 +77,36 @@ __global__ void __launch_bounds__(kS2Warps * 32) fd_stage2_kernel(const __grid_c
   float acc[VPL];
 #pragma unroll
   for (int i = 0; i < VPL; ++i) acc[i] = 0.f;
-  const float *op = p.o_part + static_cast<int64_t>(row) * S * D + lane * VPL;
-  // Partials in groups of 8 splits, all loads of a group issued before use.
-  // Splits with weight 0 (empty, or far below the max) are not read.
-  constexpr int U = 8;
   for (int s0 = 0; s0 < nv; s0 += U) {
-    float w[U];
-    float v[U][VPL];
+    if (s0 > 0) {  // later groups of splits (more than 16)
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int s = s0 + u;
-      const float wa = __shfl_sync(0xffffffffu, w0, s & 31);
-      const float wb = __shfl_sync(0xffffffffu, w1, s & 31);
-      w[u] = s < nv ? (s < 32 ? wa : wb) : 0.f;
+      for (int u = 0; u < U; ++u) {
 #pragma unroll
-      for (int i = 0; i < VPL; ++i) v[u][i] = 0.f;
-      if (w[u] > 0.f) {
-        if constexpr (VPL == 4) {
-          const float4 t = *reinterpret_cast<const float4 *>(op + s * D);
-          v[u][0] = t.x;
-          v[u][1] = t.y;
-          v[u][2] = t.z;
-          v[u][3] = t.w;
-        } else {
-          const float2 t = *reinterpret_cast<const float2 *>(op + s * D);
-          v[u][0] = t.x;
-          v[u][1] = t.y;
+        for (int i = 0; i < VPL; ++i) v[u][i] = 0.f;
+        if (s0 + u < nv) {
+          if constexpr (VPL == 4) {
+            const float4 t = *reinterpret_cast<const float4 *>(op + (s0 + u) * D);
+            v[u][0] = t.x;
+            v[u][1] = t.y;
+            v[u][2] = t.z;
+            v[u][3] = t.w;
+          } else {
+            const float2 t = *reinterpret_cast<const float2 *>(op + (s0 + u) * D);
+            v[u][0] = t.x;
+            v[u][1] = t.y;
+          }
         }
       }
     }
 #pragma unroll
-    for (int u = 0; u < U; ++u)
+    for (int u = 0; u < U; ++u) {
+      const int sp = s0 + u;
+      const float wa = __shfl_sync(0xffffffffu, w0, sp & 31);
+      const float wb = __shfl_sync(0xffffffffu, w1, sp & 31);
+      const float w = sp < nv ? (sp < 32 ? wa : wb) : 0.f;  // empty splits carry weight 0
 #pragma unroll
-      for (int i = 0; i < VPL; ++i) acc[i] = fmaf(w[u], v[u][i], acc[i]);
+      for (int i = 0; i < VPL; ++i) acc[i] = fmaf(w, v[u][i], acc[i]);
+    }
   }
   const float inv = Z > 0.f ? 1.f / Z : 0.f;
   const int hq = row % p.Hq;
