@@ -673,6 +673,46 @@ __device__ __forceinline__ void merge_tile(const Stage1Params &p, int b, int h, 
   }
 }
 
+// L2 prefetch of a CTA's first STAGES blocks of K and V, issued before the
+// dependency wait by the producer warp. The length and page ids are read with
+// relaxed loads while the previous kernel may still be writing them: they
+// only choose which boxes to prefetch (a stale page id costs bandwidth; an id
+// outside the pool is skipped), and the kernel reads both again after the
+// wait. TMA drops boxes that fall outside the tensor.
+// Returns the (clamped) length the prefetch used.
+template <class C>
+__device__ __forceinline__ int prefetch_first_blocks(const CUtensorMap *tmk, const CUtensorMap *tmv,
+                                                     const Stage1Params &p, int b, int h, int s,
+                                                     int lane) {
+  if (lane == 0) {
+    tma_prefetch_desc(tmk);
+    tma_prefetch_desc(tmv);
+  }
+  const int P = p.page_size;
+  const int cap = p.max_pages * P;
+  int L = ld_relaxed_gpu(p.seqlens + b * p.sl_s);
+  L = L < 0 ? 0 : (L > cap ? cap : L);
+  const int chunk = split_chunk(L, p.num_splits, p.log2_page, p.chunk_min);
+  const int c0 = s * chunk;
+  const int c1 = min(L, c0 + chunk);
+  if (c0 >= c1) return L;
+  const int t1 = min(c1, c0 + C::STAGES * C::BLOCK_N);
+  const int log2_seg = P < C::SEG_MAX ? p.log2_page : 6;
+  const int nseg = (t1 - c0 + (1 << log2_seg) - 1) >> log2_seg;
+  const int *pt = p.page_table + b * p.pt_sb;
+  for (int i = lane; i < nseg; i += 32) {
+    const int ts = c0 + (i << log2_seg);
+    const int pid = ld_relaxed_gpu(pt + (ts >> p.log2_page));
+    if (pid < 0 || pid >= p.num_pages) continue;
+#pragma unroll
+    for (int bx = 0; bx < C::N_BOX; ++bx) {
+      tma_prefetch_4d(tmk, bx * C::BOX_ELEMS, h, ts & (P - 1), pid);
+      tma_prefetch_4d(tmv, bx * C::BOX_ELEMS, h, ts & (P - 1), pid);
+    }
+  }
+  return L;
+}
+
 template <int KIND, int D, bool FUSED, bool DEEP>
 __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, DEEP>::MIN_BLOCKS)
     fd_stage1_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -687,10 +727,52 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rt = blockIdx.x % p.row_tiles, s = blockIdx.x / p.row_tiles;
   const int h = blockIdx.y, b = blockIdx.z;
+  // The pipeline barriers read no input: set them up before the wait below.
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::STAGES; ++i) {
+      mbar_init(&full[i], C::QUANT ? 1 + 32 : 1);
+      mbar_init(&empty[i], C::NUM_CW);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
   // Launched as a programmatic dependent of the previous kernel in the stream:
   // everything that kernel wrote is visible after this wait, before any input
-  // is read.
+  // is read for its value. The one-wave variant's CTAs are often resident
+  // while that kernel drains; they spend the wait pulling their first blocks
+  // into L2 (from values that only steer prefetches).
+  int hint_L = -1;  // deep producer warp: the length its prefetch used
+  if constexpr (DEEP) {
+    if (warp == C::NUM_CW) hint_L = prefetch_first_blocks<C>(&tmk, &tmv, p, b, h, s, lane);
+  }
   griddep_wait();
+  // Every trigger of this kernel comes after its wait: the merge kernel relies
+  // on that to read the lengths before its own wait.
+  // The one-wave grid lets the merge kernel be scheduled from here on (every
+  // CTA of this grid is resident by then), so it is waiting, not launching,
+  // when this grid completes; it reads the workspace only after that. The
+  // multi-wave variants trigger as they finish: an early merge grid would sit
+  // on the resources their last wave uses.
+  if constexpr (DEEP) griddep_launch_dependents();
+
+  // The deep producer loads its first page ids now, at the hinted split range,
+  // in the same round trip as the length; they are used only if the length
+  // read after the wait equals the hint (then the range is the same).
+  int pn0 = 0, pn1 = 0;
+  if constexpr (DEEP) {
+    if (warp == C::NUM_CW && hint_L > 0) {
+      const int hc = split_chunk(hint_L, p.num_splits, p.log2_page, p.chunk_min);
+      const int h0 = s * hc, h1 = min(hint_L, h0 + hc);
+      if (h0 < h1) {
+        const int *pt = p.page_table + b * p.pt_sb;
+        const int first = h0 >> p.log2_page;
+        const int np = ((min(h0 + C::BLOCK_N, h1) - 1) >> p.log2_page) - first + 1;
+        pn0 = lane < np ? ld_cg(pt + first + lane) : 0;
+        pn1 = lane + 32 < np ? ld_cg(pt + first + 32 + lane) : 0;
+      }
+    }
+  }
 
   // Consumers issue their query-tile loads now, so their latency overlaps the
   // length load below (the tile is written to shared memory later).
@@ -714,7 +796,8 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
   const int P = p.page_size;
 
   // ---- split range from cache_seqlens (on the device; no host metadata)
-  int L = p.seqlens[b * p.sl_s];
+  // (the deep variant read these words before the wait: take them from L2)
+  int L = DEEP ? ld_cg(p.seqlens + b * p.sl_s) : p.seqlens[b * p.sl_s];
   const int cap = p.max_pages * P;
   if (L < 0 || L > cap) {
     if (threadIdx.x == 0) atomicOr(p.status, FD_DEVSTAT_SEQLEN_OVERFLOW);
@@ -731,7 +814,7 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
     // With the fused merge, a request with no keys has no split to merge
     // it: its split-0 CTA writes the empty rows (out = 0, lse = -inf).
     if (!FUSED && !(p.counters && L == 0 && s == 0)) {
-      griddep_launch_dependents();
+      if constexpr (!DEEP) griddep_launch_dependents();
       return;
     }
     const int ntile_rows = min(16, p.R - rt * 16);
@@ -740,18 +823,9 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
       const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       write_row_outputs<C>(p, true, b, h, s, rt * 16 + r, d0, z, 8, -INFINITY, d0 == 0);
     }
-    griddep_launch_dependents();
+    if constexpr (!DEEP) griddep_launch_dependents();
     return;
   }
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < C::STAGES; ++i) {
-      mbar_init(&full[i], C::QUANT ? 1 + 32 : 1);
-      mbar_init(&empty[i], C::NUM_CW);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
 
   const int n_iters = (c1 - c0 + C::BLOCK_N - 1) / C::BLOCK_N;
 
@@ -771,11 +845,10 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
       const int tok0 = c0 + it * C::BLOCK_N;
       const int first = tok0 >> p.log2_page;
       const int np = ((min(tok0 + C::BLOCK_N, c1) - 1) >> p.log2_page) - first + 1;
-      q0 = lane < np ? pt[first + lane] : 0;
-      q1 = lane + 32 < np ? pt[first + 32 + lane] : 0;
+      q0 = lane < np ? (DEEP ? ld_cg(pt + first + lane) : pt[first + lane]) : 0;
+      q1 = lane + 32 < np ? (DEEP ? ld_cg(pt + first + 32 + lane) : pt[first + 32 + lane]) : 0;
     };
-    int pn0, pn1;
-    load_pids(0, pn0, pn1);
+    if (!DEEP || L != hint_L) load_pids(0, pn0, pn1);
     int issued = 0;
     for (int it = 0; it < n_iters; ++it) {
       int p0 = pn0, p1 = pn1;
@@ -1044,7 +1117,7 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
       }
     }
   }
-  griddep_launch_dependents();
+  if constexpr (!DEEP) griddep_launch_dependents();
 }
 
 template <int KIND, int D, bool FUSED, bool DEEP>

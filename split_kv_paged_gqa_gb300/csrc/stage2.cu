@@ -25,9 +25,9 @@ constexpr int kS2Warps = 8;
 
 template <int D>
 __global__ void __launch_bounds__(kS2Warps * 32) fd_stage2_kernel(const __grid_constant__ Stage2Params p) {
-  griddep_wait();
-  // the next call's stage 1 may be scheduled now; it waits for this grid's
-  // writes before reading anything
+  // The next kernel may be scheduled at once: a programmatic dependent waits
+  // for this grid to complete (after its own wait below) before it reads
+  // anything this grid writes.
   griddep_launch_dependents();
   constexpr int VPL = D / 32;  // values per lane
   const int row = blockIdx.x * kS2Warps + (threadIdx.x >> 5);
@@ -35,7 +35,12 @@ __global__ void __launch_bounds__(kS2Warps * 32) fd_stage2_kernel(const __grid_c
   if (row >= p.B * p.Tq * p.Hq) return;
   const int S = p.num_splits;
   const int b_row = row / (p.Hq * p.Tq);
-  int L = p.seqlens[b_row * p.sl_s];
+  // The length is read before the wait: stage 1 triggers this grid only after
+  // its own dependency wait, so whatever wrote the lengths before stage 1 has
+  // completed by now, and stage 1 does not write them. It comes from L2, not
+  // from a line this SM's L1 may still hold from an earlier kernel.
+  int L = ld_cg(p.seqlens + b_row * p.sl_s);
+  griddep_wait();
   const int cap = p.max_pages << p.log2_page;
   L = L < 0 ? 0 : (L > cap ? cap : L);  // as stage 1 clamps it
   const int nv = split_count(L, S, p.log2_page, p.chunk_min);  // splits stage 1 wrote
