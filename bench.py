@@ -3,10 +3,12 @@
 
 Metric: paged flash-decode KV GB/s (algorithmic bytes / device time per call)
 and us/call at 32K KV. Workload (one step = one decode call = stage 1 +
-stage 2 over the batch): batch 64, every KV length 32768, 64 query heads,
-8 KV heads, head_dim 128, page size 64, one query token, bf16 Q/K/V drawn
-N(0, 1), num_splits from the startup autotuner. The 8.6 GB of KV per step is
-far larger than L2, so no flush is needed between steps.
+stage 2 over the batch, replayed from a CUDA graph): batch 64, every KV
+length 32768, 64 query heads, 8 KV heads, head_dim 128, page size 64, one
+query token, bf16 Q/K/V drawn N(0, 1), num_splits from the startup
+autotuner. The 8.6 GB of KV per step is far larger than L2, so no flush is
+needed between steps; workloads whose step is smaller rotate their calls over
+disjoint copies of the inputs spanning at least 4x L2.
 
 Also reported on the same line: the roofline of the dominant kernel (stage 1,
 live CUDA-event timing of its launches), the CPU baseline (the float64 oracle
@@ -22,7 +24,6 @@ collective on the data path); value = all ranks' bytes / max-over-ranks time.
 from __future__ import annotations
 
 import argparse
-import glob
 import hashlib
 import json
 import math
@@ -44,6 +45,7 @@ from split_kv_paged_gqa_gb300 import workloads as wl  # noqa: E402
 WORKLOAD = "long_bf16_b64"
 METRIC = "paged flash-decode KV GB/s (fraction of HBM peak) and us/call at 32K KV"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
 
 
 # ---------------------------------------------------------------------------
@@ -77,11 +79,14 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+STAGE1_SOURCES = ("stage1.cuh", "stage1_bf16.cu", "stage1_i8.cu", "stage1_i4.cu", "ptx.cuh", "kernels.h")
+
+
 def stage1_source_sha() -> str:
+    """Hash of the files the stage-1 kernel is compiled from (host code excluded)."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "split_kv_paged_gqa_gb300", "csrc", "*"))):
-        if p.endswith((".cu", ".cuh", ".h")):
-            h.update(open(p, "rb").read())
+    for name in STAGE1_SOURCES:
+        h.update(open(os.path.join(ROOT, "split_kv_paged_gqa_gb300", "csrc", name), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -204,7 +209,20 @@ def oracle_baseline(w: wl.Workload, requests, key_hi=None):
 # the CUDA arm
 
 
+def rotation_copies(call_bytes: int, l2_bytes: int, limit: int = 4096) -> int:
+    """How many disjoint copies of a step's inputs the timed calls rotate over.
+
+    Enough that the copies' KV together spans at least 4x L2, so no call finds
+    its KV still in L2 from an earlier one (1 when a single step already does).
+    """
+    if call_bytes >= 4 * l2_bytes:
+        return 1
+    return int(min(limit, -(-4 * l2_bytes // max(call_bytes, 1))))
+
+
 def run_fd(args):
+    import dataclasses
+
     import torch
 
     import __graft_entry__
@@ -216,9 +234,21 @@ def run_fd(args):
     __graft_entry__.build()
     dev = torch.device("cuda", local)
     shape = wl.CONFIGS[args.config]
-    w = wl.make_workload(shape, wl.CONFIG_SEEDS[args.config] + rank, dev)
+    seed = wl.CONFIG_SEEDS[args.config] + rank
     B = shape.batch
-    Lmax = int(w.lengths.max())
+    # the step's lengths, drawn as the workload generator draws them
+    lengths = wl.draw_lengths(shape.lengths, B, np.random.default_rng(seed))
+    _, call_bytes0 = algorithmic_bytes(shape, lengths, False)
+    l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (126 << 20))
+    n_copy = rotation_copies(call_bytes0, l2_bytes)
+    if n_copy == 1:
+        w = wl.make_workload(shape, seed, dev)
+    else:
+        # n_copy requests groups with the step's lengths, each on pages of its own
+        big = dataclasses.replace(shape, batch=B * n_copy,
+                                  pool_pages=shape.pool_pages * n_copy if shape.pool_pages else None)
+        w = wl.make_workload(big, seed, dev, lengths=np.tile(lengths, n_copy))
+    Lmax = int(lengths.max())
 
     plan = fd.fd_plan_create(local, B, shape.q_per_req, shape.num_q_heads, shape.num_kv_heads, shape.head_dim,
                              shape.page_size, shape.kv_dtype, 64)
@@ -232,16 +262,36 @@ def run_fd(args):
     fd.fd_set_max_seqlen_hint(plan, Lmax)
     S = fd.fd_query_splits(plan, B, Lmax)
 
-    out = torch.empty_like(w.q)
-    lse = torch.empty(w.q.shape[:3], dtype=torch.float32, device=dev)
+    out = torch.empty((B,) + tuple(w.q.shape[1:]), dtype=w.q.dtype, device=dev)
+    lse = torch.empty(out.shape[:3], dtype=torch.float32, device=dev)
 
-    def step():
-        fd.fd_decode_paged(w.q, w.k_cache, w.v_cache, w.kv_scales, w.page_table, w.cache_seqlens,
-                           shape.q_per_req, 0, out, lse)
+    def step(i):
+        g0 = (i % n_copy) * B
+        fd.fd_decode_paged(w.q[g0:g0 + B], w.k_cache, w.v_cache, w.kv_scales, w.page_table[g0:g0 + B],
+                           w.cache_seqlens[g0:g0 + B], shape.q_per_req, 0, out, lse)
 
+    # Each step is one decode call (stage 1 + stage 2) replayed from a CUDA
+    # graph, as a serving loop runs decode; consecutive calls rotate over the
+    # copies of the inputs.
     stream = torch.cuda.current_stream()
-    for _ in range(args.warmup):
-        step()
+    cap_stream = torch.cuda.Stream()
+    cap_stream.wait_stream(stream)
+    with torch.cuda.stream(cap_stream):
+        for i in range(3):
+            step(i)
+    stream.wait_stream(cap_stream)
+    torch.cuda.synchronize()
+
+    def capture(n, first):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                step(first + i)
+        return g
+
+    g_warm = capture(args.warmup, 0)
+    g_main = capture(args.steps, args.warmup)
+    g_warm.replay()
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
     clocks.start()
@@ -250,23 +300,43 @@ def run_fd(args):
     torch.cuda.synchronize()
     dist_barrier(world)
     e0.record(stream)
-    for _ in range(args.steps):
-        step()
+    g_main.replay()
     e1.record(stream)
     torch.cuda.synchronize()
     dist_barrier(world)
     ms_step = e0.elapsed_time(e1) / args.steps
     ms_step_max = dist_max(ms_step, world, dev)
+    del g_warm, g_main
 
-    # live per-kernel timing (CUDA events around each stage on the launch stream)
+    # spread: 10 trials of 50 graph-replayed calls, each trial on the copies
+    # that follow the previous trial's
+    n_tr, per_tr = 10, 50
+    trial_us = []
+    for t in range(n_tr):
+        g_tr = capture(per_tr, args.warmup + args.steps + t * per_tr)
+        e0.record(stream)
+        g_tr.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        trial_us.append(e0.elapsed_time(e1) / per_tr * 1e3)
+        del g_tr
+    trial_us.sort()
+    trials = {"trials": n_tr, "calls_per_trial": per_tr, "median_us": round(statistics.median(trial_us), 2),
+              "p10_us": round(float(np.percentile(trial_us, 10)), 2),
+              "p90_us": round(float(np.percentile(trial_us, 90)), 2)}
+
+    # live per-kernel timing: CUDA events around each stage on the launch
+    # stream, recorded as event nodes of a replayed graph of the same calls
     n_prof = min(args.steps, 300)
     fd.fd_profile_begin(plan)
-    for _ in range(n_prof):
-        step()
+    g_prof = capture(n_prof, args.warmup)
+    g_prof.replay()
+    torch.cuda.synchronize()
+    del g_prof
     calls, s1_ms, s2_ms = fd.fd_profile_end(plan)
     clk = clocks.stop()
 
-    stage1_bytes, call_bytes = algorithmic_bytes(shape, w.lengths, S == 1)
+    stage1_bytes, call_bytes = algorithmic_bytes(shape, lengths, S == 1)
     value = world * call_bytes / (ms_step_max * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
     s1_avg_ms = s1_ms / max(calls, 1)
@@ -280,12 +350,14 @@ def run_fd(args):
     sl_h = w.cache_seqlens.cpu().pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    q_d, pt_d, sl_d = torch.empty_like(w.q), torch.empty_like(w.page_table), torch.empty_like(w.cache_seqlens)
+    q_d, pt_d, sl_d = torch.empty_like(w.q[:B]), torch.empty_like(w.page_table[:B]), torch.empty_like(
+        w.cache_seqlens[:B])
 
-    def e2e_step(k_src=None, v_src=None, k_dst=None, v_dst=None):
-        q_d.copy_(q_h, non_blocking=True)
-        pt_d.copy_(pt_h, non_blocking=True)
-        sl_d.copy_(sl_h, non_blocking=True)
+    def e2e_step(i, k_src=None, v_src=None, k_dst=None, v_dst=None):
+        g0 = (i % n_copy) * B
+        q_d.copy_(q_h[g0:g0 + B], non_blocking=True)
+        pt_d.copy_(pt_h[g0:g0 + B], non_blocking=True)
+        sl_d.copy_(sl_h[g0:g0 + B], non_blocking=True)
         if k_src is not None:
             k_dst.copy_(k_src, non_blocking=True)
             v_dst.copy_(v_src, non_blocking=True)
@@ -296,17 +368,17 @@ def run_fd(args):
         lse_h.copy_(lse, non_blocking=True)
 
     n_e2e = min(args.steps, 200)
-    for _ in range(3):
-        e2e_step()
+    for i in range(3):
+        e2e_step(i)
     torch.cuda.synchronize()
     dist_barrier(world)
     e0.record(stream)
-    for _ in range(n_e2e):
-        e2e_step()
+    for i in range(n_e2e):
+        e2e_step(i)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = dist_max(e0.elapsed_time(e1) / n_e2e, world, dev)
-    h2d = q_h.numel() * 2 + pt_h.numel() * 4 + sl_h.numel() * 4
+    h2d = q_d.numel() * 2 + pt_d.numel() * 4 + sl_d.numel() * 4
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
     e2e = {"value": world * call_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -320,12 +392,12 @@ def run_fd(args):
             k_h = w.k_cache.cpu().pin_memory()
             v_h = w.v_cache.cpu().pin_memory()
             k_d, v_d = torch.empty_like(w.k_cache), torch.empty_like(w.v_cache)
-            e2e_step(k_h, v_h, k_d, v_d)
+            e2e_step(0, k_h, v_h, k_d, v_d)
             torch.cuda.synchronize()
             n_kv = 5
             e0.record(stream)
-            for _ in range(n_kv):
-                e2e_step(k_h, v_h, k_d, v_d)
+            for i in range(n_kv):
+                e2e_step(i, k_h, v_h, k_d, v_d)
             e1.record(stream)
             torch.cuda.synchronize()
             ms = dist_max(e0.elapsed_time(e1) / n_kv, world, dev)
@@ -345,9 +417,10 @@ def run_fd(args):
         sweep = {}
         cap_stream = torch.cuda.Stream()
         for bs in [b for b in (1, 16, 64) if b <= B]:
-            groups = max(1, B // bs)
+            groups = max(1, (B * n_copy) // bs)
             per_req = call_bytes / B
-            n_rot = max(groups, 8)
+            # enough calls that their KV spans 4x L2 (as far as the copies go)
+            n_rot = min(groups, max(8, -(-4 * l2_bytes // int(bs * per_req))))
             res = {}
             for s_try in sorted(set([1, 2, 4, 8, 16, 32, 64] + [fd.fd_query_splits(plan, bs, Lmax)])):
                 outs = torch.empty((bs,) + tuple(w.q.shape[1:]), dtype=w.q.dtype, device=dev)
@@ -398,6 +471,11 @@ def run_fd(args):
     if rank != 0:
         return None
     gpu_launches = args.steps * (1 if S == 1 else 2)
+    if n_copy == 1:
+        l2_note = "inputs larger than L2 (%.2f GB of KV per step), no flush" % (call_bytes / 1e9)
+    else:
+        l2_note = ("calls rotate over %d disjoint copies of the step's inputs (%.2f GB of KV together, at least "
+                   "4x the %.0f MB L2), no flush" % (n_copy, n_copy * call_bytes / 1e9, l2_bytes / 1e6))
     return {
         "metric": METRIC,
         "value": round(value, 1),
@@ -412,14 +490,17 @@ def run_fd(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V, random page permutation)",
-        "config": {"workload": f"{args.config}: batch {B}, KV length {Lmax} each, Hq {shape.num_q_heads}, "
-                               f"Hkv {shape.num_kv_heads}, head_dim {shape.head_dim}, page {shape.page_size}, "
-                               f"Tq {shape.q_per_req}, {shape.kv_dtype} KV",
+        "config": {"workload": f"{args.config}: batch {B}, KV lengths {shape.lengths} (max {Lmax}), "
+                               f"Hq {shape.num_q_heads}, Hkv {shape.num_kv_heads}, head_dim {shape.head_dim}, "
+                               f"page {shape.page_size}, Tq {shape.q_per_req}, {shape.kv_dtype} KV",
                    "batch_per_gpu": B, "kv_len": Lmax, "num_splits": S, "num_splits_source": "autotuned",
-                   "autotune_s": round(tune_s, 2),
-                   "l2": "inputs larger than L2 (%.1f GB of KV per step), no flush" % (call_bytes / 1e9),
+                   "autotune_s": round(tune_s, 2), "l2": l2_note,
+                   "timing": f"each step one decode call (stage 1 + stage 2); {args.steps} calls replayed from "
+                             f"one CUDA graph between CUDA events",
                    "bytes_per_step": call_bytes, "parallelism": f"replicas x{world}"},
+        "spread": trials,
         "fraction_of_hbm_peak": round(value / world / peak, 4),
+        "fraction_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
         "roofline": {"bound": "hbm", "kernel": "fd_stage1_kernel", "achieved": round(achieved, 1),
                      "peak": peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
                      "measured" else "fallback 6.8 TB/s", "unit": "GB/s", "frac": round(achieved / peak, 4),

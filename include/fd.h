@@ -257,9 +257,15 @@ FD_API fd_status fd_plan_workspace_bytes(fd_plan *plan, size_t *bytes);
 /* fd_profile_begin / fd_profile_end - per-stage device time of decode calls.
  * Between begin and end, every fd_decode_paged on this plan records CUDA
  * events on its stream before stage 1, between the stages and after stage 2.
+ * Calls made while a stream is being captured record the events as timed
+ * event nodes of the graph; replay the graph (once) before fd_profile_end,
+ * and destroy it before or right after: fd_profile_end destroys the events.
+ * The merge kernel of a profiled call is launched without programmatic
+ * dependent launch (the event between the stages separates them anyway).
  * fd_profile_end synchronises on those events and returns the number of
  * calls and the summed stage-1 and stage-2 milliseconds (stage 2 is 0 for
- * calls with num_splits = 1). Not for use inside graph capture. */
+ * calls with num_splits = 1). fd_profile_end itself is not for use inside
+ * graph capture. */
 FD_API fd_status fd_profile_begin(fd_plan *plan);
 FD_API fd_status fd_profile_end(fd_plan *plan, int *calls, double *stage1_ms, double *stage2_ms);
 

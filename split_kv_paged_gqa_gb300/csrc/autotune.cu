@@ -430,15 +430,15 @@ fd_status fd_autotune(fd_plan *plan, const int *batch_sizes, int n_batch, int mi
       }
       timed.emplace_back(S, t);
     }
-    // Among the candidates within 2% of the fastest, take the most splits:
-    // uniform-length tuning inputs cannot show the imbalance of a mixed batch,
-    // which more (balanced) splits absorb.
+    // Among the candidates within 1% of the fastest (about the spread of the
+    // timing), take the most splits: uniform-length tuning inputs cannot show
+    // the imbalance of a mixed batch, which more (balanced) splits absorb.
     double fastest = timed[0].second;
     for (auto &c : timed) fastest = std::min(fastest, c.second);
     int best = 0;
     double best_t = 0.0;
     for (auto &c : timed)
-      if (c.second <= fastest * 1.02 && c.first > best) {
+      if (c.second <= fastest * 1.01 && c.first > best) {
         best = c.first;
         best_t = c.second;
       }

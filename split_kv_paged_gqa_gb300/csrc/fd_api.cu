@@ -463,16 +463,23 @@ extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cach
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+  // Profiling events; under stream capture they become timed event nodes of
+  // the graph (external records), so a replayed graph is profiled without
+  // host launch gaps.
+  unsigned rec_flags = cudaEventRecordDefault;
   if (pl->profiling) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    FD_CUDA_TRY(cudaStreamIsCapturing(st, &cs));
+    if (cs == cudaStreamCaptureStatusActive) rec_flags = cudaEventRecordExternal;
     for (auto &x : ev) FD_CUDA_TRY(cudaEventCreate(&x));
     for (auto &x : ev) pl->prof_events.push_back(x);
-    FD_CUDA_TRY(cudaEventRecord(ev[0], st));
+    FD_CUDA_TRY(cudaEventRecordWithFlags(ev[0], st, rec_flags));
   }
   dim3 grid(p.row_tiles * S, pl->hkv, B);
   const long ctas = static_cast<long>(grid.x) * grid.y * grid.z;
   const bool deep = ctas <= pl->num_sms;  // one wave: one CTA per SM with a deeper ring
   cudaError_t e = fd::launch_stage1(pl->kind, D, S == 1, deep, tmk, tmv, p, grid, st);
-  if (pl->profiling) FD_CUDA_TRY(cudaEventRecord(ev[1], st));
+  if (pl->profiling) FD_CUDA_TRY(cudaEventRecordWithFlags(ev[1], st, rec_flags));
   if (e != cudaSuccess) return fail(FD_ERR_CUDA, "stage-1 launch failed: %s (%d)", cudaGetErrorString(e), (int)e);
   if (S > 1 && !p.counters) {
     fd::Stage2Params p2;
@@ -500,7 +507,7 @@ extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cach
     e = fd::launch_stage2(p2, st, !pl->profiling);
     if (e != cudaSuccess) return fail(FD_ERR_CUDA, "stage-2 launch failed: %s (%d)", cudaGetErrorString(e), (int)e);
   }
-  if (pl->profiling) FD_CUDA_TRY(cudaEventRecord(ev[2], st));
+  if (pl->profiling) FD_CUDA_TRY(cudaEventRecordWithFlags(ev[2], st, rec_flags));
   return FD_OK;
 }
 

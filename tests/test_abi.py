@@ -259,6 +259,22 @@ def test_nearest_match_is_invalidated_when_a_config_is_saved(tmp_path):
         fd.fd_plan_destroy(plan)
 
 
+def test_near_ties_go_to_more_splits_within_one_percent(tmp_path):
+    plan = _host_plan(B=64, S=64)
+    try:
+        fd.fd_autotune_set_cache_dir(plan, str(tmp_path))
+        times = {1: 100.0, 2: 100.9, 4: 101.2, 8: 103.0}
+        fd.fd_autotune_set_timer(plan, lambda b, k, S: times.get(S, 200.0))
+        fd.fd_autotune(plan, [64], 32768, 32768)
+        assert fd.fd_query_splits(plan, 64, 32768) == 2    # 0.9 % slower: kept; 1.2 %: not
+        times2 = {1: 100.0, 2: 101.3}
+        fd.fd_autotune_set_timer(plan, lambda b, k, S: times2.get(S, 200.0))
+        fd.fd_autotune(plan, [16], 32768, 32768)
+        assert fd.fd_query_splits(plan, 16, 32768) == 1
+    finally:
+        fd.fd_plan_destroy(plan)
+
+
 def test_heuristic_without_table():
     plan = _host_plan(B=64, S=64)
     try:

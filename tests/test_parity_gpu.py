@@ -257,6 +257,38 @@ def test_graph_capture_replay_picks_up_new_metadata():
         assert_parity(out, lse, ref_out, ref_lse, label=f"graph replay {trial}")
 
 
+def test_profiled_calls_inside_a_captured_graph():
+    """Profiling events captured as graph nodes: timed per call, results unchanged."""
+    shape = _shape("bf16", 2, 1, 16, 4, 128, 16, (700, 1500))
+    w = wl.make_workload(shape, 33, "cuda")
+    plan = plan_for(shape)
+    fd.fd_set_plan(plan)
+    out = torch.empty_like(w.q)
+    lse = torch.empty(w.q.shape[:3], dtype=torch.float32, device="cuda")
+
+    def call():
+        fd.fd_decode_paged(w.q, w.k_cache, w.v_cache, None, w.page_table, w.cache_seqlens, 1, 4, out, lse)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.current_stream().wait_stream(s)
+    fd.fd_profile_begin(plan)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(3):
+            call()
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    del g
+    calls, s1_ms, s2_ms = fd.fd_profile_end(plan)
+    assert calls == 3 and s1_ms > 0 and s2_ms > 0
+    ref_out, ref_lse = decode_ref_inputs(wl.oracle_inputs(w))
+    assert_parity(out, lse, ref_out, ref_lse, label="profiled graph")
+
+
 # ---------------------------------------------------------------------------
 # full-size workloads, in the launch configuration the bench times, on sampled requests
 
