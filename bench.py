@@ -52,20 +52,54 @@ NOMINAL_HBM_GBS = 8000.0
 # small helpers (host only)
 
 
-def algorithmic_bytes(shape: wl.DecodeShape, lengths: np.ndarray, fused: bool):
+def split_counts(lengths: np.ndarray, page_size: int, S: int, s_cap: int = 64, balanced: bool = True):
+    """Non-empty splits per request of a call, as the library places them.
+
+    Equal policy: ceil(L / chunk) with chunk = P * ceil(ceil(L / S) / P), at
+    most S. Balanced policy (the default, for B > 1): the batch's pages are cut
+    into chunks of cp = ceil(n_total / (B * S)) pages and a request of n pages
+    gets min(s_cap, ceil(n / cp)) as its S. Used for byte and launch accounting.
+    """
+    L = np.asarray(lengths, dtype=np.int64)
+    n = -(-L // page_size)
+    if balanced and len(L) > 1:
+        cp = max(1, -(-int(n.sum()) // (len(L) * S)))
+        Sb = np.where(n > 0, np.minimum(s_cap, -(-n // cp)), 1)
+    else:
+        Sb = np.full_like(L, S)
+    chunk = page_size * (-(-(-(-L // Sb)) // page_size))
+    return np.where(L > 0, np.minimum(-(-L // np.maximum(chunk, 1)), Sb), 0)
+
+
+def nearest_pow2(v: int) -> int:
+    """The power of two nearest v on a log scale (the library's mean-hint bucket)."""
+    p = 1 << max(0, (int(v) - 1).bit_length())
+    return p // 2 if p > 1 and 2 * v * v < p * p else p
+
+
+def launches_per_call(batch: int, S: int, balanced: bool = True) -> int:
+    """Kernels one decode call launches: stage 1, plus the merge whenever a
+    request may be split (any S > 1, or the balanced policy with B > 1)."""
+    return 2 if (S > 1 or (balanced and batch > 1)) else 1
+
+
+def algorithmic_bytes(shape: wl.DecodeShape, lengths: np.ndarray, direct=None):
     """(stage-1 bytes, whole-call bytes) a decode call must move at minimum.
 
     K + V (+ fp32 scales) of every owned key read once per KV head, q, the
     page-table entries of the owned pages and the lengths; the call also
-    writes out (bf16) and lse (fp32). Split-workspace traffic is overhead.
+    writes out (bf16) and lse (fp32). Stage 1 writes the outputs of the
+    requests marked in ``direct`` (one non-empty split). Split-workspace
+    traffic is overhead.
     """
     B, Tq, Hq, D, P = shape.batch, shape.q_per_req, shape.num_q_heads, shape.head_dim, shape.page_size
     kv = int(lengths.sum()) * wl.kv_bytes_per_token(shape)
     q = B * Tq * Hq * D * 2
-    out = B * Tq * Hq * D * 2 + B * Tq * Hq * 4
+    out_req = Tq * Hq * D * 2 + Tq * Hq * 4
     meta = int(sum(-(-int(L) // P) for L in lengths)) * 4 + B * 4
-    stage1 = kv + q + meta + (out if fused else 0)
-    return stage1, kv + q + meta + out
+    n_direct = 0 if direct is None else int(np.count_nonzero(direct))
+    stage1 = kv + q + meta + n_direct * out_req
+    return stage1, kv + q + meta + B * out_req
 
 
 def measured_peaks():
@@ -238,7 +272,7 @@ def run_fd(args):
     B = shape.batch
     # the step's lengths, drawn as the workload generator draws them
     lengths = wl.draw_lengths(shape.lengths, B, np.random.default_rng(seed))
-    _, call_bytes0 = algorithmic_bytes(shape, lengths, False)
+    _, call_bytes0 = algorithmic_bytes(shape, lengths)
     l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (126 << 20))
     n_copy = rotation_copies(call_bytes0, l2_bytes)
     if n_copy == 1:
@@ -253,13 +287,17 @@ def run_fd(args):
     plan = fd.fd_plan_create(local, B, shape.q_per_req, shape.num_q_heads, shape.num_kv_heads, shape.head_dim,
                              shape.page_size, shape.kv_dtype, 64)
     fd.fd_set_plan(plan)
-    # startup autotune of num_splits, outside any capture
+    # startup autotune of num_splits, outside any capture, at the buckets of
+    # the max and of the mean length (the balanced split policy looks the
+    # table up at the mean's bucket)
+    Lmean = max(1, int(round(float(lengths.mean()))))
     bucket = 1 << (Lmax - 1).bit_length()
     tune_batches = sorted({b for b in (1, 16, 64, B) if b <= B})
     t0 = time.perf_counter()
-    fd.fd_autotune(plan, tune_batches, bucket, bucket)
+    fd.fd_autotune(plan, tune_batches, min(nearest_pow2(Lmean), bucket), bucket)
     tune_s = time.perf_counter() - t0
     fd.fd_set_max_seqlen_hint(plan, Lmax)
+    fd.fd_set_mean_seqlen_hint(plan, Lmean)
     S = fd.fd_query_splits(plan, B, Lmax)
 
     out = torch.empty((B,) + tuple(w.q.shape[1:]), dtype=w.q.dtype, device=dev)
@@ -336,7 +374,8 @@ def run_fd(args):
     calls, s1_ms, s2_ms = fd.fd_profile_end(plan)
     clk = clocks.stop()
 
-    stage1_bytes, call_bytes = algorithmic_bytes(shape, lengths, S == 1)
+    nv = split_counts(lengths, shape.page_size, S)
+    stage1_bytes, call_bytes = algorithmic_bytes(shape, lengths, direct=(nv == 1))
     value = world * call_bytes / (ms_step_max * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
     s1_avg_ms = s1_ms / max(calls, 1)
@@ -470,7 +509,7 @@ def run_fd(args):
     fd.fd_plan_destroy(plan)
     if rank != 0:
         return None
-    gpu_launches = args.steps * (1 if S == 1 else 2)
+    gpu_launches = args.steps * launches_per_call(B, S)
     if n_copy == 1:
         l2_note = "inputs larger than L2 (%.2f GB of KV per step), no flush" % (call_bytes / 1e9)
     else:
@@ -493,7 +532,8 @@ def run_fd(args):
         "config": {"workload": f"{args.config}: batch {B}, KV lengths {shape.lengths} (max {Lmax}), "
                                f"Hq {shape.num_q_heads}, Hkv {shape.num_kv_heads}, head_dim {shape.head_dim}, "
                                f"page {shape.page_size}, Tq {shape.q_per_req}, {shape.kv_dtype} KV",
-                   "batch_per_gpu": B, "kv_len": Lmax, "num_splits": S, "num_splits_source": "autotuned",
+                   "batch_per_gpu": B, "kv_len": Lmax, "kv_len_mean": Lmean, "num_splits": S,
+                   "num_splits_source": "autotuned", "split_policy": "balanced",
                    "autotune_s": round(tune_s, 2), "l2": l2_note,
                    "timing": f"each step one decode call (stage 1 + stage 2); {args.steps} calls replayed from "
                              f"one CUDA graph between CUDA events",

@@ -68,6 +68,23 @@ typedef enum fd_dtype {
   FD_INT32 = 4
 } fd_dtype;
 
+/* How a call cuts its requests' keys into splits (fd_plan_set_split_policy). */
+typedef enum fd_split_policy {
+  /* Default. Every split of the batch holds about the same number of pages:
+   * the batch's n_total pages (sum of ceil(L_b / P)) are cut into chunks of
+   * cp = ceil(n_total / (B * num_splits)) pages, and request b gets
+   * min(s_cap, ceil(ceil(L_b / P) / cp)) equal page-aligned splits, where
+   * s_cap = min(64, the plan's workspace rows / (B * Tq * Hq)) >= max_splits.
+   * A long request gets more splits than a short one, so a mixed-length
+   * batch keeps its CTAs evenly loaded; with equal lengths the splits are
+   * exactly those of FD_SPLIT_EQUAL. The map is rebuilt on the device from
+   * cache_seqlens by every call. */
+  FD_SPLIT_BALANCED = 0,
+  /* num_splits equal page-aligned chunks of each request's keys:
+   * chunk_b = P * ceil(ceil(L_b / num_splits) / P). */
+  FD_SPLIT_EQUAL = 1
+} fd_split_policy;
+
 /* Bits of the plan's device status word (see fd_read_device_status). */
 #define FD_DEVSTAT_BAD_PAGE 1u         /* a visible key's page id was outside [0, num_pages) */
 #define FD_DEVSTAT_SEQLEN_OVERFLOW 2u  /* cache_seqlens[b] > page_table width * page size, or < 0 */
@@ -127,8 +144,18 @@ FD_API fd_status fd_set_plan(fd_plan *plan);
 FD_API fd_plan *fd_get_plan(void);
 
 /*
- * fd_decode_paged - one decode attention call (stage 1 and, when
- * num_splits > 1, stage 2), enqueued on stream.
+ * fd_plan_set_split_policy - choose how calls on this plan place their split
+ * boundaries (an fd_split_policy; default FD_SPLIT_BALANCED). Results do not
+ * depend on it beyond rounding. Host only; takes effect from the next call.
+ * The balanced policy is this library's own: the pages describe per-request
+ * num_splits only (FA3's knob in "Covered decode kernels" of "feat(autotune):
+ * separate general and decode attention warmup").
+ */
+FD_API fd_status fd_plan_set_split_policy(fd_plan *plan, int policy);
+
+/*
+ * fd_decode_paged - one decode attention call (stage 1 and, when any request
+ * is split, stage 2), enqueued on stream.
  *
  *  q             bf16 [B, Tq, Hq, D], innermost stride 1.
  *  k_cache       [num_pages, P, Hkv, D] bf16 or int8, or [num_pages, P, Hkv, D/2]
@@ -149,8 +176,11 @@ FD_API fd_plan *fd_get_plan(void);
  *                Query token t sees keys [0, L_b - (Tq-1) + t) (causal MTP).
  *  num_splits    1..plan max_splits, or 0 to use the autotuned value for
  *                (B, bucket of the max-seqlen hint) (see fd_set_max_seqlen_hint).
- *                Splits are equal page-aligned chunks of each request's keys;
- *                results do not depend on it beyond rounding.
+ *                Splits per request: on average over the batch under the
+ *                balanced policy, exactly under the equal one (see
+ *                fd_split_policy). Results do not depend on it beyond
+ *                rounding. A request with a single non-empty split gets its
+ *                outputs from stage 1 directly.
  *  out           [B, Tq, Hq, D] bf16 (round to nearest even) or fp32,
  *                innermost stride 1.
  *  lse           fp32 [B, Tq, Hq] natural-log LSE of the scaled scores, or NULL.
@@ -180,7 +210,8 @@ FD_API fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cache, c
  * FD_ERR_WORKSPACE.
  *
  * Arguments are those of fd_decode_paged, with these differences:
- *  - num_splits must be 1..64 (there is no tuning table);
+ *  - num_splits must be 1..64 (there is no tuning table), and splits are
+ *    always FD_SPLIT_EQUAL;
  *  - softmax_scale is explicit (0 = 1/sqrt(D));
  *  - the device is the current one.
  *
@@ -205,6 +236,14 @@ FD_API fd_status fd_decode_paged_static(const fd_tensor *q, const fd_tensor *k_c
  * uses the real length). 0 clears the hint (the longest bucket is used). */
 FD_API fd_status fd_set_max_seqlen_hint(fd_plan *plan, int max_seqlen);
 
+/* fd_set_mean_seqlen_hint - host-known mean of cache_seqlens for the next
+ * calls with num_splits = 0 under the balanced split policy: the tuning table
+ * is then looked up at the power of two nearest the mean (log scale) instead
+ * of the bucket of the max. Balanced splits give a mixed-length batch of mean
+ * m the per-CTA work of an equal-length batch of length m, which is what the
+ * table was tuned on. 0 clears the hint. Host only. */
+FD_API fd_status fd_set_mean_seqlen_hint(fd_plan *plan, int mean_seqlen);
+
 /*
  * fd_autotune - pick num_splits per (batch, KV-length bucket) by timing
  * (same page, sections "Changes" and "Covered decode kernels": decode
@@ -216,19 +255,26 @@ FD_API fd_status fd_set_max_seqlen_hint(fd_plan *plan, int max_seqlen);
  *                         max_bucket (0, 0 = 1024 .. FD_AUTOTUNE_SEQ_LEN or 32768).
  *  stream                 stream for the timing launches.
  *
- * Candidates are num_splits in {1, 2, 4, ..., max_splits}. For each key not
- * already in the table (loaded from the cache directory), synthetic inputs of
- * the bucket length are timed with CUDA events after an L2 flush; the fastest
- * is stored and the table saved. Refuses with FD_ERR_CAPTURING while the
- * stream is capturing. FD_FORCE_AUTOTUNE=1 ignores cached entries once.
- * Allocates temporary device buffers (freed before return).
+ * Candidates are num_splits in {1, 2, 4, ..., max_splits}, plus the counts
+ * that fill one or two waves of one CTA per SM. For each key not already in
+ * the table (loaded from the cache directory), synthetic inputs of the bucket
+ * length are timed as a decode loop runs them: a CUDA graph of consecutive
+ * calls, each on pages of its own (together at least 4x L2 where memory
+ * allows), replayed back to back, median of three timed blocks. The fastest
+ * candidate is stored (an exact tie goes to fewer splits) and the table
+ * saved. Tuning inputs have equal lengths; the balanced split policy carries
+ * the pick over to mixed-length batches. Refuses with FD_ERR_CAPTURING while
+ * the stream is capturing. FD_FORCE_AUTOTUNE=1 ignores cached entries once.
+ * Allocates temporary device buffers and a private stream (freed before
+ * return); the timing runs on that stream after the work of `stream`.
  */
 FD_API fd_status fd_autotune(fd_plan *plan, const int *batch_sizes, int n_batch, int min_bucket,
                       int max_bucket, fd_stream_t stream);
 
 /* fd_query_splits - the num_splits a num_splits = 0 call would use for
- * (batch, max_seqlen): the tuned entry of the nearest tuned batch and the
- * bucket of max_seqlen, else the built-in heuristic. Host only. */
+ * (batch, max_seqlen) and the plan's mean-length hint: the tuned entry of the
+ * nearest tuned batch and the lookup bucket (see fd_set_mean_seqlen_hint),
+ * else the built-in heuristic. Host only. */
 FD_API fd_status fd_query_splits(fd_plan *plan, int batch, int max_seqlen, int *num_splits);
 
 /* Timer hook for fd_autotune: returns the time of one call with num_splits
@@ -264,7 +310,7 @@ FD_API fd_status fd_plan_workspace_bytes(fd_plan *plan, size_t *bytes);
  * dependent launch (the event between the stages separates them anyway).
  * fd_profile_end synchronises on those events and returns the number of
  * calls and the summed stage-1 and stage-2 milliseconds (stage 2 is 0 for
- * calls with num_splits = 1). fd_profile_end itself is not for use inside
+ * calls that launch no merge). fd_profile_end itself is not for use inside
  * graph capture. */
 FD_API fd_status fd_profile_begin(fd_plan *plan);
 FD_API fd_status fd_profile_end(fd_plan *plan, int *calls, double *stage1_ms, double *stage2_ms);

@@ -15,7 +15,8 @@ from typing import Optional, Sequence, Tuple
 
 __all__ = [
     "FdError", "load_library", "fd_plan_create", "fd_plan_destroy", "fd_set_plan", "fd_get_plan",
-    "fd_decode_paged", "fd_decode_paged_static", "fd_set_max_seqlen_hint", "fd_autotune", "fd_query_splits",
+    "fd_decode_paged", "fd_decode_paged_static", "fd_plan_set_split_policy", "fd_set_max_seqlen_hint",
+    "fd_set_mean_seqlen_hint", "fd_autotune", "fd_query_splits",
     "fd_autotune_set_timer", "fd_autotune_set_cache_dir", "fd_autotune_stats",
     "fd_read_device_status", "fd_plan_workspace_bytes", "fd_profile_begin", "fd_profile_end",
     "fd_status_string", "fd_last_error",
@@ -23,6 +24,7 @@ __all__ = [
     "FD_ERR_CUDA", "FD_ERR_DEVICE_STATUS", "FD_ERR_TIMEOUT", "FD_ERR_NO_PLAN", "FD_ERR_IO",
     "FD_BF16", "FD_FP32", "FD_INT8", "FD_INT4X2", "FD_INT32",
     "FD_DEVSTAT_BAD_PAGE", "FD_DEVSTAT_SEQLEN_OVERFLOW", "FD_DEVSTAT_WAIT_TIMEOUT",
+    "FD_SPLIT_BALANCED", "FD_SPLIT_EQUAL",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfd.so")
@@ -31,6 +33,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfd.so")
  FD_ERR_DEVICE_STATUS, FD_ERR_TIMEOUT, FD_ERR_NO_PLAN, FD_ERR_IO) = range(10)
 FD_BF16, FD_FP32, FD_INT8, FD_INT4X2, FD_INT32 = range(5)
 FD_DEVSTAT_BAD_PAGE, FD_DEVSTAT_SEQLEN_OVERFLOW, FD_DEVSTAT_WAIT_TIMEOUT = 1, 2, 4
+FD_SPLIT_BALANCED, FD_SPLIT_EQUAL = 0, 1
 
 _KV_NAMES = {"bf16": FD_BF16, "int8": FD_INT8, "int4": FD_INT4X2}
 
@@ -75,7 +78,9 @@ def load_library(path: Optional[str] = None):
         "fd_get_plan": (P, []),
         "fd_decode_paged": (I, [T, T, T, T, T, T, I, I, T, T, P]),
         "fd_decode_paged_static": (I, [T, T, T, T, T, T, I, I, F, T, T, P]),
+        "fd_plan_set_split_policy": (I, [P, I]),
         "fd_set_max_seqlen_hint": (I, [P, I]),
+        "fd_set_mean_seqlen_hint": (I, [P, I]),
         "fd_autotune": (I, [P, ctypes.POINTER(I), I, I, I, P]),
         "fd_query_splits": (I, [P, I, I, ctypes.POINTER(I)]),
         "fd_autotune_set_timer": (I, [P, TIMER_FN, P]),
@@ -205,8 +210,19 @@ def fd_decode_paged_static(q, k_cache, v_cache, kv_scales, page_table, cache_seq
                                                  _stream_handle(stream)))
 
 
+def fd_plan_set_split_policy(plan: int, policy) -> None:
+    """FD_SPLIT_BALANCED (default) or FD_SPLIT_EQUAL; also "balanced" / "equal"."""
+    if isinstance(policy, str):
+        policy = {"balanced": FD_SPLIT_BALANCED, "equal": FD_SPLIT_EQUAL}[policy]
+    _check(load_library().fd_plan_set_split_policy(plan, int(policy)))
+
+
 def fd_set_max_seqlen_hint(plan: int, max_seqlen: int) -> None:
     _check(load_library().fd_set_max_seqlen_hint(plan, max_seqlen))
+
+
+def fd_set_mean_seqlen_hint(plan: int, mean_seqlen: int) -> None:
+    _check(load_library().fd_set_mean_seqlen_hint(plan, int(mean_seqlen)))
 
 
 def fd_autotune(plan: int, batch_sizes: Sequence[int], min_bucket: int = 0, max_bucket: int = 0,

@@ -12,13 +12,18 @@
 //
 // Table key: (batch, bucket) with bucket a power of two of the KV length.
 // Lookup for a call: the nearest tuned batch (smallest >= B, else the
-// largest), then the bucket of the host-known max length (exact, else the
-// smallest larger, else the largest), memoised until the next save. Without
-// any entry a heuristic sizes the grid to two CTAs per SM.
+// largest), then the lookup bucket (exact, else the smallest larger, else the
+// largest), memoised until the next save. The lookup bucket is the next power
+// of two >= the host-known max length; under the balanced split policy with a
+// mean-length hint it is the power of two nearest the mean instead: balanced
+// splits give a mixed batch of mean m the per-CTA work of an equal-length
+// batch of length m, which is what the table was tuned on. Without any entry
+// a heuristic sizes the grid to two CTAs per SM.
 #include <cuda_runtime.h>
 #include <sys/stat.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -41,6 +46,13 @@ int next_pow2(int v) {
 }
 
 bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+
+// The power of two nearest to v on a log scale (the geometric midpoint
+// between p / 2 and p decides).
+int nearest_pow2(int v) {
+  const int p = next_pow2(v);
+  return (p > 1 && 2.0 * v * v < static_cast<double>(p) * p) ? p / 2 : p;
+}
 
 int heuristic_splits(const fd_plan *pl, int batch, int max_seqlen) {
   const int G = pl->hq / pl->hkv;
@@ -110,17 +122,22 @@ __global__ void fill_f32_kernel(float *p, size_t n, float v) {
     p[i] = v;
 }
 
+// Calls in one captured sequence at most (each on pages of its own).
+constexpr int kMaxSeq = 64;
+
 struct TuneBuffers {
-  void *q = nullptr, *out = nullptr, *k = nullptr, *v = nullptr, *flush = nullptr;
+  void *q = nullptr, *out = nullptr, *k = nullptr, *v = nullptr;
   float *lse = nullptr, *scales = nullptr;
   int *pt = nullptr, *sl = nullptr;
-  size_t flush_bytes = 0;
   long pool_pages = 0;
   int width = 0, bmax = 0, tq = 1;
+  double l2_bytes = 0.0;
+  cudaStream_t ts = nullptr;  // private stream: captured and replayed sequences
   ~TuneBuffers() {
-    for (void *p : {q, out, k, v, flush, static_cast<void *>(lse), static_cast<void *>(scales),
+    for (void *p : {q, out, k, v, static_cast<void *>(lse), static_cast<void *>(scales),
                     static_cast<void *>(pt), static_cast<void *>(sl)})
       if (p) cudaFree(p);
+    if (ts) cudaStreamDestroy(ts);
   }
 };
 
@@ -140,10 +157,16 @@ fd_status tune_alloc(fd_plan *pl, TuneBuffers &tb, int bmax, int max_bucket, cud
   tb.bmax = bmax;
   tb.tq = pl->max_q;
   tb.width = (max_bucket + pl->page - 1) / pl->page;
-  const long need = static_cast<long>(bmax) * tb.width;
-  // a pool well above L2 so timed calls stream from HBM, capped at what is needed
-  const long cap = static_cast<long>((4.0 * std::max(l2, 1 << 20)) / page_bytes) + 1;
-  tb.pool_pages = std::min(need, cap);
+  // Pool: distinct pages for the largest batch's call and for a sequence of
+  // eight one-request calls, at least 4x L2 of K+V, at most a quarter of the
+  // free device memory (beyond that, page ids wrap around the pool).
+  size_t free_b = 0, total_b = 0;
+  TRY_CUDA(cudaMemGetInfo(&free_b, &total_b));
+  const size_t kv_page = 2 * page_bytes + (pl->kv_dtype != FD_BF16 ? 2ull * pl->page * pl->hkv * ng * 4 : 0);
+  long want = std::max(static_cast<long>(bmax), 8L) * tb.width;
+  want = std::max(want, static_cast<long>(4.0 * std::max(l2, 1 << 20) / kv_page) + 1);
+  const long mem_cap = static_cast<long>(free_b / 4 / kv_page);
+  tb.pool_pages = std::max(1L, std::min(want, mem_cap));
   const size_t qn = static_cast<size_t>(bmax) * tb.tq * pl->hq * pl->d;
   const size_t kvn = static_cast<size_t>(tb.pool_pages) * pl->page * pl->hkv * rowe;
   TRY_CUDA(cudaMalloc(&tb.q, qn * 2));
@@ -156,10 +179,11 @@ fd_status tune_alloc(fd_plan *pl, TuneBuffers &tb, int bmax, int max_bucket, cud
     TRY_CUDA(cudaMalloc(&tb.scales, sn * 4));
     fill_f32_kernel<<<1024, 256, 0, st>>>(tb.scales, sn, 0.02f);
   }
-  TRY_CUDA(cudaMalloc(&tb.pt, static_cast<size_t>(bmax) * tb.width * 4));
+  const size_t pt_rows = static_cast<size_t>(bmax) * kMaxSeq;
+  TRY_CUDA(cudaMalloc(&tb.pt, pt_rows * tb.width * 4));
   TRY_CUDA(cudaMalloc(&tb.sl, static_cast<size_t>(bmax) * 4));
-  tb.flush_bytes = 2ull * std::max(l2, 1 << 20);
-  TRY_CUDA(cudaMalloc(&tb.flush, tb.flush_bytes));
+  TRY_CUDA(cudaStreamCreateWithFlags(&tb.ts, cudaStreamNonBlocking));
+  tb.l2_bytes = static_cast<double>(std::max(l2, 1 << 20));
   fill_bf16_kernel<<<1024, 256, 0, st>>>(static_cast<__nv_bfloat16 *>(tb.q), qn, 17u);
   if (pl->kv_dtype == FD_BF16) {
     fill_bf16_kernel<<<4096, 256, 0, st>>>(static_cast<__nv_bfloat16 *>(tb.k), kvn, 29u);
@@ -169,11 +193,12 @@ fd_status tune_alloc(fd_plan *pl, TuneBuffers &tb, int bmax, int max_bucket, cud
     fill_u8_kernel<<<4096, 256, 0, st>>>(static_cast<uint8_t *>(tb.v), kvn, 31u);
   }
   TRY_CUDA(cudaGetLastError());
-  std::vector<int> pt(static_cast<size_t>(bmax) * tb.width);
-  for (int b = 0; b < bmax; ++b)
+  // row r holds pages r * width ... (mod pool): rows of different calls of a
+  // sequence name different pages while the pool lasts
+  std::vector<int> pt(pt_rows * tb.width);
+  for (size_t r = 0; r < pt_rows; ++r)
     for (int p = 0; p < tb.width; ++p)
-      pt[static_cast<size_t>(b) * tb.width + p] =
-          static_cast<int>((static_cast<long>(b) * tb.width + p) % tb.pool_pages);
+      pt[r * tb.width + p] = static_cast<int>((static_cast<long>(r) * tb.width + p) % tb.pool_pages);
   TRY_CUDA(cudaMemcpyAsync(tb.pt, pt.data(), pt.size() * 4, cudaMemcpyHostToDevice, st));
   TRY_CUDA(cudaStreamSynchronize(st));
   return FD_OK;
@@ -193,41 +218,81 @@ void make_desc(fd_tensor &t, void *data, fd_dtype dt, std::initializer_list<int6
   }
 }
 
-fd_status tune_time(fd_plan *pl, TuneBuffers &tb, int batch, int bucket, int S, cudaStream_t st,
-                    double *ms_out) {
+// Device time of one call with `S` splits in the steady state of a decode
+// loop: a CUDA graph of n_seq calls, each on pages of its own, replayed back
+// to back (each call's start overlaps the previous call's end). The calls of
+// a sequence together read at least 4x L2 where the pool allows, so no call
+// finds its pages in L2 from the previous replay. Median of three blocks of
+// at least eight calls.
+fd_status tune_time(fd_plan *pl, TuneBuffers &tb, int batch, int bucket, int S, double *ms_out) {
   const int rowe = pl->kv_dtype == FD_INT4X2 ? pl->d / 2 : pl->d;
   const int ng = pl->kv_dtype == FD_INT4X2 ? pl->d / 32 : 1;
+  const long call_pages = static_cast<long>(batch) * tb.width;
+  const long fit = std::max(1L, tb.pool_pages / call_pages);  // sequences with distinct pages
+  const double call_bytes = static_cast<double>(batch) * bucket * pl->hkv * rowe *
+                            (pl->kv_dtype == FD_BF16 ? 4.0 : 2.0);
+  const long cold = static_cast<long>(std::ceil(4.0 * tb.l2_bytes / std::max(call_bytes, 1.0)));
+  const int n_seq = static_cast<int>(std::min<long>({fit, static_cast<long>(kMaxSeq), std::max(1L, cold)}));
+  const int reps = std::max(1, (8 + n_seq - 1) / n_seq);  // replays per timed block
+  cudaStream_t ts = tb.ts;
   std::vector<int> sl(batch, bucket);
-  TRY_CUDA(cudaMemcpyAsync(tb.sl, sl.data(), sl.size() * 4, cudaMemcpyHostToDevice, st));
-  fd_tensor q, k, v, sc, pt, sq, out, lse;
+  TRY_CUDA(cudaMemcpyAsync(tb.sl, sl.data(), sl.size() * 4, cudaMemcpyHostToDevice, ts));
+  TRY_CUDA(cudaStreamSynchronize(ts));
+  fd_tensor q, k, v, sc, sq, out, lse;
   make_desc(q, tb.q, FD_BF16, {batch, tb.tq, pl->hq, pl->d});
   make_desc(k, tb.k, pl->kv_dtype, {tb.pool_pages, pl->page, pl->hkv, rowe});
   make_desc(v, tb.v, pl->kv_dtype, {tb.pool_pages, pl->page, pl->hkv, rowe});
   make_desc(sc, tb.scales, FD_FP32, {2, tb.pool_pages, pl->page, pl->hkv, ng});
-  make_desc(pt, tb.pt, FD_INT32, {batch, tb.width});
   make_desc(sq, tb.sl, FD_INT32, {batch});
   make_desc(out, tb.out, FD_BF16, {batch, tb.tq, pl->hq, pl->d});
   make_desc(lse, tb.lse, FD_FP32, {batch, tb.tq, pl->hq});
   fd_plan *prev = fd_get_plan();
   fd_set_plan(pl);
-  cudaEvent_t e0, e1;
-  cudaEventCreate(&e0);
-  cudaEventCreate(&e1);
-  std::vector<float> times;
+  const bool was_profiling = pl->profiling;
+  pl->profiling = false;
+
   fd_status s = FD_OK;
-  for (int rep = 0; rep < 4 && s == FD_OK; ++rep) {
-    cudaMemsetAsync(tb.flush, rep & 0xff, tb.flush_bytes, st);
-    cudaEventRecord(e0, st);
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  cudaError_t ce = cudaStreamBeginCapture(ts, cudaStreamCaptureModeThreadLocal);
+  if (ce != cudaSuccess) s = fail(FD_ERR_CUDA, "autotune: capture failed: %s", cudaGetErrorString(ce));
+  for (int i = 0; i < n_seq && s == FD_OK; ++i) {
+    fd_tensor pt;
+    make_desc(pt, tb.pt + static_cast<size_t>(i) * call_pages, FD_INT32, {batch, tb.width});
     s = fd_decode_paged(&q, &k, &v, tb.scales ? &sc : nullptr, &pt, &sq, tb.tq, S, &out, &lse,
-                        reinterpret_cast<fd_stream_t>(st));
-    cudaEventRecord(e1, st);
-    if (cudaEventSynchronize(e1) != cudaSuccess) s = fail(FD_ERR_CUDA, "autotune: timing call failed");
-    float ms = 0.f;
-    cudaEventElapsedTime(&ms, e0, e1);
-    if (rep > 0) times.push_back(ms);  // first call warms up
+                        reinterpret_cast<fd_stream_t>(ts));
   }
-  cudaEventDestroy(e0);
-  cudaEventDestroy(e1);
+  if (ce == cudaSuccess) {
+    const cudaError_t e2 = cudaStreamEndCapture(ts, &graph);
+    if (s == FD_OK && e2 != cudaSuccess)
+      s = fail(FD_ERR_CUDA, "autotune: capture failed: %s", cudaGetErrorString(e2));
+  }
+  if (s == FD_OK && cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess)
+    s = fail(FD_ERR_CUDA, "autotune: graph instantiation failed");
+
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  std::vector<float> times;
+  if (s == FD_OK) {
+    cudaEventCreate(&e0);
+    cudaEventCreate(&e1);
+    // the first replay uploads the graph and warms up
+    if (cudaGraphLaunch(exec, ts) != cudaSuccess) s = fail(FD_ERR_CUDA, "autotune: graph launch failed");
+  }
+  for (int blk = 0; blk < 3 && s == FD_OK; ++blk) {
+    cudaEventRecord(e0, ts);
+    for (int r = 0; r < reps && s == FD_OK; ++r)
+      if (cudaGraphLaunch(exec, ts) != cudaSuccess) s = fail(FD_ERR_CUDA, "autotune: graph launch failed");
+    cudaEventRecord(e1, ts);
+    if (s == FD_OK && cudaEventSynchronize(e1) != cudaSuccess) s = fail(FD_ERR_CUDA, "autotune: timing failed");
+    float ms = 0.f;
+    if (s == FD_OK) cudaEventElapsedTime(&ms, e0, e1);
+    times.push_back(ms / (reps * n_seq));
+  }
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  if (exec) cudaGraphExecDestroy(exec);
+  if (graph) cudaGraphDestroy(graph);
+  pl->profiling = was_profiling;
   fd_set_plan(prev);
   if (s != FD_OK) return s;
   std::sort(times.begin(), times.end());
@@ -307,8 +372,9 @@ fd_status autotune_save(fd_plan *pl) {
 }
 
 int choose_splits(fd_plan *pl, int batch, int max_seqlen) {
-  if (pl->table.empty()) return heuristic_splits(pl, batch, max_seqlen);
-  const int bucket_q = max_seqlen > 0 ? next_pow2(max_seqlen) : 0;
+  const bool by_mean = pl->split_policy == FD_SPLIT_BALANCED && pl->mean_hint > 0;
+  if (pl->table.empty()) return heuristic_splits(pl, batch, by_mean ? pl->mean_hint : max_seqlen);
+  const int bucket_q = by_mean ? nearest_pow2(pl->mean_hint) : (max_seqlen > 0 ? next_pow2(max_seqlen) : 0);
   auto m = pl->memo.find({batch, bucket_q});
   if (m != pl->memo.end()) return m->second;
   std::set<int> batches;
@@ -425,20 +491,16 @@ fd_status fd_autotune(fd_plan *plan, const int *batch_sizes, int n_batch, int mi
       if (plan->timer) {
         t = plan->timer(plan->timer_user, key.first, key.second, S);
       } else {
-        fd_status s = tune_time(plan, tb, key.first, key.second, S, st, &t);
+        fd_status s = tune_time(plan, tb, key.first, key.second, S, &t);
         if (s != FD_OK) return s;
       }
       timed.emplace_back(S, t);
     }
-    // Among the candidates within 1% of the fastest (about the spread of the
-    // timing), take the most splits: uniform-length tuning inputs cannot show
-    // the imbalance of a mixed batch, which more (balanced) splits absorb.
-    double fastest = timed[0].second;
-    for (auto &c : timed) fastest = std::min(fastest, c.second);
-    int best = 0;
-    double best_t = 0.0;
+    // the fastest; on an exact tie, the fewer splits
+    int best = timed[0].first;
+    double best_t = timed[0].second;
     for (auto &c : timed)
-      if (c.second <= fastest * 1.01 && c.first > best) {
+      if (c.second < best_t) {
         best = c.first;
         best_t = c.second;
       }

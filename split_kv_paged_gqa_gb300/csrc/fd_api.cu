@@ -10,6 +10,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -218,10 +219,25 @@ fd_status fd_plan_workspace_bytes(fd_plan *plan, size_t *bytes) {
   return FD_OK;
 }
 
+fd_status fd_plan_set_split_policy(fd_plan *plan, int policy) {
+  if (!plan) return fail(FD_ERR_INVALID_ARG, "plan is NULL");
+  if (policy != FD_SPLIT_BALANCED && policy != FD_SPLIT_EQUAL)
+    return fail(FD_ERR_INVALID_ARG, "split policy %d unknown", policy);
+  plan->split_policy = policy;
+  return FD_OK;
+}
+
 fd_status fd_set_max_seqlen_hint(fd_plan *plan, int max_seqlen) {
   if (!plan) return fail(FD_ERR_INVALID_ARG, "plan is NULL");
   if (max_seqlen < 0) return fail(FD_ERR_INVALID_ARG, "max_seqlen %d < 0", max_seqlen);
   plan->seqlen_hint = max_seqlen;
+  return FD_OK;
+}
+
+fd_status fd_set_mean_seqlen_hint(fd_plan *plan, int mean_seqlen) {
+  if (!plan) return fail(FD_ERR_INVALID_ARG, "plan is NULL");
+  if (mean_seqlen < 0) return fail(FD_ERR_INVALID_ARG, "mean_seqlen %d < 0", mean_seqlen);
+  plan->mean_hint = mean_seqlen;
   return FD_OK;
 }
 
@@ -402,8 +418,16 @@ extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cach
   if (S < 0 || S > pl->max_splits) return fail(FD_ERR_INVALID_ARG, "num_splits %d not in [0, %d]", S, pl->max_splits);
   if (S == 0) S = fd::choose_splits(pl, B, pl->seqlen_hint);
   if (pl->device < 0) return fail(FD_ERR_WORKSPACE, "host-only plan cannot decode");
-  if (S > 1 && (!pl->o_part || static_cast<size_t>(B) * Tq * pl->hq * S > pl->ws_rows))
+  // Balanced splits (more than one request, a workspace with room for at
+  // least two partials per output row): s_cap partial rows per output row.
+  const size_t out_rows = static_cast<size_t>(B) * Tq * pl->hq;
+  const int s_room = pl->o_part ? static_cast<int>(std::min<size_t>(64, pl->ws_rows / out_rows)) : 0;
+  const bool balanced = pl->split_policy == FD_SPLIT_BALANCED && B > 1 && s_room >= 2;
+  const int s_cap = balanced ? s_room : S;
+  if (S > 1 && (!pl->o_part || out_rows * S > pl->ws_rows))
     return fail(FD_ERR_WORKSPACE, "plan workspace too small");
+  // any request may be split: merge kernel (or fused merge) needed
+  const bool merge = S > 1 || balanced;
 
   fd::DeviceGuard guard(pl->device);
   if (!guard.ok) return fail(FD_ERR_CUDA, "cannot make device %d current", pl->device);
@@ -440,10 +464,10 @@ extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cach
   p.R = p.G * Tq;
   p.row_tiles = (p.R + 15) / 16;
   p.num_splits = S;
-  // Equal splits per request. (A common chunk derived from the batch's max
-  // length measured slower on mixed-length batches: short requests' small
-  // splits already backfill the SMs, and a common chunk leaves empty CTAs.)
   p.chunk_min = 0;
+  p.balanced = balanced ? 1 : 0;
+  p.batch = B;
+  p.s_cap = s_cap;
   p.scale_log2 = pl->scale * 1.4426950408889634f;
   p.o_part = pl->o_part;
   p.lse_part = pl->lse_part;
@@ -459,7 +483,9 @@ extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cach
     p.l_sh = lse->stride[2];
   }
   p.status = pl->status;
-  p.counters = (S > 1 && !pl->merge_kernel) ? pl->counters : nullptr;
+  // The fused merge (FD_MERGE=fused) serves the equal policy only: under the
+  // balanced one a request with no keys has no split CTA to write its rows.
+  p.counters = (S > 1 && !balanced && !pl->merge_kernel) ? pl->counters : nullptr;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
@@ -476,12 +502,22 @@ extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cach
     FD_CUDA_TRY(cudaEventRecordWithFlags(ev[0], st, rec_flags));
   }
   dim3 grid(p.row_tiles * S, pl->hkv, B);
-  const long ctas = static_cast<long>(grid.x) * grid.y * grid.z;
-  const bool deep = ctas <= pl->num_sms;  // one wave: one CTA per SM with a deeper ring
-  cudaError_t e = fd::launch_stage1(pl->kind, D, S == 1, deep, tmk, tmv, p, grid, st);
+  if (balanced) {
+    // The batch has at most B * (S + 1) splits: sum_b ceil(n_b / cp) <=
+    // n_total / cp + B, and n_total / cp <= B * S.
+    const long long units = std::min<long long>(static_cast<long long>(B) * (S + 1), static_cast<long long>(B) * s_cap);
+    const long long x = units * pl->hkv * p.row_tiles;
+    if (x > 0x7fffffffLL) return fail(FD_ERR_UNSUPPORTED, "balanced split grid too large (%lld CTAs)", x);
+    grid = dim3(static_cast<unsigned>(x), 1, 1);
+  }
+  // One wave of the expected CTAs (B * S splits; the balanced grid's extra
+  // CTAs exit at once): one CTA per SM with a deeper ring.
+  const long ctas = static_cast<long>(p.row_tiles) * S * pl->hkv * B;
+  const bool deep = ctas <= pl->num_sms;
+  cudaError_t e = fd::launch_stage1(pl->kind, D, !merge, deep, tmk, tmv, p, grid, st);
   if (pl->profiling) FD_CUDA_TRY(cudaEventRecordWithFlags(ev[1], st, rec_flags));
   if (e != cudaSuccess) return fail(FD_ERR_CUDA, "stage-1 launch failed: %s (%d)", cudaGetErrorString(e), (int)e);
-  if (S > 1 && !p.counters) {
+  if (merge && !p.counters) {
     fd::Stage2Params p2;
     p2.o_part = pl->o_part;
     p2.lse_part = pl->lse_part;
@@ -490,6 +526,8 @@ extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cach
     p2.Hq = pl->hq;
     p2.D = D;
     p2.num_splits = S;
+    p2.balanced = p.balanced;
+    p2.s_cap = s_cap;
     p2.seqlens = p.seqlens;
     p2.sl_s = p.sl_s;
     p2.log2_page = p.log2_page;

@@ -142,6 +142,7 @@ extern "C" fd_status fd_decode_paged_static(const fd_tensor *q, const fd_tensor 
   pl.kv_dtype = static_cast<fd_dtype>(k_cache->dtype);
   pl.kind = kind;
   pl.max_splits = num_splits;
+  pl.split_policy = FD_SPLIT_EQUAL;  // the scratch is sized for num_splits rows per output row
   pl.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
   pl.o_part = s.scratch;
   pl.lse_part = s.scratch + rows * D;

@@ -11,10 +11,7 @@ namespace fd {
 enum KvKind : int { KV_BF16 = 0, KV_I8 = 1, KV_I4 = 2 };
 
 // Keys per split of a request with L keys: equal page-aligned chunks
-// P * ceil(ceil(L / S) / P), but never fewer than chunk_min keys. With
-// chunk_min derived from the batch's max length, every non-empty split of
-// every request holds about the same number of keys (load balance across a
-// mixed-length batch); requests shorter than the max use fewer splits.
+// P * ceil(ceil(L / S) / P), but never fewer than chunk_min keys.
 __host__ __device__ inline int split_chunk(int L, int S, int log2_page, int chunk_min) {
   const int per = (L + S - 1) / S;
   const int c = ((per + (1 << log2_page) - 1) >> log2_page) << log2_page;
@@ -29,7 +26,33 @@ __host__ __device__ inline int split_count(int L, int S, int log2_page, int chun
   return n < S ? n : S;
 }
 
+// Balanced split policy. A call asking for S splits per request cuts the
+// batch's n_total pages (sum over requests of ceil(L_b / P)) into chunks of
+//   cp = ceil(n_total / (B * S)) pages,
+// and a request of n pages gets ceil(n / cp) splits (at least 1, at most
+// s_cap), which then cut it into equal page-aligned chunks as split_chunk
+// does. Every split of the batch holds about cp pages, whatever the length
+// mix. With equal lengths, every request gets split_count(L, S) splits of
+// split_chunk(L, S) keys: the same splits as the equal policy.
+__host__ __device__ inline int balanced_chunk_pages(long long n_total, int B, int S) {
+  const long long units = static_cast<long long>(B) * S;
+  const long long cp = (n_total + units - 1) / units;
+  return cp < 1 ? 1 : (cp > 0x7fffffffLL ? 0x7fffffff : static_cast<int>(cp));
+}
+
+// The split budget of a request with n pages (the S that split_chunk and
+// split_count take for it).
+__host__ __device__ inline int balanced_budget(int n_pages, int cp, int s_cap) {
+  if (n_pages <= 0) return 1;
+  const int s = static_cast<int>((static_cast<long long>(n_pages) + cp - 1) / cp);
+  return s < s_cap ? s : s_cap;
+}
+
 // Stage 1: one CTA per (row tile, split, KV head, request).
+// Equal policy: grid (row_tiles * S, Hkv, B). Balanced policy: a flat grid
+// over (split unit, KV head, row tile), x = (u * Hkv + h) * row_tiles + rt,
+// where units number the splits of the batch request by request; CTAs past
+// the batch's last unit exit at once.
 struct Stage1Params {
   const __nv_bfloat16 *q;          // [B, Tq, Hq, D]
   int64_t q_sb, q_st, q_sh;        // element strides of q (d stride is 1)
@@ -44,10 +67,14 @@ struct Stage1Params {
   int log2_page;                   // log2(P)
   int max_pages;                   // W
   int Tq, Hq, Hkv, G, R, row_tiles;
-  int num_splits;                  // S
-  int chunk_min;                   // minimum keys per split (0: equal splits per request)
+  int num_splits;                  // S (balanced policy: splits per request on average)
+  int chunk_min;                   // minimum keys per split (0: none)
+  int balanced;                    // 1: balanced split policy (see balanced_chunk_pages)
+  int batch;                       // B
+  int s_cap;                       // partial rows per output row in the workspace (>= splits of any request)
   float scale_log2;                // softmax_scale * log2(e)
-  // split outputs (num_splits > 1): workspace rows [B, Tq, Hq, S] of D floats
+  // split outputs: workspace rows [B, Tq, Hq, s_cap] of D floats (a request
+  // with one non-empty split writes its final outputs directly instead)
   float *o_part;
   float *lse_part;
   // fused outputs (num_splits == 1)
@@ -67,7 +94,9 @@ struct Stage2Params {
   const float *o_part;
   const float *lse_part;
   int B, Tq, Hq, D, num_splits;
-  // the split geometry of stage 1: only the non-empty splits of a request are read
+  int balanced, s_cap;
+  // the split geometry of stage 1: only the non-empty splits of a request are
+  // read; a request with exactly one was written by stage 1 and is skipped
   const int *seqlens;
   int64_t sl_s;
   int log2_page, max_pages, chunk_min;

@@ -30,9 +30,11 @@ struct fd_plan {
   unsigned *counters = nullptr;  // [max_batch * hkv * max row tiles], fused split merge
   size_t n_counters = 0;
   bool merge_kernel = true;      // merge splits with the stage-2 kernel (FD_MERGE=fused: in stage 1)
+  int split_policy = FD_SPLIT_BALANCED;  // an fd_split_policy
 
   // num_splits selection
-  int seqlen_hint = 0;
+  int seqlen_hint = 0;  // host-known max of cache_seqlens (0: unknown)
+  int mean_hint = 0;    // host-known mean of cache_seqlens (0: unknown)
   std::map<std::pair<int, int>, int> table;         // (batch, bucket) -> num_splits
   std::map<std::pair<int, int>, double> table_time;  // (batch, bucket) -> best time
   std::map<std::pair<int, int>, int> memo;          // nearest-key lookups, cleared on save

@@ -51,6 +51,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "splitmap.cuh"
 
 namespace fd {
 
@@ -96,7 +97,10 @@ struct S1Cfg {
   static constexpr int QAB = QA_SMEM ? (D / 16) * 32 * 16 : 0;
   static constexpr int OFF_BAR = (OFF_QA + QAB + 7) / 8 * 8;
   static constexpr int OFF_FLAG = OFF_BAR + 2 * STAGES * 8;  // "this CTA merges" flag
-  static constexpr int SMEM = OFF_FLAG + 16;
+  // the epilogue's (request, split, length, budget | direct << 16), parked
+  // here through the main loop so they hold no registers there
+  static constexpr int OFF_META = OFF_FLAG + 16;
+  static constexpr int SMEM = OFF_META + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;         // slack to align the base to 1024
   // CTAs per SM the shared memory allows (228 KB per SM, 1 KB reserved per CTA)
   static constexpr int MIN_BLOCKS = 3 * (SMEM_ALLOC + 1024) <= 228 * 1024   ? 3
@@ -592,7 +596,7 @@ __device__ __forceinline__ void write_row_outputs(const Stage1Params &p, bool fu
     }
     if (write_lse && p.lse) p.lse[b * p.l_sb + t * p.l_st + hq * p.l_sh] = lse_nat;
   } else {
-    const int64_t rowi = ((static_cast<int64_t>(b) * p.Tq + t) * p.Hq + hq) * p.num_splits + s;
+    const int64_t rowi = ((static_cast<int64_t>(b) * p.Tq + t) * p.Hq + hq) * p.s_cap + s;
     float *dst = p.o_part + rowi * C::D + d0;
     for (int i = 0; i < nvals; i += 4)
       *reinterpret_cast<float4 *>(dst + i) = make_float4(vals[i], vals[i + 1], vals[i + 2], vals[i + 3]);
@@ -614,7 +618,7 @@ __device__ __forceinline__ void merge_tile(const Stage1Params &p, int b, int h, 
   for (int r = warp; r < nrows; r += nwarps) {
     const int rg = rt * 16 + r;
     const int t = rg / p.G, hq = h * p.G + (rg - t * p.G);
-    const int64_t base = ((static_cast<int64_t>(b) * p.Tq + t) * p.Hq + hq) * p.num_splits;
+    const int64_t base = ((static_cast<int64_t>(b) * p.Tq + t) * p.Hq + hq) * p.s_cap;
     const float l0 = lane < nv ? __ldcg(p.lse_part + base + lane) : -INFINITY;
     const float l1 = lane + 32 < nv ? __ldcg(p.lse_part + base + lane + 32) : -INFINITY;
     float M = fmaxf(l0, l1);
@@ -683,7 +687,7 @@ __device__ __forceinline__ void merge_tile(const Stage1Params &p, int b, int h, 
 template <class C>
 __device__ __forceinline__ int prefetch_first_blocks(const CUtensorMap *tmk, const CUtensorMap *tmv,
                                                      const Stage1Params &p, int b, int h, int s,
-                                                     int lane) {
+                                                     int S_req, int lane) {
   if (lane == 0) {
     tma_prefetch_desc(tmk);
     tma_prefetch_desc(tmv);
@@ -692,7 +696,7 @@ __device__ __forceinline__ int prefetch_first_blocks(const CUtensorMap *tmk, con
   const int cap = p.max_pages * P;
   int L = ld_relaxed_gpu(p.seqlens + b * p.sl_s);
   L = L < 0 ? 0 : (L > cap ? cap : L);
-  const int chunk = split_chunk(L, p.num_splits, p.log2_page, p.chunk_min);
+  const int chunk = split_chunk(L, S_req, p.log2_page, p.chunk_min);
   const int c0 = s * chunk;
   const int c1 = min(L, c0 + chunk);
   if (c0 >= c1) return L;
@@ -725,8 +729,23 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
   uint64_t *empty = full + C::STAGES;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rt = blockIdx.x % p.row_tiles, s = blockIdx.x / p.row_tiles;
-  const int h = blockIdx.y, b = blockIdx.z;
+  // Which (request b, split s of its S_req, KV head h, row tile rt) this CTA
+  // computes. Balanced policy: unit u of the batch, located after the wait.
+  int rt, h, u = 0, b, s;
+  if (p.balanced) {
+    rt = blockIdx.x % p.row_tiles;
+    h = (blockIdx.x / p.row_tiles) % p.Hkv;
+    u = blockIdx.x / (p.row_tiles * p.Hkv);
+    b = -1;
+    s = 0;
+  } else {
+    rt = blockIdx.x % p.row_tiles;
+    s = blockIdx.x / p.row_tiles;
+    h = blockIdx.y;
+    b = blockIdx.z;
+  }
+  int S_req = p.num_splits;
+  const int cap = p.max_pages * p.page_size;
   // The pipeline barriers read no input: set them up before the wait below.
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::STAGES; ++i) {
@@ -743,8 +762,20 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
   // while that kernel drains; they spend the wait pulling their first blocks
   // into L2 (from values that only steer prefetches).
   int hint_L = -1;  // deep producer warp: the length its prefetch used
+  int hint_b = b, hint_s = s, hint_S = S_req;
   if constexpr (DEEP) {
-    if (warp == C::NUM_CW) hint_L = prefetch_first_blocks<C>(&tmk, &tmv, p, b, h, s, lane);
+    if (warp == C::NUM_CW) {
+      if (p.balanced) {
+        const int cp = balanced_chunk_pages(
+            batch_pages<true>(p.seqlens, p.sl_s, p.batch, cap, p.log2_page, lane), p.batch, p.num_splits);
+        const SplitUnit su = locate_unit<true>(p.seqlens, p.sl_s, p.batch, cap, p.log2_page, cp, p.s_cap,
+                                               p.chunk_min, u, lane);
+        hint_b = su.b;
+        hint_s = su.s;
+        hint_S = su.sb;
+      }
+      if (hint_b >= 0) hint_L = prefetch_first_blocks<C>(&tmk, &tmv, p, hint_b, h, hint_s, hint_S, lane);
+    }
   }
   griddep_wait();
   // Every trigger of this kernel comes after its wait: the merge kernel relies
@@ -756,16 +787,30 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
   // on the resources their last wave uses.
   if constexpr (DEEP) griddep_launch_dependents();
 
+  if (p.balanced) {  // every warp locates the unit (same loads, same answer)
+    const int cp = balanced_chunk_pages(batch_pages<false>(p.seqlens, p.sl_s, p.batch, cap, p.log2_page, lane),
+                                        p.batch, p.num_splits);
+    const SplitUnit su =
+        locate_unit<false>(p.seqlens, p.sl_s, p.batch, cap, p.log2_page, cp, p.s_cap, p.chunk_min, u, lane);
+    if (su.b < 0) {  // past the batch's last split
+      if constexpr (!DEEP) griddep_launch_dependents();
+      return;
+    }
+    b = su.b;
+    s = su.s;
+    S_req = su.sb;
+  }
+
   // The deep producer loads its first page ids now, at the hinted split range,
   // in the same round trip as the length; they are used only if the length
   // read after the wait equals the hint (then the range is the same).
   int pn0 = 0, pn1 = 0;
   if constexpr (DEEP) {
     if (warp == C::NUM_CW && hint_L > 0) {
-      const int hc = split_chunk(hint_L, p.num_splits, p.log2_page, p.chunk_min);
-      const int h0 = s * hc, h1 = min(hint_L, h0 + hc);
+      const int hc = split_chunk(hint_L, hint_S, p.log2_page, p.chunk_min);
+      const int h0 = hint_s * hc, h1 = min(hint_L, h0 + hc);
       if (h0 < h1) {
-        const int *pt = p.page_table + b * p.pt_sb;
+        const int *pt = p.page_table + hint_b * p.pt_sb;
         const int first = h0 >> p.log2_page;
         const int np = ((min(h0 + C::BLOCK_N, h1) - 1) >> p.log2_page) - first + 1;
         pn0 = lane < np ? ld_cg(pt + first + lane) : 0;
@@ -798,14 +843,16 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
   // ---- split range from cache_seqlens (on the device; no host metadata)
   // (the deep variant read these words before the wait: take them from L2)
   int L = DEEP ? ld_cg(p.seqlens + b * p.sl_s) : p.seqlens[b * p.sl_s];
-  const int cap = p.max_pages * P;
   if (L < 0 || L > cap) {
     if (threadIdx.x == 0) atomicOr(p.status, FD_DEVSTAT_SEQLEN_OVERFLOW);
     L = L < 0 ? 0 : cap;
   }
-  const int chunk = split_chunk(L, p.num_splits, p.log2_page, p.chunk_min);
+  const int chunk = split_chunk(L, S_req, p.log2_page, p.chunk_min);
   const int c0 = s * chunk;
   const int c1 = min(L, c0 + chunk);
+  // A request with a single non-empty split gets its final outputs from this
+  // CTA; the merge skips it.
+  const bool direct = FUSED || split_count(L, S_req, p.log2_page, p.chunk_min) == 1;
 
   if (c0 >= c1) {
     // An empty split of a split call writes nothing: the merge reads only the
@@ -848,7 +895,7 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
       q0 = lane < np ? (DEEP ? ld_cg(pt + first + lane) : pt[first + lane]) : 0;
       q1 = lane + 32 < np ? (DEEP ? ld_cg(pt + first + 32 + lane) : pt[first + 32 + lane]) : 0;
     };
-    if (!DEEP || L != hint_L) load_pids(0, pn0, pn1);
+    if (!DEEP || L != hint_L || b != hint_b || s != hint_s || S_req != hint_S) load_pids(0, pn0, pn1);
     int issued = 0;
     for (int it = 0; it < n_iters; ++it) {
       int p0 = pn0, p1 = pn1;
@@ -925,6 +972,8 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
       const int i = threadIdx.x + k * C::NUM_CW * 32;
       if (i < Q_JOBS) *reinterpret_cast<uint4 *>(qs + (i / (D / 8)) * C::QROW + (i % (D / 8)) * 16) = qv[k];
     }
+    if (threadIdx.x == 0)
+      *reinterpret_cast<int4 *>(smem + C::OFF_META) = make_int4(b, s, L, S_req | (direct ? 1 << 16 : 0));
     named_barrier(1, C::NUM_CW * 32);
     uint32_t qa[D / 16][4];
     float qc[2][C::NG], rs[2];
@@ -1035,6 +1084,10 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
     l[1] += __shfl_xor_sync(0xffffffffu, l[1], 1);
     l[1] += __shfl_xor_sync(0xffffffffu, l[1], 2);
     named_barrier(1, C::NUM_CW * 32);  // every consumer is done with the ring
+    const int4 meta = *reinterpret_cast<const int4 *>(smem + C::OFF_META);  // after the barrier above
+    const int b_e = meta.x, s_e = meta.y, L_e = meta.z, S_e = meta.w & 0xffff;
+    const bool direct_e = (meta.w >> 16) != 0;
+    const int h_e = p.balanced ? (blockIdx.x / p.row_tiles) % p.Hkv : blockIdx.y;
     float *co = reinterpret_cast<float *>(smem);
     float *cm = reinterpret_cast<float *>(smem + C::CMB_O);
     float *cl = cm + C::NUM_CW * 16;
@@ -1092,18 +1145,18 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
         for (int w = 0; w < C::NUM_CW; ++w) a = fmaf(wt[w], co[(w * 16 + row) * C::CROW + d0 + i], a);
         vals[i] = a * inv;
       }
-      if (rg < p.R) write_row_outputs<C>(p, FUSED, b, h, s, rg, d0, vals, DPT, lse_nat, d0 == 0);
+      if (rg < p.R) write_row_outputs<C>(p, direct_e, b_e, h_e, s_e, rg, d0, vals, DPT, lse_nat, d0 == 0);
     }
     if constexpr (!FUSED) {
-      if (p.counters) {
+      if (p.counters && !direct_e) {
         // Fused merge: publish this split's partials, count it, and let the
         // last split of the (request, KV head, row tile) merge them all.
         volatile unsigned *flag = reinterpret_cast<volatile unsigned *>(smem + C::OFF_FLAG);
         __threadfence();
         named_barrier(1, C::NUM_CW * 32);
-        const int nv = split_count(L, p.num_splits, p.log2_page, p.chunk_min);
+        const int nv = split_count(L_e, S_e, p.log2_page, p.chunk_min);
         if (threadIdx.x == 0) {
-          unsigned *ctr = p.counters + (static_cast<int64_t>(b) * p.Hkv + h) * p.row_tiles + rt;
+          unsigned *ctr = p.counters + (static_cast<int64_t>(b_e) * p.Hkv + h_e) * p.row_tiles + rt;
           const unsigned done = atomicAdd(ctr, 1u) + 1u;
           const bool last = done == static_cast<unsigned>(nv);
           if (last) {
@@ -1113,7 +1166,7 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
           *flag = last ? 1u : 0u;
         }
         named_barrier(1, C::NUM_CW * 32);
-        if (*flag) merge_tile<C>(p, b, h, rt, nv, warp, C::NUM_CW, lane);
+        if (*flag) merge_tile<C>(p, b_e, h_e, rt, nv, warp, C::NUM_CW, lane);
       }
     }
   }

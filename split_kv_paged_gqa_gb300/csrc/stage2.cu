@@ -6,11 +6,13 @@
 // row (request, query token, query head) with split partials (o_s, lse_s):
 //   M = max_s lse_s,  w_s = exp(lse_s - M),  out = sum_s w_s o_s / sum_s w_s,
 //   lse = M + ln(sum_s w_s).
-// Only the non-empty splits of the row's request (split_count of its length)
-// are read; splits with lse_s = -inf (a row with no visible key in them) carry
-// weight 0 (their partial is a finite 0); a row whose splits are all empty gets
-// out = 0, lse = -inf. One warp per row; the
-// split partials of a row are contiguous (S x D fp32) and read coalesced.
+// Only the non-empty splits of the row's request (split_count of its length
+// and split budget) are read; a request with exactly one was written by
+// stage 1 directly and is skipped here. Splits with lse_s = -inf (a row with
+// no visible key in them) carry weight 0 (their partial is a finite 0); a row
+// whose splits are all empty gets out = 0, lse = -inf. One warp per row; the
+// split partials of a row are contiguous (nv x D fp32, at a stride of s_cap
+// rows per output row) and read coalesced.
 // Launched with programmatic dependent launch: the grid may start while stage 1
 // drains and waits on griddepcontrol before touching the workspace.
 #include <cuda_bf16.h>
@@ -18,6 +20,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "splitmap.cuh"
 
 namespace fd {
 
@@ -33,19 +36,25 @@ __global__ void __launch_bounds__(kS2Warps * 32) fd_stage2_kernel(const __grid_c
   const int row = blockIdx.x * kS2Warps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= p.B * p.Tq * p.Hq) return;
-  const int S = p.num_splits;
   const int b_row = row / (p.Hq * p.Tq);
+  const int cap = p.max_pages << p.log2_page;
   // The length is read before the wait: stage 1 triggers this grid only after
   // its own dependency wait, so whatever wrote the lengths before stage 1 has
   // completed by now, and stage 1 does not write them. It comes from L2, not
   // from a line this SM's L1 may still hold from an earlier kernel.
-  int L = ld_cg(p.seqlens + b_row * p.sl_s);
+  // The balanced split map is rebuilt from all the lengths, before the wait too.
+  const int L = load_len<false>(p.seqlens, p.sl_s, b_row, cap);  // clamped as stage 1 clamps it
+  int S_req = p.num_splits;
+  if (p.balanced) {
+    const int cp = balanced_chunk_pages(batch_pages<false>(p.seqlens, p.sl_s, p.B, cap, p.log2_page, lane), p.B,
+                                        p.num_splits);
+    S_req = balanced_budget((L + (1 << p.log2_page) - 1) >> p.log2_page, cp, p.s_cap);
+  }
+  const int nv = split_count(L, S_req, p.log2_page, p.chunk_min);  // splits stage 1 wrote
+  if (nv == 1) return;  // stage 1 wrote this row's outputs
   griddep_wait();
-  const int cap = p.max_pages << p.log2_page;
-  L = L < 0 ? 0 : (L > cap ? cap : L);  // as stage 1 clamps it
-  const int nv = split_count(L, S, p.log2_page, p.chunk_min);  // splits stage 1 wrote
-  const float *lp = p.lse_part + static_cast<int64_t>(row) * S;
-  const float *op = p.o_part + static_cast<int64_t>(row) * S * D + lane * VPL;
+  const float *lp = p.lse_part + static_cast<int64_t>(row) * p.s_cap;
+  const float *op = p.o_part + static_cast<int64_t>(row) * p.s_cap * D + lane * VPL;
   // The LSEs and the first 16 partials are requested together (one round
   // trip for up to 16 splits); the weights are applied once both are in.
   constexpr int U = 16;

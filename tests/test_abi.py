@@ -259,18 +259,18 @@ def test_nearest_match_is_invalidated_when_a_config_is_saved(tmp_path):
         fd.fd_plan_destroy(plan)
 
 
-def test_near_ties_go_to_more_splits_within_one_percent(tmp_path):
+def test_tuner_keeps_the_fastest_and_breaks_exact_ties_toward_fewer_splits(tmp_path):
     plan = _host_plan(B=64, S=64)
     try:
         fd.fd_autotune_set_cache_dir(plan, str(tmp_path))
-        times = {1: 100.0, 2: 100.9, 4: 101.2, 8: 103.0}
+        times = {1: 100.0, 2: 99.5, 4: 101.2, 8: 103.0}
         fd.fd_autotune_set_timer(plan, lambda b, k, S: times.get(S, 200.0))
         fd.fd_autotune(plan, [64], 32768, 32768)
-        assert fd.fd_query_splits(plan, 64, 32768) == 2    # 0.9 % slower: kept; 1.2 %: not
-        times2 = {1: 100.0, 2: 101.3}
+        assert fd.fd_query_splits(plan, 64, 32768) == 2    # the argmin, however close
+        times2 = {2: 100.0, 4: 100.0, 1: 100.0}
         fd.fd_autotune_set_timer(plan, lambda b, k, S: times2.get(S, 200.0))
         fd.fd_autotune(plan, [16], 32768, 32768)
-        assert fd.fd_query_splits(plan, 16, 32768) == 1
+        assert fd.fd_query_splits(plan, 16, 32768) == 1    # exact tie: fewer splits
     finally:
         fd.fd_plan_destroy(plan)
 
@@ -299,5 +299,44 @@ def test_autotune_rejects_bad_arguments():
         with pytest.raises(fd.FdError) as e:                # host-only plan cannot time kernels
             fd.fd_autotune(plan, [1], 1024, 1024, stream=0)
         assert e.value.status == fd.FD_ERR_WORKSPACE
+    finally:
+        fd.fd_plan_destroy(plan)
+
+
+def test_split_policy_argument():
+    plan = _host_plan()
+    try:
+        fd.fd_plan_set_split_policy(plan, fd.FD_SPLIT_EQUAL)
+        fd.fd_plan_set_split_policy(plan, "balanced")
+        with pytest.raises(fd.FdError) as e:
+            fd.fd_plan_set_split_policy(plan, 2)
+        assert e.value.status == fd.FD_ERR_INVALID_ARG
+    finally:
+        fd.fd_plan_destroy(plan)
+    with pytest.raises(fd.FdError):
+        fd.fd_plan_set_split_policy(None, 0)
+
+
+def test_mean_hint_picks_the_nearest_bucket_under_the_balanced_policy(tmp_path):
+    plan = _host_plan(B=64, S=64)
+    try:
+        fd.fd_autotune_set_cache_dir(plan, str(tmp_path))
+        best = {4096: 2, 8192: 4, 16384: 8, 32768: 16}
+        fd.fd_autotune_set_timer(plan, lambda b, k, S: abs(S - best[k]) + 1.0)
+        fd.fd_autotune(plan, [64], 4096, 32768)
+        assert fd.fd_query_splits(plan, 64, 30000) == 16          # no mean hint: bucket of the max
+        fd.fd_set_mean_seqlen_hint(plan, 5932)                    # nearest power of two: 8192
+        assert fd.fd_query_splits(plan, 64, 30000) == 4
+        fd.fd_set_mean_seqlen_hint(plan, 5000)                    # below 8192 / sqrt(2): 4096
+        assert fd.fd_query_splits(plan, 64, 30000) == 2
+        fd.fd_set_mean_seqlen_hint(plan, 23000)                   # 16384 * sqrt(2) = 23170.5: 16384
+        assert fd.fd_query_splits(plan, 64, 30000) == 8
+        fd.fd_plan_set_split_policy(plan, "equal")                # equal splits: the max decides
+        assert fd.fd_query_splits(plan, 64, 30000) == 16
+        fd.fd_plan_set_split_policy(plan, "balanced")
+        fd.fd_set_mean_seqlen_hint(plan, 0)                       # cleared
+        assert fd.fd_query_splits(plan, 64, 30000) == 16
+        with pytest.raises(fd.FdError):
+            fd.fd_set_mean_seqlen_hint(plan, -1)
     finally:
         fd.fd_plan_destroy(plan)

@@ -71,14 +71,64 @@ def test_parity_cases(case, S):
     assert_needles(w, out, inp)
 
 
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-B{c[1]}-T{c[2]}-H{c[3]}/{c[4]}-D{c[5]}-P{c[6]}")
+@pytest.mark.parametrize("S", [3, 8])
+def test_parity_cases_equal_policy(case, S):
+    """The same cases with equal splits per request (FD_SPLIT_EQUAL)."""
+    shape = _shape(*case)
+    w = wl.make_workload(shape, 100 + CASES.index(case), "cuda", poison=True, needles=True, extra_pages=3)
+    inp = wl.oracle_inputs(w)
+    ref_out, ref_lse = decode_ref_inputs(inp)
+    plan = fd.fd_plan_create(0, shape.batch, shape.q_per_req, shape.num_q_heads, shape.num_kv_heads,
+                             shape.head_dim, shape.page_size, shape.kv_dtype, 64)
+    try:
+        fd.fd_plan_set_split_policy(plan, "equal")
+        out32, lse32 = run(w, S, torch.float32, plan=plan)
+        assert_parity(out32, lse32, ref_out, ref_lse, label=f"{case} S={S} equal")
+        assert_needles(w, out32, inp)
+    finally:
+        fd.fd_set_plan(None)
+        fd.fd_plan_destroy(plan)
+
+
+# ---------------------------------------------------------------------------
+# balanced splits on skewed batches: empty requests, one long request among
+# short ones, and a workspace so small that long requests hit its split cap
+
+
+@pytest.mark.parametrize("kind", ["bf16", "int8", "int4"])
+@pytest.mark.parametrize("max_splits", [2, 64])
+def test_balanced_splits_on_skewed_batches(kind, max_splits):
+    Tq = 4 if kind == "int4" else 1
+    lengths = (0, 9000, 3, 40, 0, 129, 1, 2000)
+    shape = _shape(kind, len(lengths), Tq, 16, 4, 128, 16, lengths)
+    w = wl.make_workload(shape, 55, "cuda", poison=True, needles=True)
+    inp = wl.oracle_inputs(w)
+    ref_out, ref_lse = decode_ref_inputs(inp)
+    # max_splits 2: the workspace holds 2 partials per output row, so the long
+    # request is cut into 2 splits however many the balanced map asks for
+    plan = fd.fd_plan_create(0, shape.batch, Tq, 16, 4, 128, 16, kind, max_splits)
+    try:
+        for S in sorted({1, 2, min(4, max_splits), max_splits}):
+            out32, lse32 = run(w, S, torch.float32, plan=plan)
+            assert_parity(out32, lse32, ref_out, ref_lse, label=f"{kind} balanced S={S} cap={max_splits}")
+            assert_needles(w, out32, inp)
+    finally:
+        fd.fd_set_plan(None)
+        fd.fd_plan_destroy(plan)
+
+
 # ---------------------------------------------------------------------------
 # results for different num_splits agree
 
 
+@pytest.mark.parametrize("policy", ["balanced", "equal"])
 @pytest.mark.parametrize("kind", ["bf16", "int8", "int4"])
-def test_cross_split_agreement(kind):
+def test_cross_split_agreement(kind, policy):
     shape = _shape(kind, 3, 1, 32, 8, 128, 16, (3000, 5000, 129))
     w = wl.make_workload(shape, 7, "cuda", poison=True)
+    plan = plan_for(shape)
+    fd.fd_plan_set_split_policy(plan, policy)
     base_f, base_l = run(w, 1, torch.float32)
     base_b, _ = run(w, 1, torch.bfloat16)
     for S in (2, 4, 8, 16, 32, 64):
@@ -89,6 +139,7 @@ def test_cross_split_agreement(kind):
         d = (ob.float() - base_b.float()).abs()
         ulp = torch.where(base_b.float().abs() >= 0.5, 2.0 ** -7, 0.0)   # one bf16 rounding flip
         assert (d <= SPLIT_ATOL + ulp).all(), f"bf16 out S={S}: {d.max().item()}"
+    fd.fd_plan_set_split_policy(plan, "balanced")
 
 
 # ---------------------------------------------------------------------------
@@ -114,7 +165,8 @@ def test_mixed_lengths_with_max_length_hints(kind):
 
 
 # ---------------------------------------------------------------------------
-# split merge: fused into stage 1 (default) and the separate stage-2 kernel
+# split merge: the stage-2 kernel (default) and, under the equal split
+# policy, the opt-in fused merge in stage 1
 
 
 @pytest.mark.parametrize("kind", ["bf16", "int4"])
@@ -128,6 +180,10 @@ def test_fused_merge_matches_oracle_and_stage2_merge(kind, monkeypatch):
     monkeypatch.setenv("FD_MERGE", "fused")
     plan1 = fd.fd_plan_create(0, 4, Tq, 32, 8, 128, 16, kind, 64)
     monkeypatch.delenv("FD_MERGE")
+    # the fused merge serves the equal policy; both plans use it so that their
+    # splits, and so their rounding, are the same
+    fd.fd_plan_set_split_policy(plan1, "equal")
+    fd.fd_plan_set_split_policy(plan2, "equal")
     try:
         for S in (2, 7, 64):   # plan2: stage-2 kernel; plan1: fused merge, including an empty request
             o2, l2 = run(w, S, torch.float32, plan=plan2)
