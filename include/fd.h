@@ -241,7 +241,9 @@ FD_API fd_status fd_set_max_seqlen_hint(fd_plan *plan, int max_seqlen);
  * is then looked up at the power of two nearest the mean (log scale) instead
  * of the bucket of the max. Balanced splits give a mixed-length batch of mean
  * m the per-CTA work of an equal-length batch of length m, which is what the
- * table was tuned on. 0 clears the hint. Host only. */
+ * table was tuned on. If the max hint is also set and at least 1.25 x the
+ * mean, the table tuned on mixed lengths is used (when it has entries).
+ * 0 clears the hint. Host only. */
 FD_API fd_status fd_set_mean_seqlen_hint(fd_plan *plan, int mean_seqlen);
 
 /*
@@ -260,10 +262,12 @@ FD_API fd_status fd_set_mean_seqlen_hint(fd_plan *plan, int mean_seqlen);
  * the table (loaded from the cache directory), synthetic inputs of the bucket
  * length are timed as a decode loop runs them: a CUDA graph of consecutive
  * calls, each on pages of its own (together at least 4x L2 where memory
- * allows), replayed back to back, median of three timed blocks. The fastest
+ * allows), replayed back to back, median of five timed blocks. The fastest
  * candidate is stored (an exact tie goes to fewer splits) and the table
- * saved. Tuning inputs have equal lengths; the balanced split policy carries
- * the pick over to mixed-length batches. Refuses with FD_ERR_CAPTURING while
+ * saved. Each (batch, bucket K) is tuned twice: with every request K keys
+ * long, and (batches of 2 or more) with lengths spread evenly over
+ * [K/8, 15K/8] (mean K), the table that calls whose hints show a spread use
+ * (see fd_set_mean_seqlen_hint). Refuses with FD_ERR_CAPTURING while
  * the stream is capturing. FD_FORCE_AUTOTUNE=1 ignores cached entries once.
  * Allocates temporary device buffers and a private stream (freed before
  * return); the timing runs on that stream after the work of `stream`.
@@ -278,7 +282,8 @@ FD_API fd_status fd_autotune(fd_plan *plan, const int *batch_sizes, int n_batch,
 FD_API fd_status fd_query_splits(fd_plan *plan, int batch, int max_seqlen, int *num_splits);
 
 /* Timer hook for fd_autotune: returns the time of one call with num_splits
- * for (batch, bucket), in any unit. NULL restores CUDA-event timing. With a
+ * for (batch, bucket), in any unit; bucket is negative (-K) for the
+ * mixed-length inputs of bucket K. NULL restores CUDA-event timing. With a
  * hook installed fd_autotune launches nothing, so its table logic can be
  * exercised on a host-only plan. */
 typedef double (*fd_timer_fn)(void *user, int batch, int bucket, int num_splits);

@@ -10,15 +10,19 @@
 // "Changes": FORCE_AUTOTUNE as adaptive tuning); cached nearest-key matches are
 // invalidated when a new configuration is saved.
 //
-// Table key: (batch, bucket) with bucket a power of two of the KV length.
+// Table key: (batch, bucket) with bucket a power of two of the KV length,
+// stored as -bucket for the mixed-length table (see tuning_lengths).
 // Lookup for a call: the nearest tuned batch (smallest >= B, else the
 // largest), then the lookup bucket (exact, else the smallest larger, else the
 // largest), memoised until the next save. The lookup bucket is the next power
 // of two >= the host-known max length; under the balanced split policy with a
 // mean-length hint it is the power of two nearest the mean instead: balanced
-// splits give a mixed batch of mean m the per-CTA work of an equal-length
-// batch of length m, which is what the table was tuned on. Without any entry
-// a heuristic sizes the grid to two CTAs per SM.
+// splits give a mixed batch of mean m about the per-CTA work of an
+// equal-length batch of length m. When the hints also show a spread (max >=
+// 1.25 x mean), the mixed-length table is used: at few splits per request,
+// the uneven last splits of a mixed batch leave SMs idle that an equal-length
+// batch keeps busy, so the two want different counts. Without any entry a
+// heuristic sizes the grid to two CTAs per SM.
 #include <cuda_runtime.h>
 #include <sys/stat.h>
 
@@ -84,6 +88,16 @@ std::vector<int> candidate_splits(const fd_plan *pl, int batch) {
 
 const char *kv_name(fd_dtype t) {
   return t == FD_BF16 ? "bf16" : t == FD_INT8 ? "int8" : t == FD_INT4X2 ? "int4" : "x";
+}
+
+// Request lengths of the tuning inputs for bucket K: all K, or (mixed) spread
+// evenly over [K/8, 15K/8], whose mean is K.
+std::vector<int> tuning_lengths(int batch, int bucket, bool mixed) {
+  std::vector<int> L(batch, bucket);
+  if (mixed && batch > 1)
+    for (int i = 0; i < batch; ++i)
+      L[i] = std::max(1, static_cast<int>(std::lround(bucket * (1.0 + 14.0 * i / (batch - 1)) / 8.0)));
+  return L;
 }
 
 std::string cache_path(const fd_plan *pl) {
@@ -156,7 +170,7 @@ fd_status tune_alloc(fd_plan *pl, TuneBuffers &tb, int bmax, int max_bucket, cud
   const size_t page_bytes = static_cast<size_t>(pl->page) * pl->hkv * rowe * es;
   tb.bmax = bmax;
   tb.tq = pl->max_q;
-  tb.width = (max_bucket + pl->page - 1) / pl->page;
+  tb.width = (2 * max_bucket + pl->page - 1) / pl->page;  // room for mixed lengths up to 15/8 bucket
   // Pool: distinct pages for the largest batch's call and for a sequence of
   // eight one-request calls, at least 4x L2 of K+V, at most a quarter of the
   // free device memory (beyond that, page ids wrap around the pool).
@@ -222,20 +236,21 @@ void make_desc(fd_tensor &t, void *data, fd_dtype dt, std::initializer_list<int6
 // loop: a CUDA graph of n_seq calls, each on pages of its own, replayed back
 // to back (each call's start overlaps the previous call's end). The calls of
 // a sequence together read at least 4x L2 where the pool allows, so no call
-// finds its pages in L2 from the previous replay. Median of three blocks of
-// at least eight calls.
-fd_status tune_time(fd_plan *pl, TuneBuffers &tb, int batch, int bucket, int S, double *ms_out) {
+// finds its pages in L2 from the previous replay. Median of five blocks of
+// at least sixteen calls (candidates 2 % apart must not swap places by noise).
+fd_status tune_time(fd_plan *pl, TuneBuffers &tb, int batch, int bucket, bool mixed, int S, double *ms_out) {
   const int rowe = pl->kv_dtype == FD_INT4X2 ? pl->d / 2 : pl->d;
   const int ng = pl->kv_dtype == FD_INT4X2 ? pl->d / 32 : 1;
   const long call_pages = static_cast<long>(batch) * tb.width;
   const long fit = std::max(1L, tb.pool_pages / call_pages);  // sequences with distinct pages
-  const double call_bytes = static_cast<double>(batch) * bucket * pl->hkv * rowe *
-                            (pl->kv_dtype == FD_BF16 ? 4.0 : 2.0);
+  const std::vector<int> sl = tuning_lengths(batch, bucket, mixed);
+  double keys = 0.0;
+  for (int x : sl) keys += x;
+  const double call_bytes = keys * pl->hkv * rowe * (pl->kv_dtype == FD_BF16 ? 4.0 : 2.0);
   const long cold = static_cast<long>(std::ceil(4.0 * tb.l2_bytes / std::max(call_bytes, 1.0)));
   const int n_seq = static_cast<int>(std::min<long>({fit, static_cast<long>(kMaxSeq), std::max(1L, cold)}));
-  const int reps = std::max(1, (8 + n_seq - 1) / n_seq);  // replays per timed block
+  const int reps = std::max(1, (16 + n_seq - 1) / n_seq);  // replays per timed block
   cudaStream_t ts = tb.ts;
-  std::vector<int> sl(batch, bucket);
   TRY_CUDA(cudaMemcpyAsync(tb.sl, sl.data(), sl.size() * 4, cudaMemcpyHostToDevice, ts));
   TRY_CUDA(cudaStreamSynchronize(ts));
   fd_tensor q, k, v, sc, sq, out, lse;
@@ -278,7 +293,7 @@ fd_status tune_time(fd_plan *pl, TuneBuffers &tb, int batch, int bucket, int S, 
     // the first replay uploads the graph and warms up
     if (cudaGraphLaunch(exec, ts) != cudaSuccess) s = fail(FD_ERR_CUDA, "autotune: graph launch failed");
   }
-  for (int blk = 0; blk < 3 && s == FD_OK; ++blk) {
+  for (int blk = 0; blk < 5 && s == FD_OK; ++blk) {
     cudaEventRecord(e0, ts);
     for (int r = 0; r < reps && s == FD_OK; ++r)
       if (cudaGraphLaunch(exec, ts) != cudaSuccess) s = fail(FD_ERR_CUDA, "autotune: graph launch failed");
@@ -339,10 +354,11 @@ fd_status autotune_load(fd_plan *pl) {
     const size_t close = txt.find('}', pos);
     if (close == std::string::npos) break;
     const std::string obj = txt.substr(pos, close - pos);
-    long b, k, s;
+    long b, k, s, spread = 0;
+    if (!field(obj, "spread", &spread)) spread = 0;
     if (field(obj, "batch", &b) && field(obj, "bucket", &k) && field(obj, "num_splits", &s) && b >= 1 &&
         is_pow2(static_cast<int>(k)) && s >= 1 && s <= pl->max_splits)
-      pl->table[{static_cast<int>(b), static_cast<int>(k)}] = static_cast<int>(s);
+      pl->table[{static_cast<int>(b), static_cast<int>(spread ? -k : k)}] = static_cast<int>(s);
     pos = close;
   }
   pl->memo.clear();
@@ -361,8 +377,9 @@ fd_status autotune_save(fd_plan *pl) {
   bool first = true;
   for (const auto &kv : pl->table) {
     auto t = pl->table_time.find(kv.first);
-    fprintf(f, "%s\n    {\"batch\": %d, \"bucket\": %d, \"num_splits\": %d, \"time\": %.6g}", first ? "" : ",",
-            kv.first.first, kv.first.second, kv.second, t == pl->table_time.end() ? 0.0 : t->second);
+    fprintf(f, "%s\n    {\"batch\": %d, \"bucket\": %d, \"spread\": %d, \"num_splits\": %d, \"time\": %.6g}",
+            first ? "" : ",", kv.first.first, std::abs(kv.first.second), kv.first.second < 0 ? 1 : 0, kv.second,
+            t == pl->table_time.end() ? 0.0 : t->second);
     first = false;
   }
   fprintf(f, "\n  ]\n}\n");
@@ -375,15 +392,23 @@ int choose_splits(fd_plan *pl, int batch, int max_seqlen) {
   const bool by_mean = pl->split_policy == FD_SPLIT_BALANCED && pl->mean_hint > 0;
   if (pl->table.empty()) return heuristic_splits(pl, batch, by_mean ? pl->mean_hint : max_seqlen);
   const int bucket_q = by_mean ? nearest_pow2(pl->mean_hint) : (max_seqlen > 0 ? next_pow2(max_seqlen) : 0);
-  auto m = pl->memo.find({batch, bucket_q});
+  bool mixed = by_mean && batch > 1 && 4LL * max_seqlen >= 5LL * pl->mean_hint;
+  const int memo_key = mixed ? -bucket_q : bucket_q;
+  auto m = pl->memo.find({batch, memo_key});
   if (m != pl->memo.end()) return m->second;
   std::set<int> batches;
-  for (const auto &kv : pl->table) batches.insert(kv.first.first);
+  for (const auto &kv : pl->table)
+    if ((kv.first.second < 0) == mixed) batches.insert(kv.first.first);
+  if (batches.empty()) {  // no mixed-length entries: the equal-length table
+    mixed = false;
+    for (const auto &kv : pl->table)
+      if (kv.first.second > 0) batches.insert(kv.first.first);
+  }
   auto bi = batches.lower_bound(batch);
   const int tb = bi != batches.end() ? *bi : *batches.rbegin();
-  std::set<int> buckets;
+  std::set<int> buckets;  // absolute buckets of the chosen table
   for (const auto &kv : pl->table)
-    if (kv.first.first == tb) buckets.insert(kv.first.second);
+    if (kv.first.first == tb && (kv.first.second < 0) == mixed) buckets.insert(std::abs(kv.first.second));
   int kb;
   if (bucket_q == 0) {
     kb = *buckets.rbegin();
@@ -391,8 +416,8 @@ int choose_splits(fd_plan *pl, int batch, int max_seqlen) {
     auto ki = buckets.lower_bound(bucket_q);
     kb = ki != buckets.end() ? *ki : *buckets.rbegin();
   }
-  const int S = std::min(pl->table[{tb, kb}], pl->max_splits);
-  pl->memo[{batch, bucket_q}] = S;
+  const int S = std::min(pl->table[{tb, mixed ? -kb : kb}], pl->max_splits);
+  pl->memo[{batch, memo_key}] = S;
   return S;
 }
 
@@ -463,16 +488,20 @@ fd_status fd_autotune(fd_plan *plan, const int *batch_sizes, int n_batch, int mi
   const char *force_env = std::getenv("FD_FORCE_AUTOTUNE");
   const bool force = force_env && force_env[0] == '1';
 
+  // keys (batch, bucket) for equal lengths and (batch, -bucket) for mixed
+  // lengths (batches of two or more requests)
   std::vector<std::pair<int, int>> todo;
   for (int i = 0; i < n_batch; ++i)
-    for (int k = min_bucket; k <= max_bucket; k <<= 1) {
-      const std::pair<int, int> key{batch_sizes[i], k};
-      if (!force && plan->table.count(key)) {
-        ++plan->cache_hits;
-        continue;
+    for (int k = min_bucket; k <= max_bucket; k <<= 1)
+      for (int sign : {1, -1}) {
+        if (sign < 0 && batch_sizes[i] < 2) continue;
+        const std::pair<int, int> key{batch_sizes[i], sign * k};
+        if (!force && plan->table.count(key)) {
+          ++plan->cache_hits;
+          continue;
+        }
+        if (std::find(todo.begin(), todo.end(), key) == todo.end()) todo.push_back(key);
       }
-      if (std::find(todo.begin(), todo.end(), key) == todo.end()) todo.push_back(key);
-    }
   if (todo.empty()) return FD_OK;
 
   fd::DeviceGuard guard(plan->device);
@@ -491,7 +520,7 @@ fd_status fd_autotune(fd_plan *plan, const int *batch_sizes, int n_batch, int mi
       if (plan->timer) {
         t = plan->timer(plan->timer_user, key.first, key.second, S);
       } else {
-        fd_status s = tune_time(plan, tb, key.first, key.second, S, &t);
+        fd_status s = tune_time(plan, tb, key.first, std::abs(key.second), key.second < 0, S, &t);
         if (s != FD_OK) return s;
       }
       timed.emplace_back(S, t);

@@ -189,20 +189,23 @@ def _fake_timer(best_for):
 
 def test_autotune_buckets_nearest_and_persistence(tmp_path, monkeypatch):
     monkeypatch.delenv("FD_FORCE_AUTOTUNE", raising=False)
-    best = lambda b, k: min(64, max(1, k // (256 * b)))        # a made-up optimum
+    # a made-up optimum; the mixed-length inputs (bucket -K) want twice the splits
+    best = lambda b, k: min(64, max(1, abs(k) // (256 * b)) * (2 if k < 0 else 1))
     plan = _host_plan(B=64, S=64)
     try:
         fd.fd_autotune_set_cache_dir(plan, str(tmp_path))
         timer, calls = _fake_timer(best)
         fd.fd_autotune_set_timer(plan, timer)
         fd.fd_autotune(plan, [1, 16], 1024, 8192)
-        # 2 batches x 4 buckets; every power of two up to 64 is tried for each key,
-        # plus split counts that fill one or two waves of the SMs
-        assert fd.fd_autotune_stats(plan) == (8, 0)
+        # 4 buckets x (batch 1: equal lengths; batch 16: equal and mixed lengths);
+        # every power of two up to 64 is tried for each key, plus split counts
+        # that fill one or two waves of the SMs
+        assert fd.fd_autotune_stats(plan) == (12, 0)
         per_key = {}
         for b, k, S in calls:
             per_key.setdefault((b, k), []).append(S)
-        assert len(per_key) == 8
+        assert len(per_key) == 12 and sum(1 for b, k in per_key if k < 0) == 4
+        assert all(b == 16 for b, k in per_key if k < 0)
         for S_list in per_key.values():
             assert {1, 2, 4, 8, 16, 32, 64} <= set(S_list) and max(S_list) <= 64
             assert len(S_list) == len(set(S_list))
@@ -220,11 +223,18 @@ def test_autotune_buckets_nearest_and_persistence(tmp_path, monkeypatch):
         files = list(tmp_path.glob("fd_splits_*.json"))
         assert len(files) == 1
         entries = json.load(open(files[0]))["entries"]
-        assert len(entries) == 8
+        assert len(entries) == 12 and sum(e["spread"] for e in entries) == 4
+        assert all(e["bucket"] > 0 for e in entries)
+        # hints that show a spread (max >= 1.25 x mean) use the mixed-length table
+        fd.fd_set_mean_seqlen_hint(plan, 2000)
+        assert fd.fd_query_splits(plan, 16, 8000) == best(16, -2048)
+        assert fd.fd_query_splits(plan, 16, 2400) == best(16, 2048)   # max / mean = 1.2
+        assert fd.fd_query_splits(plan, 1, 8000) == best(1, 2048)     # one request: no spread
+        fd.fd_set_mean_seqlen_hint(plan, 0)
         # a second call is served from the table: no new search
         calls.clear()
         fd.fd_autotune(plan, [1, 16], 1024, 8192)
-        assert calls == [] and fd.fd_autotune_stats(plan) == (8, 8)
+        assert calls == [] and fd.fd_autotune_stats(plan) == (12, 12)
     finally:
         fd.fd_plan_destroy(plan)
 
@@ -236,7 +246,9 @@ def test_autotune_buckets_nearest_and_persistence(tmp_path, monkeypatch):
         timer2, calls2 = _fake_timer(best)
         fd.fd_autotune_set_timer(plan2, timer2)
         fd.fd_autotune(plan2, [16], 1024, 8192)
-        assert calls2 == [] and fd.fd_autotune_stats(plan2) == (0, 4)
+        assert calls2 == [] and fd.fd_autotune_stats(plan2) == (0, 8)
+        fd.fd_set_mean_seqlen_hint(plan2, 2000)                      # the mixed table reloads too
+        assert fd.fd_query_splits(plan2, 16, 8000) == best(16, -2048)
         # FD_FORCE_AUTOTUNE re-searches even cached keys
         monkeypatch.setenv("FD_FORCE_AUTOTUNE", "1")
         fd.fd_autotune(plan2, [16], 1024, 1024)
@@ -322,15 +334,17 @@ def test_mean_hint_picks_the_nearest_bucket_under_the_balanced_policy(tmp_path):
     try:
         fd.fd_autotune_set_cache_dir(plan, str(tmp_path))
         best = {4096: 2, 8192: 4, 16384: 8, 32768: 16}
-        fd.fd_autotune_set_timer(plan, lambda b, k, S: abs(S - best[k]) + 1.0)
+        best_mixed = {4096: 4, 8192: 8, 16384: 16, 32768: 32}
+        fd.fd_autotune_set_timer(plan, lambda b, k, S: abs(S - (best[k] if k > 0 else best_mixed[-k])) + 1.0)
         fd.fd_autotune(plan, [64], 4096, 32768)
         assert fd.fd_query_splits(plan, 64, 30000) == 16          # no mean hint: bucket of the max
         fd.fd_set_mean_seqlen_hint(plan, 5932)                    # nearest power of two: 8192
-        assert fd.fd_query_splits(plan, 64, 30000) == 4
+        assert fd.fd_query_splits(plan, 64, 7000) == 4            # max / mean < 1.25: equal lengths
+        assert fd.fd_query_splits(plan, 64, 30000) == 8           # spread: the mixed-length table
         fd.fd_set_mean_seqlen_hint(plan, 5000)                    # below 8192 / sqrt(2): 4096
-        assert fd.fd_query_splits(plan, 64, 30000) == 2
+        assert fd.fd_query_splits(plan, 64, 6000) == 2
         fd.fd_set_mean_seqlen_hint(plan, 23000)                   # 16384 * sqrt(2) = 23170.5: 16384
-        assert fd.fd_query_splits(plan, 64, 30000) == 8
+        assert fd.fd_query_splits(plan, 64, 24000) == 8
         fd.fd_plan_set_split_policy(plan, "equal")                # equal splits: the max decides
         assert fd.fd_query_splits(plan, 64, 30000) == 16
         fd.fd_plan_set_split_policy(plan, "balanced")

@@ -368,3 +368,32 @@ def test_full_size_sampled(name):
     assert_parity(out, lse, ref_out, ref_lse, requests=sample, label=name)
     del w
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
+# the startup tuner on the device: both tables, then decode with its pick
+
+
+def test_autotune_on_device_then_decode(tmp_path):
+    import json
+    shape = _shape("bf16", 4, 1, 16, 4, 128, 16, (300, 1800, 900, 40))
+    w = wl.make_workload(shape, 61, "cuda", poison=True)
+    ref_out, ref_lse = decode_ref_inputs(wl.oracle_inputs(w))
+    plan = fd.fd_plan_create(0, 4, 1, 16, 4, 128, 16, "bf16", 16)
+    try:
+        fd.fd_autotune_set_cache_dir(plan, str(tmp_path))
+        fd.fd_autotune(plan, [4], 1024, 2048)
+        assert fd.fd_autotune_stats(plan) == (4, 0)          # 2 buckets x (equal, mixed lengths)
+        entries = json.load(open(next(tmp_path.glob("fd_splits_*.json"))))["entries"]
+        assert len(entries) == 4 and sum(e["spread"] for e in entries) == 2
+        assert all(1 <= e["num_splits"] <= 16 and e["time"] > 0 for e in entries)
+        fd.fd_set_max_seqlen_hint(plan, 1800)
+        fd.fd_set_mean_seqlen_hint(plan, 760)
+        S = fd.fd_query_splits(plan, 4, 1800)
+        assert 1 <= S <= 16
+        out, lse = run(w, 0, torch.float32, plan=plan)         # num_splits from the table
+        assert_parity(out, lse, ref_out, ref_lse, label=f"tuned S={S}")
+        assert fd.fd_read_device_status(plan) == 0
+    finally:
+        fd.fd_set_plan(None)
+        fd.fd_plan_destroy(plan)
