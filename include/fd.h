@@ -126,7 +126,14 @@ typedef struct fd_plan fd_plan;
  *
  * Allocates the split workspace (fp32 partial outputs and LSE, sized for
  * max_batch * max_q_per_req * Hq * max_splits rows of D) and a status word on
- * the device. Reads FD_AUTOTUNE_CACHE_DIR for the tuning cache directory.
+ * the device. Reads, at creation:
+ *  - FD_AUTOTUNE_CACHE_DIR: the tuning cache directory;
+ *  - FD_MERGE=fused: merge splits in stage 1 (last split CTA of a tile)
+ *    instead of the stage-2 kernel (equal split policy only);
+ *  - FD_QUANT_KERNEL=tc: run INT8 / INT4 caches with head_dim 128 on the
+ *    tcgen05 stage-1 kernel (tensor-memory accumulators) instead of the
+ *    register (mma.sync) kernel. Same results within rounding; slower on
+ *    GB300 at the time of writing.
  */
 FD_API fd_status fd_plan_create(int device, int max_batch, int max_q_per_req, int num_q_heads,
                          int num_kv_heads, int head_dim, int page_size, fd_dtype kv_dtype,

@@ -158,6 +158,11 @@ fd_status fd_plan_create(int device, int max_batch, int max_q_per_req, int num_q
   // lengthens the critical path more than the second launch costs).
   const char *mg = std::getenv("FD_MERGE");
   pl->merge_kernel = !(mg && std::strcmp(mg, "fused") == 0);
+  // Quantised caches run stage 1 on the register (mma.sync) kernel;
+  // FD_QUANT_KERNEL=tc selects the tcgen05 kernel for head_dim 128 (measured
+  // slower on GB300: its code conversions run on two warps per scheduler).
+  const char *qk = std::getenv("FD_QUANT_KERNEL");
+  pl->quant_tc = qk && std::strcmp(qk, "tc") == 0;
 
   if (device >= 0) {
     fd::DeviceGuard guard(device);
@@ -514,7 +519,10 @@ extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cach
   // CTAs exit at once): one CTA per SM with a deeper ring.
   const long ctas = static_cast<long>(p.row_tiles) * S * pl->hkv * B;
   const bool deep = ctas <= pl->num_sms;
-  cudaError_t e = fd::launch_stage1(pl->kind, D, !merge, deep, tmk, tmv, p, grid, st);
+  // the tcgen05 kernel: quantised caches, head_dim 128, one row tile per CTA, merge by stage 2
+  const bool tc = pl->quant_tc && pl->kind != fd::KV_BF16 && D == 128 && !p.counters;
+  cudaError_t e = tc ? fd::launch_stage1_tc(pl->kind, !merge, tmk, tmv, p, grid, st)
+                     : fd::launch_stage1(pl->kind, D, !merge, deep, tmk, tmv, p, grid, st);
   if (pl->profiling) FD_CUDA_TRY(cudaEventRecordWithFlags(ev[1], st, rec_flags));
   if (e != cudaSuccess) return fail(FD_ERR_CUDA, "stage-1 launch failed: %s (%d)", cudaGetErrorString(e), (int)e);
   if (merge && !p.counters) {

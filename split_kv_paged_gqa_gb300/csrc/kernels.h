@@ -121,6 +121,12 @@ cudaError_t launch_stage1(int kind, int head_dim, bool fused, bool deep, const C
 
 cudaError_t launch_stage2(const Stage2Params &p, cudaStream_t stream, bool pdl);
 
+// Stage 1 on the tcgen05 tensor cores for INT8 / INT4 caches with head_dim
+// 128 (one row tile of up to 16 query rows per CTA, no fused merge).
+cudaError_t stage1_tc_prepare(int kind);
+cudaError_t launch_stage1_tc(int kind, bool fused, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                             const Stage1Params &p, dim3 grid, cudaStream_t stream);
+
 // Per-kind entry points (one translation unit each).
 cudaError_t stage1_prepare_bf16(int head_dim);
 cudaError_t stage1_prepare_i8(int head_dim);

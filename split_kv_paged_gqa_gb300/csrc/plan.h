@@ -31,6 +31,7 @@ struct fd_plan {
   size_t n_counters = 0;
   bool merge_kernel = true;      // merge splits with the stage-2 kernel (FD_MERGE=fused: in stage 1)
   int split_policy = FD_SPLIT_BALANCED;  // an fd_split_policy
+  bool quant_tc = false;  // INT8 / INT4 with head_dim 128 on the tcgen05 stage-1 kernel (FD_QUANT_KERNEL=tc)
 
   // num_splits selection
   int seqlen_hint = 0;  // host-known max of cache_seqlens (0: unknown)

@@ -55,14 +55,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, unsigned by
                : "memory");
 }
 
+// try_wait suspends the calling thread until the phase completes or the
+// suspend-time hint (nanoseconds) runs out, so a waiting warp issues almost
+// nothing while it waits.
+constexpr uint32_t kSuspendHintNs = 10000000u;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -211,6 +216,23 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// fp16x2 arithmetic on packed 32-bit registers
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, float v) {
+  __half2 r = __hsub2(*reinterpret_cast<__half2 *>(&a), __floats2half2_rn(v, v));
+  return *reinterpret_cast<uint32_t *>(&r);
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
+  return *reinterpret_cast<uint32_t *>(&r);
+}
+
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, float mul, float add) {
+  __half2 r = __hfma2(*reinterpret_cast<__half2 *>(&a), __floats2half2_rn(mul, mul),
+                      __floats2half2_rn(add, add));
+  return *reinterpret_cast<uint32_t *>(&r);
 }
 
 // TMA shared-memory swizzle of a byte offset inside a tile whose rows are

@@ -119,22 +119,6 @@ __device__ __forceinline__ uint32_t u8pair_to_f16_biased(uint32_t t) {
   return (t & 0x00FF00FFu) | 0x64006400u;
 }
 
-__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, float v) {
-  __half2 r = __hsub2(*reinterpret_cast<__half2 *>(&a), __floats2half2_rn(v, v));
-  return *reinterpret_cast<uint32_t *>(&r);
-}
-
-__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
-  __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
-  return *reinterpret_cast<uint32_t *>(&r);
-}
-
-__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, float mul, float add) {
-  __half2 r = __hfma2(*reinterpret_cast<__half2 *>(&a), __floats2half2_rn(mul, mul),
-                      __floats2half2_rn(add, add));
-  return *reinterpret_cast<uint32_t *>(&r);
-}
-
 // ----------------------------------------------------------------------------
 // One 16-key block of one warp, bf16 cache: scores, online softmax, PV.
 //
@@ -918,12 +902,13 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
       // segments of SEG slots starting at token tok0 + i * SEG, each inside one page
       const int nseg = (tend - tok0 + SEG - 1) >> log2_seg;
       if (lane == 0) mbar_arrive_expect_tx(&full[stage], static_cast<unsigned>(nseg) * seg_bytes * 2u);
-      for (int i = 0; i < nseg; ++i) {
-        const int ts = tok0 + (i << log2_seg);
+      {  // lane i issues segment i (a stage holds at most BLOCK_N / 8 <= 16 segments)
+        const int i = lane;
+        const int ts = tok0 + (min(i, nseg - 1) << log2_seg);
         const int pi = (ts >> p.log2_page) - first;
         const int a0 = __shfl_sync(0xffffffffu, p0, pi & 31);
         const int a1 = __shfl_sync(0xffffffffu, p1, pi & 31);
-        if (lane == 0) {
+        if (i < nseg) {
           const int pid = pi < 32 ? a0 : a1;
           const int slot0 = ts & (P - 1);
           const int row0 = i << log2_seg;

@@ -160,12 +160,14 @@ cudaError_t launch_stage2(const Stage2Params &p, cudaStream_t stream, bool pdl) 
 int stage1_block_n(int, int) { return 64; }
 
 cudaError_t stage1_prepare(int kind, int head_dim) {
+  cudaError_t e = cudaErrorInvalidValue;
   switch (kind) {
     case KV_BF16: return stage1_prepare_bf16(head_dim);
-    case KV_I8: return stage1_prepare_i8(head_dim);
-    case KV_I4: return stage1_prepare_i4(head_dim);
+    case KV_I8: e = stage1_prepare_i8(head_dim); break;
+    case KV_I4: e = stage1_prepare_i4(head_dim); break;
   }
-  return cudaErrorInvalidValue;
+  if (e == cudaSuccess && head_dim == 128) e = stage1_tc_prepare(kind);
+  return e;
 }
 
 cudaError_t launch_stage1(int kind, int head_dim, bool fused, bool deep, const CUtensorMap &tmk,

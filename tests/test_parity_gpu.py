@@ -91,6 +91,61 @@ def test_parity_cases_equal_policy(case, S):
         fd.fd_plan_destroy(plan)
 
 
+def _plan_with_env(shape, monkeypatch, max_splits=64, **env):
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    plan = fd.fd_plan_create(0, shape.batch, shape.q_per_req, shape.num_q_heads, shape.num_kv_heads,
+                             shape.head_dim, shape.page_size, shape.kv_dtype, max_splits)
+    for k in env:
+        monkeypatch.delenv(k)
+    return plan
+
+
+@pytest.mark.parametrize("case", [c for c in CASES if c[0] != "bf16" and c[5] == 128],
+                         ids=lambda c: f"{c[0]}-B{c[1]}-T{c[2]}-H{c[3]}/{c[4]}-D{c[5]}-P{c[6]}")
+@pytest.mark.parametrize("S", [1, 3, 8])
+def test_parity_cases_tcgen05_kernel(case, S, monkeypatch):
+    """Quantised head_dim-128 cases on the tcgen05 stage-1 kernel (FD_QUANT_KERNEL=tc)."""
+    shape = _shape(*case)
+    w = wl.make_workload(shape, 100 + CASES.index(case), "cuda", poison=True, needles=True, extra_pages=3)
+    inp = wl.oracle_inputs(w)
+    ref_out, ref_lse = decode_ref_inputs(inp)
+    plan = _plan_with_env(shape, monkeypatch, FD_QUANT_KERNEL="tc")
+    try:
+        out32, lse32 = run(w, S, torch.float32, plan=plan)
+        assert_parity(out32, lse32, ref_out, ref_lse, label=f"{case} S={S} tcgen05 kernel")
+        assert_needles(w, out32, inp)
+        out, lse = run(w, S, plan=plan)
+        assert_parity(out, lse, ref_out, ref_lse, label=f"{case} S={S} tcgen05 bf16 out", bf16_rounding=True)
+    finally:
+        fd.fd_set_plan(None)
+        fd.fd_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("kind", ["int8", "int4"])
+def test_tcgen05_kernel_skewed_batch_and_split_agreement(kind, monkeypatch):
+    Tq = 4 if kind == "int4" else 1
+    lengths = (0, 9000, 3, 40, 0, 129, 1, 2000)
+    shape = _shape(kind, len(lengths), Tq, 16, 4, 128, 16, lengths)
+    w = wl.make_workload(shape, 56, "cuda", poison=True, needles=True)
+    inp = wl.oracle_inputs(w)
+    ref_out, ref_lse = decode_ref_inputs(inp)
+    plan = _plan_with_env(shape, monkeypatch, FD_QUANT_KERNEL="tc")
+    try:
+        base = None
+        for S in (1, 2, 7, 64):
+            out32, lse32 = run(w, S, torch.float32, plan=plan)
+            assert_parity(out32, lse32, ref_out, ref_lse, label=f"{kind} tcgen05 S={S}")
+            assert_needles(w, out32, inp)
+            if base is None:
+                base = out32
+            assert (out32 - base).abs().max().item() <= SPLIT_ATOL
+        assert fd.fd_read_device_status(plan) == 0
+    finally:
+        fd.fd_set_plan(None)
+        fd.fd_plan_destroy(plan)
+
+
 # ---------------------------------------------------------------------------
 # balanced splits on skewed batches: empty requests, one long request among
 # short ones, and a workspace so small that long requests hit its split cap
@@ -176,10 +231,14 @@ def test_fused_merge_matches_oracle_and_stage2_merge(kind, monkeypatch):
     w = wl.make_workload(shape, 88, "cuda", poison=True)
     ref_out, ref_lse = decode_ref_inputs(wl.oracle_inputs(w))
     monkeypatch.delenv("FD_MERGE", raising=False)
+    # the fused merge runs in the register stage-1 kernel: compare it with the
+    # stage-2 merge on the same stage-1 kernel
+    monkeypatch.setenv("FD_QUANT_KERNEL", "mma")
     plan2 = fd.fd_plan_create(0, 4, Tq, 32, 8, 128, 16, kind, 64)
     monkeypatch.setenv("FD_MERGE", "fused")
     plan1 = fd.fd_plan_create(0, 4, Tq, 32, 8, 128, 16, kind, 64)
     monkeypatch.delenv("FD_MERGE")
+    monkeypatch.delenv("FD_QUANT_KERNEL")
     # the fused merge serves the equal policy; both plans use it so that their
     # splits, and so their rounding, are the same
     fd.fd_plan_set_split_policy(plan1, "equal")
