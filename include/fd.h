@@ -265,7 +265,8 @@ FD_API fd_status fd_set_mean_seqlen_hint(fd_plan *plan, int mean_seqlen);
  *  stream                 stream for the timing launches.
  *
  * Candidates are num_splits in {1, 2, 4, ..., max_splits}, plus the counts
- * that fill one or two waves of one CTA per SM. For each key not already in
+ * that fill one or two waves of one CTA per SM, none cutting the bucket into
+ * splits of fewer than 128 keys. For each key not already in
  * the table (loaded from the cache directory), synthetic inputs of the bucket
  * length are timed as a decode loop runs them: a CUDA graph of consecutive
  * calls, each on pages of its own (together at least 4x L2 where memory

@@ -71,15 +71,18 @@ int heuristic_splits(const fd_plan *pl, int batch, int max_seqlen) {
 
 // Candidates: powers of two up to max_splits, plus the split counts that
 // fill one or two waves of one CTA per SM for this batch (e.g. 19 for one
-// request of 8 KV heads on 152 SMs), where a power of two leaves SMs idle.
-std::vector<int> candidate_splits(const fd_plan *pl, int batch) {
+// request of 8 KV heads on 152 SMs), where a power of two leaves SMs idle;
+// none that cuts the bucket length into splits of fewer than 128 keys (such
+// calls take microseconds, and their timing is noise).
+std::vector<int> candidate_splits(const fd_plan *pl, int batch, int bucket) {
+  const int cap = std::max(1, std::min(pl->max_splits, bucket / 128));
   std::vector<int> c;
-  for (int S = 1; S <= pl->max_splits; S <<= 1) c.push_back(S);
+  for (int S = 1; S <= cap; S <<= 1) c.push_back(S);
   const int G = pl->hq / pl->hkv;
   const long base = static_cast<long>(batch) * pl->hkv * ((G * pl->max_q + 15) / 16);
   for (int k = 1; k <= 2; ++k) {
     const long sw = k * static_cast<long>(pl->num_sms) / base;
-    if (sw >= 2 && sw <= pl->max_splits && !is_pow2(static_cast<int>(sw))) c.push_back(static_cast<int>(sw));
+    if (sw >= 2 && sw <= cap && !is_pow2(static_cast<int>(sw))) c.push_back(static_cast<int>(sw));
   }
   std::sort(c.begin(), c.end());
   c.erase(std::unique(c.begin(), c.end()), c.end());
@@ -515,7 +518,7 @@ fd_status fd_autotune(fd_plan *plan, const int *batch_sizes, int n_batch, int mi
   for (auto &key : todo) {
     ++plan->searches;
     std::vector<std::pair<int, double>> timed;
-    for (int S : candidate_splits(plan, key.first)) {
+    for (int S : candidate_splits(plan, key.first, std::abs(key.second))) {
       double t = 0.0;
       if (plan->timer) {
         t = plan->timer(plan->timer_user, key.first, key.second, S);

@@ -206,8 +206,10 @@ def test_autotune_buckets_nearest_and_persistence(tmp_path, monkeypatch):
             per_key.setdefault((b, k), []).append(S)
         assert len(per_key) == 12 and sum(1 for b, k in per_key if k < 0) == 4
         assert all(b == 16 for b, k in per_key if k < 0)
-        for S_list in per_key.values():
-            assert {1, 2, 4, 8, 16, 32, 64} <= set(S_list) and max(S_list) <= 64
+        for (b, k), S_list in per_key.items():
+            # powers of two whose splits hold at least 128 keys of the bucket
+            want = {S for S in (1, 2, 4, 8, 16, 32, 64) if S * 128 <= abs(k)}
+            assert want <= set(S_list) and max(S_list) <= min(64, abs(k) // 128)
             assert len(S_list) == len(set(S_list))
         for b in (1, 16):
             for k in (1024, 2048, 4096, 8192):
@@ -252,7 +254,7 @@ def test_autotune_buckets_nearest_and_persistence(tmp_path, monkeypatch):
         # FD_FORCE_AUTOTUNE re-searches even cached keys
         monkeypatch.setenv("FD_FORCE_AUTOTUNE", "1")
         fd.fd_autotune(plan2, [16], 1024, 1024)
-        assert {1, 2, 4, 8, 16, 32, 64} <= {c[2] for c in calls2} and len(calls2) >= 7
+        assert {1, 2, 4, 8} <= {c[2] for c in calls2} and len(calls2) >= 4
     finally:
         fd.fd_plan_destroy(plan2)
 
@@ -352,5 +354,20 @@ def test_mean_hint_picks_the_nearest_bucket_under_the_balanced_policy(tmp_path):
         assert fd.fd_query_splits(plan, 64, 30000) == 16
         with pytest.raises(fd.FdError):
             fd.fd_set_mean_seqlen_hint(plan, -1)
+    finally:
+        fd.fd_plan_destroy(plan)
+
+
+def test_tuner_skips_splits_shorter_than_128_keys(tmp_path):
+    plan = _host_plan(B=64, S=64)
+    try:
+        fd.fd_autotune_set_cache_dir(plan, str(tmp_path))
+        calls = []
+        fd.fd_autotune_set_timer(plan, lambda b, k, S: calls.append((abs(k), S)) or float(S))
+        fd.fd_autotune(plan, [2], 256, 1024)
+        for k, S in calls:
+            assert S * 128 <= k or S == 1, (k, S)
+        assert {S for k, S in calls if k == 1024} >= {1, 2, 4, 8}
+        assert {S for k, S in calls if k == 256} == {1, 2}
     finally:
         fd.fd_plan_destroy(plan)
