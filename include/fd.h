@@ -65,8 +65,16 @@ typedef enum fd_dtype {
   FD_FP32 = 1,
   FD_INT8 = 2,
   FD_INT4X2 = 3,  /* two signed 4-bit codes per byte, even channel in the low nibble */
-  FD_INT32 = 4
+  FD_INT32 = 4,
+  FD_INT64 = 5
 } fd_dtype;
+
+/* How fd_graph_metadata forms cu_seqlens_q. */
+typedef enum fd_q_mode {
+  FD_QMODE_PRESET = 0,  /* copied from q_in, int32 [B + 1] */
+  FD_QMODE_CUMSUM = 1,  /* exclusive prefix sum of q_in, int32 [B] query tokens per request */
+  FD_QMODE_STRIDED = 2  /* b * q_stride: q_stride query tokens per request */
+} fd_q_mode;
 
 /* How a call cuts its requests' keys into splits (fd_plan_set_split_policy). */
 typedef enum fd_split_policy {
@@ -235,6 +243,45 @@ FD_API fd_status fd_decode_paged_static(const fd_tensor *q, const fd_tensor *k_c
                                         const fd_tensor *page_table, const fd_tensor *cache_seqlens,
                                         int q_per_req, int num_splits, float softmax_scale,
                                         fd_tensor *out, fd_tensor *lse, fd_stream_t stream);
+
+/*
+ * fd_graph_metadata - the per-step metadata of a decode batch, built on the
+ * device in one launch from a serving engine's request-to-token pool: the
+ * step before fd_decode_paged in a graph-replayed decode loop ("sglang PR
+ * 29843" summary, section 实现拆解 item 1: one program per batch row builds
+ * cache_seqlens, cu_seqlens_k / cu_seqlens_q and page_table, three q modes
+ * and a -1 sentinel guard, replacing about 25 host-dispatched operations that
+ * cost 0.7-1.0 ms per replay, section 功能与动机).
+ *
+ *  req_to_token     int32 [R, C] (device): KV slot of token position c of
+ *                   pool request r, slot = page * P + offset; < 0 = no slot.
+ *                   A request's pages start on page boundaries.
+ *  req_pool_indices int32 or int64 [B]: pool row of batch row b; < 0 marks a
+ *                   padding row (all outputs of the row empty).
+ *  seq_lens         int32 [B]: keys of each request.
+ *  page_size        P >= 1.
+ *  q_mode           an fd_q_mode; q_in and q_stride as the mode says
+ *                   (q_in may be NULL for FD_QMODE_STRIDED).
+ *  page_table       int32 [B, W] out: entry j = req_to_token[r, j * P] / P
+ *                   for j < ceil(L_b / P), else -1 (also for an unallocated
+ *                   slot and on padding rows).
+ *  cache_seqlens    int32 [B] out: seq_lens (0 on padding rows).
+ *  cu_seqlens_k     int32 [B + 1] out: exclusive prefix sum of cache_seqlens.
+ *  cu_seqlens_q     int32 [B + 1] out.
+ *  status           int32 [1] (device) or NULL: FD_DEVSTAT_BAD_PAGE for a
+ *                   pool index >= R or a page past column C, and
+ *                   FD_DEVSTAT_SEQLEN_OVERFLOW for more than W pages, ORed in.
+ *  stream           stream to enqueue on.
+ *
+ * Reads no device memory on the host, never synchronises or allocates: the
+ * call can be captured in a CUDA graph together with fd_decode_paged, whose
+ * page_table and cache_seqlens it fills. Sums must fit in int32.
+ */
+FD_API fd_status fd_graph_metadata(const fd_tensor *req_to_token, const fd_tensor *req_pool_indices,
+                                   const fd_tensor *seq_lens, int page_size, int q_mode, const fd_tensor *q_in,
+                                   int q_stride, fd_tensor *page_table, fd_tensor *cache_seqlens,
+                                   fd_tensor *cu_seqlens_k, fd_tensor *cu_seqlens_q, fd_tensor *status,
+                                   fd_stream_t stream);
 
 /* fd_set_max_seqlen_hint - host-known upper bound of cache_seqlens for the
  * next calls with num_splits = 0; picks the KV-length bucket of the tuning

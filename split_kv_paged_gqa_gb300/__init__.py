@@ -16,13 +16,14 @@ from typing import Optional, Sequence, Tuple
 __all__ = [
     "FdError", "load_library", "fd_plan_create", "fd_plan_destroy", "fd_set_plan", "fd_get_plan",
     "fd_decode_paged", "fd_decode_paged_static", "fd_plan_set_split_policy", "fd_set_max_seqlen_hint",
-    "fd_set_mean_seqlen_hint", "fd_autotune", "fd_query_splits",
+    "fd_set_mean_seqlen_hint", "fd_graph_metadata", "fd_autotune", "fd_query_splits",
     "fd_autotune_set_timer", "fd_autotune_set_cache_dir", "fd_autotune_stats",
     "fd_read_device_status", "fd_plan_workspace_bytes", "fd_profile_begin", "fd_profile_end",
     "fd_status_string", "fd_last_error",
     "FD_OK", "FD_ERR_INVALID_ARG", "FD_ERR_UNSUPPORTED", "FD_ERR_WORKSPACE", "FD_ERR_CAPTURING",
     "FD_ERR_CUDA", "FD_ERR_DEVICE_STATUS", "FD_ERR_TIMEOUT", "FD_ERR_NO_PLAN", "FD_ERR_IO",
-    "FD_BF16", "FD_FP32", "FD_INT8", "FD_INT4X2", "FD_INT32",
+    "FD_BF16", "FD_FP32", "FD_INT8", "FD_INT4X2", "FD_INT32", "FD_INT64",
+    "FD_QMODE_PRESET", "FD_QMODE_CUMSUM", "FD_QMODE_STRIDED",
     "FD_DEVSTAT_BAD_PAGE", "FD_DEVSTAT_SEQLEN_OVERFLOW", "FD_DEVSTAT_WAIT_TIMEOUT",
     "FD_SPLIT_BALANCED", "FD_SPLIT_EQUAL",
 ]
@@ -31,7 +32,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfd.so")
 
 (FD_OK, FD_ERR_INVALID_ARG, FD_ERR_UNSUPPORTED, FD_ERR_WORKSPACE, FD_ERR_CAPTURING, FD_ERR_CUDA,
  FD_ERR_DEVICE_STATUS, FD_ERR_TIMEOUT, FD_ERR_NO_PLAN, FD_ERR_IO) = range(10)
-FD_BF16, FD_FP32, FD_INT8, FD_INT4X2, FD_INT32 = range(5)
+FD_BF16, FD_FP32, FD_INT8, FD_INT4X2, FD_INT32, FD_INT64 = range(6)
+FD_QMODE_PRESET, FD_QMODE_CUMSUM, FD_QMODE_STRIDED = range(3)
 FD_DEVSTAT_BAD_PAGE, FD_DEVSTAT_SEQLEN_OVERFLOW, FD_DEVSTAT_WAIT_TIMEOUT = 1, 2, 4
 FD_SPLIT_BALANCED, FD_SPLIT_EQUAL = 0, 1
 
@@ -81,6 +83,7 @@ def load_library(path: Optional[str] = None):
         "fd_plan_set_split_policy": (I, [P, I]),
         "fd_set_max_seqlen_hint": (I, [P, I]),
         "fd_set_mean_seqlen_hint": (I, [P, I]),
+        "fd_graph_metadata": (I, [T, T, T, I, I, T, I, T, T, T, T, T, P]),
         "fd_autotune": (I, [P, ctypes.POINTER(I), I, I, I, P]),
         "fd_query_splits": (I, [P, I, I, ctypes.POINTER(I)]),
         "fd_autotune_set_timer": (I, [P, TIMER_FN, P]),
@@ -123,7 +126,7 @@ def fd_last_error() -> str:
 def _dtype_code(t) -> int:
     import torch
     m = {torch.bfloat16: FD_BF16, torch.float32: FD_FP32, torch.int8: FD_INT8, torch.uint8: FD_INT4X2,
-         torch.int32: FD_INT32}
+         torch.int32: FD_INT32, torch.int64: FD_INT64}
     return m.get(t.dtype, -1)      # the library rejects unknown codes
 
 
@@ -223,6 +226,20 @@ def fd_set_max_seqlen_hint(plan: int, max_seqlen: int) -> None:
 
 def fd_set_mean_seqlen_hint(plan: int, mean_seqlen: int) -> None:
     _check(load_library().fd_set_mean_seqlen_hint(plan, int(mean_seqlen)))
+
+
+def fd_graph_metadata(req_to_token, req_pool_indices, seq_lens, page_size: int, q_mode, q_in, q_stride: int,
+                      page_table, cache_seqlens, cu_seqlens_k, cu_seqlens_q, status=None, stream=None) -> None:
+    """Enqueue the one-launch rebuild of a decode batch's metadata (page_table,
+    cache_seqlens, cu_seqlens_k, cu_seqlens_q) from a request-to-token pool.
+    q_mode: FD_QMODE_* or "preset" / "cumsum" / "strided"."""
+    if isinstance(q_mode, str):
+        q_mode = {"preset": FD_QMODE_PRESET, "cumsum": FD_QMODE_CUMSUM, "strided": FD_QMODE_STRIDED}[q_mode]
+    d = [make_descriptor(t) for t in (req_to_token, req_pool_indices, seq_lens, q_in, page_table, cache_seqlens,
+                                      cu_seqlens_k, cu_seqlens_q, status)]
+    _check(load_library().fd_graph_metadata(_ref(d[0]), _ref(d[1]), _ref(d[2]), page_size, int(q_mode), _ref(d[3]),
+                                            q_stride, _ref(d[4]), _ref(d[5]), _ref(d[6]), _ref(d[7]), _ref(d[8]),
+                                            _stream_handle(stream)))
 
 
 def fd_autotune(plan: int, batch_sizes: Sequence[int], min_bucket: int = 0, max_bucket: int = 0,

@@ -60,6 +60,7 @@ int elem_bytes(int dtype) {
     case FD_INT8: return 1;
     case FD_INT4X2: return 1;
     case FD_INT32: return 4;
+    case FD_INT64: return 8;
   }
   return 0;
 }
@@ -554,6 +555,79 @@ extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cach
     if (e != cudaSuccess) return fail(FD_ERR_CUDA, "stage-2 launch failed: %s (%d)", cudaGetErrorString(e), (int)e);
   }
   if (pl->profiling) FD_CUDA_TRY(cudaEventRecordWithFlags(ev[2], st, rec_flags));
+  return FD_OK;
+}
+
+extern "C" fd_status fd_graph_metadata(const fd_tensor *req_to_token, const fd_tensor *req_pool_indices,
+                                       const fd_tensor *seq_lens, int page_size, int q_mode, const fd_tensor *q_in,
+                                       int q_stride, fd_tensor *page_table, fd_tensor *cache_seqlens,
+                                       fd_tensor *cu_seqlens_k, fd_tensor *cu_seqlens_q, fd_tensor *status,
+                                       fd_stream_t stream) {
+  FD_TRY(check_tensor(req_to_token, "req_to_token", 2, false));
+  if (req_to_token->dtype != FD_INT32) return fail(FD_ERR_INVALID_ARG, "req_to_token must be int32");
+  FD_TRY(check_tensor(req_pool_indices, "req_pool_indices", 1, false));
+  if (req_pool_indices->dtype != FD_INT32 && req_pool_indices->dtype != FD_INT64)
+    return fail(FD_ERR_INVALID_ARG, "req_pool_indices must be int32 or int64");
+  const int64_t B = req_pool_indices->shape[0];
+  if (B > 65535) return fail(FD_ERR_UNSUPPORTED, "batch %lld > 65535", (long long)B);
+  FD_TRY(check_tensor(seq_lens, "seq_lens", 1, false));
+  if (seq_lens->dtype != FD_INT32 || seq_lens->shape[0] != B)
+    return fail(FD_ERR_INVALID_ARG, "seq_lens must be int32 [B=%lld]", (long long)B);
+  if (page_size < 1) return fail(FD_ERR_INVALID_ARG, "page_size %d < 1", page_size);
+  if (q_mode != FD_QMODE_PRESET && q_mode != FD_QMODE_CUMSUM && q_mode != FD_QMODE_STRIDED)
+    return fail(FD_ERR_INVALID_ARG, "q_mode %d unknown", q_mode);
+  if (q_mode != FD_QMODE_STRIDED) {
+    FD_TRY(check_tensor(q_in, "q_in", 1, false));
+    const int64_t want = q_mode == FD_QMODE_PRESET ? B + 1 : B;
+    if (q_in->dtype != FD_INT32 || q_in->shape[0] != want)
+      return fail(FD_ERR_INVALID_ARG, "q_in must be int32 [%lld]", (long long)want);
+  } else if (q_stride < 0) {
+    return fail(FD_ERR_INVALID_ARG, "q_stride %d < 0", q_stride);
+  }
+  FD_TRY(check_tensor(page_table, "page_table", 2));
+  if (page_table->dtype != FD_INT32 || page_table->shape[0] != B || page_table->shape[1] < 1)
+    return fail(FD_ERR_INVALID_ARG, "page_table must be int32 [B=%lld, W>=1]", (long long)B);
+  FD_TRY(check_tensor(cache_seqlens, "cache_seqlens", 1, false));
+  if (cache_seqlens->dtype != FD_INT32 || cache_seqlens->shape[0] != B)
+    return fail(FD_ERR_INVALID_ARG, "cache_seqlens must be int32 [B]");
+  for (int i = 0; i < 2; ++i) {
+    const fd_tensor *c = i ? cu_seqlens_q : cu_seqlens_k;
+    const char *nm = i ? "cu_seqlens_q" : "cu_seqlens_k";
+    FD_TRY(check_tensor(c, nm, 1));
+    if (c->dtype != FD_INT32 || c->shape[0] != B + 1) return fail(FD_ERR_INVALID_ARG, "%s must be int32 [B + 1]", nm);
+  }
+  if (status && status->data) {
+    FD_TRY(check_tensor(status, "status", 1));
+    if (status->dtype != FD_INT32 || status->shape[0] < 1) return fail(FD_ERR_INVALID_ARG, "status must be int32 [1]");
+  }
+  fd::MetaParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.req_to_token = static_cast<const int *>(req_to_token->data);
+  p.rt_sr = req_to_token->stride[0];
+  p.rt_sc = req_to_token->stride[1];
+  p.pool_rows = req_to_token->shape[0];
+  p.pool_cols = req_to_token->shape[1];
+  p.pool_idx = req_pool_indices->data;
+  p.idx64 = req_pool_indices->dtype == FD_INT64;
+  p.idx_s = req_pool_indices->stride[0];
+  p.seq_lens = static_cast<const int *>(seq_lens->data);
+  p.sl_s = seq_lens->stride[0];
+  p.B = static_cast<int>(B);
+  p.P = page_size;
+  p.W = static_cast<int>(std::min<int64_t>(page_table->shape[1], 0x7fffffff));
+  p.q_mode = q_mode;
+  p.q_in = q_mode != FD_QMODE_STRIDED ? static_cast<const int *>(q_in->data) : nullptr;
+  p.q_s = q_mode != FD_QMODE_STRIDED ? q_in->stride[0] : 0;
+  p.q_stride = q_stride;
+  p.page_table = static_cast<int *>(page_table->data);
+  p.pt_sb = page_table->stride[0];
+  p.cache_seqlens = static_cast<int *>(cache_seqlens->data);
+  if (cache_seqlens->stride[0] != 1 && B > 1) return fail(FD_ERR_UNSUPPORTED, "cache_seqlens must be contiguous");
+  p.cu_k = static_cast<int *>(cu_seqlens_k->data);
+  p.cu_q = static_cast<int *>(cu_seqlens_q->data);
+  p.status = (status && status->data) ? static_cast<unsigned *>(status->data) : nullptr;
+  cudaError_t e = fd::launch_graph_metadata(p, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FD_ERR_CUDA, "graph-metadata launch failed: %s (%d)", cudaGetErrorString(e), (int)e);
   return FD_OK;
 }
 

@@ -107,6 +107,30 @@ struct Stage2Params {
   int64_t l_sb, l_st, l_sh;
 };
 
+// Decode metadata of a batch from a request-to-token pool (graph_metadata.cu).
+struct MetaParams {
+  const int *req_to_token;  // [pool_rows, pool_cols]
+  int64_t rt_sr, rt_sc;     // element strides
+  int64_t pool_rows, pool_cols;
+  const void *pool_idx;     // [B] int32 or int64
+  int idx64;
+  int64_t idx_s;
+  const int *seq_lens;      // [B]
+  int64_t sl_s;
+  int B, P, W;              // batch, page size, page-table width
+  int q_mode;               // an fd_q_mode
+  const int *q_in;          // preset: [B + 1] cu_seqlens_q; cumsum: [B] query tokens; strided: unused
+  int64_t q_s;
+  int q_stride;
+  int *page_table;          // [B, W]
+  int64_t pt_sb;
+  int *cache_seqlens;       // [B]
+  int *cu_k, *cu_q;         // [B + 1]
+  unsigned *status;         // or null
+};
+
+cudaError_t launch_graph_metadata(const MetaParams &p, cudaStream_t stream);
+
 // Slots per TMA box of the stage-1 kernel: a box holds min(page_size, this)
 // rows of one page and head.
 int stage1_block_n(int kind, int head_dim);

@@ -370,3 +370,43 @@ def oracle_inputs(w: Workload, requests: Optional[Sequence[int]] = None) -> dict
         page_table=pt.astype(np.int32), cache_seqlens=L[req].astype(np.int32),
         q_per_req=w.shape.q_per_req, kv_dtype=w.shape.kv_dtype,
         softmax_scale=w.softmax_scale)
+
+
+def make_token_pool(seed: int, lengths: Sequence[int], page_size: int, max_ctx: Optional[int] = None,
+                    extra_rows: int = 0, unallocated_frac: float = 0.0) -> Tuple[np.ndarray, np.ndarray]:
+    """A serving engine's request-to-token pool, seeded: int32 [R, C] KV slots.
+
+    Pool row r (one per entry of ``lengths``, plus ``extra_rows`` empty rows)
+    holds, for token positions 0 .. ceil(len_r / P) * P - 1, the slots of the
+    pages an allocator handed it: pages are a random permutation of the whole
+    page pool, consecutive per request, and the slot of position c is
+    page * P + c % P. Positions past the request's pages hold -1. With
+    ``unallocated_frac`` that share of the pages is left without slots (-1 on
+    all its positions). Returns (req_to_token, page_of_row_pages) where the
+    second is the list of page ids per row (for checks that need no slots).
+    """
+    rng = np.random.default_rng(seed)
+    L = np.asarray(lengths, dtype=np.int64)
+    P = int(page_size)
+    n_pages = -(-L // P)
+    total = int(n_pages.sum())
+    C = int(max_ctx or max(int(n_pages.max(initial=0)) * P, 1))
+    R = len(L) + extra_rows
+    perm = rng.permutation(max(total, 1))
+    pool = np.full((R, C), -1, dtype=np.int32)
+    pages = []
+    k = 0
+    for r in range(len(L)):
+        row_pages = perm[k:k + n_pages[r]]
+        k += int(n_pages[r])
+        pages.append(row_pages.copy())
+        n = min(int(n_pages[r]) * P, C)
+        if n == 0:
+            continue
+        pos = np.arange(n)
+        slots = row_pages[pos // P] * P + pos % P
+        if unallocated_frac > 0:
+            gone = rng.random(len(row_pages)) < unallocated_frac
+            slots = np.where(gone[pos // P], -1, slots)
+        pool[r, :n] = slots.astype(np.int32)
+    return pool, pages
