@@ -323,7 +323,8 @@ FD_API fd_status fd_set_mean_seqlen_hint(fd_plan *plan, int mean_seqlen);
  * long, and (batches of 2 or more) with lengths spread evenly over
  * [K/8, 15K/8] (mean K), the table that calls whose hints show a spread use
  * (see fd_set_mean_seqlen_hint). Refuses with FD_ERR_CAPTURING while
- * the stream is capturing. FD_FORCE_AUTOTUNE=1 ignores cached entries once.
+ * the stream is capturing. Keys already in the table (tuned earlier or loaded
+ * from the cache) are not searched again; see fd_autotune_clear.
  * Allocates temporary device buffers and a private stream (freed before
  * return); the timing runs on that stream after the work of `stream`.
  */
@@ -343,6 +344,57 @@ FD_API fd_status fd_query_splits(fd_plan *plan, int batch, int max_seqlen, int *
  * exercised on a host-only plan. */
 typedef double (*fd_timer_fn)(void *user, int batch, int bucket, int num_splits);
 FD_API fd_status fd_autotune_set_timer(fd_plan *plan, fd_timer_fn fn, void *user);
+
+/*
+ * Warmup phases ("feat(autotune): separate general and decode attention
+ * warmup", section "Changes"): tuning is split into a GENERAL and a
+ * DECODE_ATTENTION warmup phase, entered through a nestable scope that
+ * restores the previous phase. Only decode-attention kernels search inside
+ * the decode-attention phase; nothing searches outside warmup (live
+ * requests). In this library: an fd_decode_paged call with num_splits = 0,
+ * made inside FD_PHASE_DECODE_ATTENTION on a stream that is not capturing,
+ * first tunes its batch at the representative KV length
+ * (FD_AUTOTUNE_SEQ_LEN, default 32768) if the plan's table has no entry for
+ * it, then runs with the tuned value; the same call in any other phase, or
+ * under capture, only looks the table up. A serving engine runs one such
+ * decode before capturing each decode graph, and the capture then uses the
+ * tuned value. fd_autotune itself (explicit start-up tuning) runs in any
+ * phase. The phase is per host thread.
+ */
+typedef enum fd_warmup_phase {
+  FD_PHASE_NONE = 0,              /* live requests: no tuning */
+  FD_PHASE_GENERAL = 1,           /* general (prefill) kernels may tune; decode attention does not */
+  FD_PHASE_DECODE_ATTENTION = 2   /* decode attention tunes on its calls */
+} fd_warmup_phase;
+
+/* fd_warmup_enter - make phase current on this thread; *previous (may be
+ * NULL) receives the phase to restore. fd_warmup_exit - restore it. Scopes
+ * nest: exit with the value the matching enter returned. */
+FD_API fd_status fd_warmup_enter(int phase, int *previous);
+FD_API fd_status fd_warmup_exit(int previous);
+/* fd_warmup_current - the calling thread's current phase. */
+FD_API int fd_warmup_current(void);
+
+/* Hook that writes representative tuning inputs (the page's
+ * rebuild_input_func): called by fd_autotune once per (batch, bucket,
+ * spread) key, outside capture, before that key is timed, with the tuner's
+ * own buffers: q [batch, Tq, Hq, D], k_cache / v_cache [N, P, Hkv, *] and
+ * kv_scales (NULL for bf16). It may overwrite their contents (for example
+ * with values drawn like the engine's); the page placement and the lengths
+ * stay the tuner's (bucket length, or spread over [K/8, 15K/8] when mixed is
+ * 1). A non-FD_OK return aborts the tuning with that status. */
+typedef fd_status (*fd_tune_inputs_fn)(void *user, int batch, int bucket, int mixed, fd_tensor *q,
+                                       fd_tensor *k_cache, fd_tensor *v_cache, fd_tensor *kv_scales,
+                                       fd_stream_t stream);
+FD_API fd_status fd_autotune_set_input_hook(fd_plan *plan, fd_tune_inputs_fn fn, void *user);
+
+/* fd_autotune_clear - forget every tuned entry of the plan (and, when
+ * remove_file is nonzero, delete its persisted table), so the next tuning
+ * searches afresh. Decode attention treats FD_FORCE_AUTOTUNE as adaptive
+ * (same page, section "Changes"): cached entries are reused, so that the many
+ * layers sharing a geometry never retune; a fresh search needs this call or
+ * the cache file removed. */
+FD_API fd_status fd_autotune_clear(fd_plan *plan, int remove_file);
 
 /* fd_autotune_set_cache_dir - directory of the persisted tuning table (NULL
  * or "" disables persistence). Default: $FD_AUTOTUNE_CACHE_DIR if set. */

@@ -16,7 +16,8 @@ from typing import Optional, Sequence, Tuple
 __all__ = [
     "FdError", "load_library", "fd_plan_create", "fd_plan_destroy", "fd_set_plan", "fd_get_plan",
     "fd_decode_paged", "fd_decode_paged_static", "fd_plan_set_split_policy", "fd_set_max_seqlen_hint",
-    "fd_set_mean_seqlen_hint", "fd_graph_metadata", "fd_autotune", "fd_query_splits",
+    "fd_set_mean_seqlen_hint", "fd_graph_metadata", "fd_warmup_enter", "fd_warmup_exit", "fd_warmup_current",
+    "warmup", "fd_autotune_set_input_hook", "fd_autotune_clear", "fd_autotune", "fd_query_splits",
     "fd_autotune_set_timer", "fd_autotune_set_cache_dir", "fd_autotune_stats",
     "fd_read_device_status", "fd_plan_workspace_bytes", "fd_profile_begin", "fd_profile_end",
     "fd_status_string", "fd_last_error",
@@ -24,6 +25,7 @@ __all__ = [
     "FD_ERR_CUDA", "FD_ERR_DEVICE_STATUS", "FD_ERR_TIMEOUT", "FD_ERR_NO_PLAN", "FD_ERR_IO",
     "FD_BF16", "FD_FP32", "FD_INT8", "FD_INT4X2", "FD_INT32", "FD_INT64",
     "FD_QMODE_PRESET", "FD_QMODE_CUMSUM", "FD_QMODE_STRIDED",
+    "FD_PHASE_NONE", "FD_PHASE_GENERAL", "FD_PHASE_DECODE_ATTENTION",
     "FD_DEVSTAT_BAD_PAGE", "FD_DEVSTAT_SEQLEN_OVERFLOW", "FD_DEVSTAT_WAIT_TIMEOUT",
     "FD_SPLIT_BALANCED", "FD_SPLIT_EQUAL",
 ]
@@ -34,6 +36,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfd.so")
  FD_ERR_DEVICE_STATUS, FD_ERR_TIMEOUT, FD_ERR_NO_PLAN, FD_ERR_IO) = range(10)
 FD_BF16, FD_FP32, FD_INT8, FD_INT4X2, FD_INT32, FD_INT64 = range(6)
 FD_QMODE_PRESET, FD_QMODE_CUMSUM, FD_QMODE_STRIDED = range(3)
+FD_PHASE_NONE, FD_PHASE_GENERAL, FD_PHASE_DECODE_ATTENTION = range(3)
 FD_DEVSTAT_BAD_PAGE, FD_DEVSTAT_SEQLEN_OVERFLOW, FD_DEVSTAT_WAIT_TIMEOUT = 1, 2, 4
 FD_SPLIT_BALANCED, FD_SPLIT_EQUAL = 0, 1
 
@@ -46,6 +49,9 @@ class FdTensor(ctypes.Structure):
 
 
 TIMER_FN = ctypes.CFUNCTYPE(ctypes.c_double, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int)
+INPUTS_FN = ctypes.CFUNCTYPE(ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                             ctypes.POINTER(FdTensor), ctypes.POINTER(FdTensor), ctypes.POINTER(FdTensor),
+                             ctypes.POINTER(FdTensor), ctypes.c_void_p)
 
 
 class FdError(RuntimeError):
@@ -84,6 +90,11 @@ def load_library(path: Optional[str] = None):
         "fd_set_max_seqlen_hint": (I, [P, I]),
         "fd_set_mean_seqlen_hint": (I, [P, I]),
         "fd_graph_metadata": (I, [T, T, T, I, I, T, I, T, T, T, T, T, P]),
+        "fd_warmup_enter": (I, [I, ctypes.POINTER(I)]),
+        "fd_warmup_exit": (I, [I]),
+        "fd_warmup_current": (I, []),
+        "fd_autotune_set_input_hook": (I, [P, INPUTS_FN, P]),
+        "fd_autotune_clear": (I, [P, I]),
         "fd_autotune": (I, [P, ctypes.POINTER(I), I, I, I, P]),
         "fd_query_splits": (I, [P, I, I, ctypes.POINTER(I)]),
         "fd_autotune_set_timer": (I, [P, TIMER_FN, P]),
@@ -240,6 +251,65 @@ def fd_graph_metadata(req_to_token, req_pool_indices, seq_lens, page_size: int, 
     _check(load_library().fd_graph_metadata(_ref(d[0]), _ref(d[1]), _ref(d[2]), page_size, int(q_mode), _ref(d[3]),
                                             q_stride, _ref(d[4]), _ref(d[5]), _ref(d[6]), _ref(d[7]), _ref(d[8]),
                                             _stream_handle(stream)))
+
+
+def fd_warmup_enter(phase: int) -> int:
+    """Enter a warmup phase on this thread; returns the phase to restore."""
+    prev = ctypes.c_int()
+    _check(load_library().fd_warmup_enter(int(phase), ctypes.byref(prev)))
+    return prev.value
+
+
+def fd_warmup_exit(previous: int) -> None:
+    _check(load_library().fd_warmup_exit(int(previous)))
+
+
+def fd_warmup_current() -> int:
+    return load_library().fd_warmup_current()
+
+
+class warmup:
+    """Nestable warmup scope: ``with warmup(FD_PHASE_DECODE_ATTENTION): ...``
+    restores the previous phase on exit."""
+
+    def __init__(self, phase: int):
+        self.phase = phase
+        self.prev = None
+
+    def __enter__(self):
+        self.prev = fd_warmup_enter(self.phase)
+        return self
+
+    def __exit__(self, *exc):
+        fd_warmup_exit(self.prev)
+        return False
+
+
+_input_hooks = {}
+
+
+def fd_autotune_set_input_hook(plan: int, fn) -> None:
+    """Install ``fn(batch, bucket, mixed, q, k_cache, v_cache, kv_scales)``
+    (fd_tensor descriptors of the tuner's device buffers; kv_scales is None
+    for bf16) that writes representative tuning inputs; None removes it."""
+    if fn is None:
+        _input_hooks.pop(plan, None)
+        _check(load_library().fd_autotune_set_input_hook(plan, INPUTS_FN(), None))
+        return
+
+    def hook(user, b, k, mixed, q, kc, vc, sc, stream):
+        try:
+            fn(b, k, mixed, q.contents, kc.contents, vc.contents, sc.contents if sc else None)
+            return FD_OK
+        except Exception:
+            return FD_ERR_INVALID_ARG
+    cb = INPUTS_FN(hook)
+    _input_hooks[plan] = cb
+    _check(load_library().fd_autotune_set_input_hook(plan, cb, None))
+
+
+def fd_autotune_clear(plan: int, remove_file: bool = False) -> None:
+    _check(load_library().fd_autotune_clear(plan, 1 if remove_file else 0))
 
 
 def fd_autotune(plan: int, batch_sizes: Sequence[int], min_bucket: int = 0, max_bucket: int = 0,

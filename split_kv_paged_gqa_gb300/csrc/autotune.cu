@@ -7,8 +7,11 @@
 // section "Covered decode kernels"); KV-length run keys are bucketed while a
 // call still uses its real lengths; chosen configurations are persisted per
 // kernel and reused, and deleting the cache forces a new search (section
-// "Changes": FORCE_AUTOTUNE as adaptive tuning); cached nearest-key matches are
-// invalidated when a new configuration is saved.
+// "Changes": decode attention treats FORCE_AUTOTUNE as adaptive tuning, so
+// entries already tuned are never searched again); cached nearest-key matches
+// are invalidated when a new configuration is saved. The warmup phases of the
+// same section (GENERAL, DECODE_ATTENTION; a nestable scope that restores the
+// previous phase) decide whether a decode call may tune (autotune_on_call).
 //
 // Table key: (batch, bucket) with bucket a power of two of the KV length,
 // stored as -bucket for the mixed-length table (see tuning_lengths).
@@ -27,6 +30,7 @@
 #include <sys/stat.h>
 
 #include <algorithm>
+#include <cerrno>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -42,6 +46,8 @@
 using fd::fail;
 
 namespace {
+
+thread_local int g_phase = FD_PHASE_NONE;  // the calling thread's warmup phase
 
 int next_pow2(int v) {
   int r = 1;
@@ -391,6 +397,24 @@ fd_status autotune_save(fd_plan *pl) {
   return FD_OK;
 }
 
+fd_status autotune_on_call(fd_plan *pl, int batch, cudaStream_t stream) {
+  if (g_phase != FD_PHASE_DECODE_ATTENTION) return FD_OK;  // only decode attention tunes, only in its phase
+  if (!pl->timer) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return fail(FD_ERR_CUDA, "cudaStreamIsCapturing failed");
+    if (cs != cudaStreamCaptureStatusNone) return FD_OK;  // never inside capture: look the table up
+  }
+  if (!pl->cache_loaded) autotune_load(pl);
+  int len = 32768;  // the representative KV length
+  if (const char *e = std::getenv("FD_AUTOTUNE_SEQ_LEN")) {
+    const int v = atoi(e);
+    if (v > 0) len = v;
+  }
+  const int bucket = next_pow2(len);
+  if (pl->table.count({batch, bucket})) return FD_OK;
+  return fd_autotune(pl, &batch, 1, bucket, bucket, reinterpret_cast<fd_stream_t>(stream));
+}
+
 int choose_splits(fd_plan *pl, int batch, int max_seqlen) {
   const bool by_mean = pl->split_policy == FD_SPLIT_BALANCED && pl->mean_hint > 0;
   if (pl->table.empty()) return heuristic_splits(pl, batch, by_mean ? pl->mean_hint : max_seqlen);
@@ -444,6 +468,43 @@ fd_status fd_autotune_set_timer(fd_plan *plan, fd_timer_fn fn, void *user) {
   return FD_OK;
 }
 
+fd_status fd_autotune_set_input_hook(fd_plan *plan, fd_tune_inputs_fn fn, void *user) {
+  if (!plan) return fail(FD_ERR_INVALID_ARG, "plan is NULL");
+  plan->input_hook = fn;
+  plan->input_user = user;
+  return FD_OK;
+}
+
+fd_status fd_autotune_clear(fd_plan *plan, int remove_file) {
+  if (!plan) return fail(FD_ERR_INVALID_ARG, "plan is NULL");
+  plan->table.clear();
+  plan->table_time.clear();
+  plan->memo.clear();
+  plan->cache_loaded = true;  // do not reload the file being discarded
+  if (remove_file && !plan->cache_dir.empty()) {
+    if (std::remove(cache_path(plan).c_str()) != 0 && errno != ENOENT)
+      return fail(FD_ERR_IO, "cannot remove %s", cache_path(plan).c_str());
+  }
+  return FD_OK;
+}
+
+fd_status fd_warmup_enter(int phase, int *previous) {
+  if (phase != FD_PHASE_NONE && phase != FD_PHASE_GENERAL && phase != FD_PHASE_DECODE_ATTENTION)
+    return fail(FD_ERR_INVALID_ARG, "warmup phase %d unknown", phase);
+  if (previous) *previous = g_phase;
+  g_phase = phase;
+  return FD_OK;
+}
+
+fd_status fd_warmup_exit(int previous) {
+  if (previous != FD_PHASE_NONE && previous != FD_PHASE_GENERAL && previous != FD_PHASE_DECODE_ATTENTION)
+    return fail(FD_ERR_INVALID_ARG, "warmup phase %d unknown", previous);
+  g_phase = previous;
+  return FD_OK;
+}
+
+int fd_warmup_current(void) { return g_phase; }
+
 fd_status fd_autotune_set_cache_dir(fd_plan *plan, const char *dir) {
   if (!plan) return fail(FD_ERR_INVALID_ARG, "plan is NULL");
   plan->cache_dir = dir ? dir : "";
@@ -488,8 +549,6 @@ fd_status fd_autotune(fd_plan *plan, const int *batch_sizes, int n_batch, int mi
     fd_status s = fd::autotune_load(plan);
     if (s != FD_OK) return s;
   }
-  const char *force_env = std::getenv("FD_FORCE_AUTOTUNE");
-  const bool force = force_env && force_env[0] == '1';
 
   // keys (batch, bucket) for equal lengths and (batch, -bucket) for mixed
   // lengths (batches of two or more requests)
@@ -499,7 +558,7 @@ fd_status fd_autotune(fd_plan *plan, const int *batch_sizes, int n_batch, int mi
       for (int sign : {1, -1}) {
         if (sign < 0 && batch_sizes[i] < 2) continue;
         const std::pair<int, int> key{batch_sizes[i], sign * k};
-        if (!force && plan->table.count(key)) {
+        if (plan->table.count(key)) {
           ++plan->cache_hits;
           continue;
         }
@@ -517,6 +576,19 @@ fd_status fd_autotune(fd_plan *plan, const int *batch_sizes, int n_batch, int mi
   }
   for (auto &key : todo) {
     ++plan->searches;
+    if (!plan->timer && plan->input_hook) {  // representative inputs from the caller
+      const int rowe = plan->kv_dtype == FD_INT4X2 ? plan->d / 2 : plan->d;
+      const int ng = plan->kv_dtype == FD_INT4X2 ? plan->d / 32 : 1;
+      fd_tensor q, k, v, sc;
+      make_desc(q, tb.q, FD_BF16, {key.first, tb.tq, plan->hq, plan->d});
+      make_desc(k, tb.k, plan->kv_dtype, {tb.pool_pages, plan->page, plan->hkv, rowe});
+      make_desc(v, tb.v, plan->kv_dtype, {tb.pool_pages, plan->page, plan->hkv, rowe});
+      make_desc(sc, tb.scales, FD_FP32, {2, tb.pool_pages, plan->page, plan->hkv, ng});
+      fd_status hs = plan->input_hook(plan->input_user, key.first, std::abs(key.second), key.second < 0 ? 1 : 0, &q,
+                                      &k, &v, tb.scales ? &sc : nullptr, reinterpret_cast<fd_stream_t>(st));
+      if (hs != FD_OK) return fail(hs, "autotune: the input hook returned %d", (int)hs);
+      if (cudaStreamSynchronize(st) != cudaSuccess) return fail(FD_ERR_CUDA, "autotune: input hook work failed");
+    }
     std::vector<std::pair<int, double>> timed;
     for (int S : candidate_splits(plan, key.first, std::abs(key.second))) {
       double t = 0.0;

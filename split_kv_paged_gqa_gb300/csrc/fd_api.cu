@@ -422,7 +422,12 @@ extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cach
   // ---- splits
   int S = num_splits;
   if (S < 0 || S > pl->max_splits) return fail(FD_ERR_INVALID_ARG, "num_splits %d not in [0, %d]", S, pl->max_splits);
-  if (S == 0) S = fd::choose_splits(pl, B, pl->seqlen_hint);
+  if (S == 0) {
+    // inside the decode-attention warmup phase (outside capture) the call
+    // first tunes its batch at the representative length if needed
+    FD_TRY(fd::autotune_on_call(pl, B, reinterpret_cast<cudaStream_t>(stream)));
+    S = fd::choose_splits(pl, B, pl->seqlen_hint);
+  }
   if (pl->device < 0) return fail(FD_ERR_WORKSPACE, "host-only plan cannot decode");
   // Balanced splits (more than one request, a workspace with room for at
   // least two partials per output row): s_cap partial rows per output row.

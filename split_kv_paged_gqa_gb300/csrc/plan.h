@@ -43,6 +43,8 @@ struct fd_plan {
   bool cache_loaded = false;
   fd_timer_fn timer = nullptr;
   void *timer_user = nullptr;
+  fd_tune_inputs_fn input_hook = nullptr;  // representative tuning inputs (rebuild hook)
+  void *input_user = nullptr;
   int searches = 0, cache_hits = 0;
 
   // last encoded TMA descriptors of the K and V caches (host-side cache:
@@ -68,6 +70,11 @@ fd_status fail(fd_status s, const char *fmt, ...);
 
 // num_splits for a call with batch B and host-known max length (0 = unknown).
 int choose_splits(fd_plan *plan, int batch, int max_seqlen);
+
+// Warmup-scope tuning of a decode call with num_splits = 0 (autotune.cu):
+// inside the decode-attention warmup phase and outside capture, tunes the
+// call's batch at the representative KV length if the table lacks it.
+fd_status autotune_on_call(fd_plan *plan, int batch, cudaStream_t stream);
 
 // Autotune cache helpers (autotune.cu).
 std::string autotune_key(const fd_plan *plan);

@@ -251,10 +251,10 @@ def test_autotune_buckets_nearest_and_persistence(tmp_path, monkeypatch):
         assert calls2 == [] and fd.fd_autotune_stats(plan2) == (0, 8)
         fd.fd_set_mean_seqlen_hint(plan2, 2000)                      # the mixed table reloads too
         assert fd.fd_query_splits(plan2, 16, 8000) == best(16, -2048)
-        # FD_FORCE_AUTOTUNE re-searches even cached keys
+        # decode attention treats FD_FORCE_AUTOTUNE as adaptive: cached keys are kept
         monkeypatch.setenv("FD_FORCE_AUTOTUNE", "1")
         fd.fd_autotune(plan2, [16], 1024, 1024)
-        assert {1, 2, 4, 8} <= {c[2] for c in calls2} and len(calls2) >= 4
+        assert calls2 == []
     finally:
         fd.fd_plan_destroy(plan2)
 
@@ -369,5 +369,79 @@ def test_tuner_skips_splits_shorter_than_128_keys(tmp_path):
             assert S * 128 <= k or S == 1, (k, S)
         assert {S for k, S in calls if k == 1024} >= {1, 2, 4, 8}
         assert {S for k, S in calls if k == 256} == {1, 2}
+    finally:
+        fd.fd_plan_destroy(plan)
+
+
+# ---------------------------------------------------------------------------
+# warmup phases: decode attention tunes on its calls only in its own phase
+
+
+def test_warmup_scopes_nest_and_restore():
+    assert fd.fd_warmup_current() == fd.FD_PHASE_NONE
+    with fd.warmup(fd.FD_PHASE_DECODE_ATTENTION):
+        assert fd.fd_warmup_current() == fd.FD_PHASE_DECODE_ATTENTION
+        with fd.warmup(fd.FD_PHASE_GENERAL):
+            assert fd.fd_warmup_current() == fd.FD_PHASE_GENERAL
+        assert fd.fd_warmup_current() == fd.FD_PHASE_DECODE_ATTENTION
+    assert fd.fd_warmup_current() == fd.FD_PHASE_NONE
+    with pytest.raises(fd.FdError):
+        fd.fd_warmup_enter(9)
+    assert fd.fd_warmup_current() == fd.FD_PHASE_NONE
+
+
+def test_decode_call_tunes_only_inside_the_decode_attention_phase(tmp_path, monkeypatch):
+    monkeypatch.delenv("FD_AUTOTUNE_SEQ_LEN", raising=False)
+    plan = _host_plan(B=4, S=8)
+    calls = []
+    try:
+        fd.fd_autotune_set_cache_dir(plan, str(tmp_path))
+        fd.fd_autotune_set_timer(plan, lambda b, k, S: calls.append((b, k, S)) or abs(S - 4) + 1.0)
+        fd.fd_set_plan(plan)
+        t = _tensors()                                   # batch 2, valid descriptors
+        _expect(fd.FD_ERR_WORKSPACE, t, S=0)                  # live phase: no tuning
+        with fd.warmup(fd.FD_PHASE_GENERAL):
+            _expect(fd.FD_ERR_WORKSPACE, t, S=0)              # general phase: decode attention does not tune
+        assert calls == []
+        with fd.warmup(fd.FD_PHASE_DECODE_ATTENTION):
+            _expect(fd.FD_ERR_WORKSPACE, t, S=0)              # tunes batch 2 at 32768, then fails on the host plan
+            assert {(b, abs(k)) for b, k, S in calls} == {(2, 32768)}
+            assert {k for b, k, S in calls} == {32768, -32768}     # equal and mixed lengths
+            assert fd.fd_autotune_stats(plan)[0] == 2
+            n = len(calls)
+            _expect(fd.FD_ERR_WORKSPACE, t, S=0)              # tuned already: adaptive, no new search
+            assert len(calls) == n
+        assert fd.fd_query_splits(plan, 2, 32768) == 4
+        monkeypatch.setenv("FD_AUTOTUNE_SEQ_LEN", "5000")
+        with fd.warmup(fd.FD_PHASE_DECODE_ATTENTION):
+            _expect(fd.FD_ERR_WORKSPACE, t, S=0)              # representative length 5000: bucket 8192
+        assert (2, 8192) in {(b, abs(k)) for b, k, S in calls}
+        # an explicit num_splits never tunes
+        calls.clear()
+        with fd.warmup(fd.FD_PHASE_DECODE_ATTENTION):
+            _expect(fd.FD_ERR_WORKSPACE, t, S=2)
+        assert calls == []
+    finally:
+        fd.fd_set_plan(None)
+        fd.fd_plan_destroy(plan)
+
+
+def test_force_is_adaptive_and_clear_searches_afresh(tmp_path, monkeypatch):
+    plan = _host_plan(B=64, S=64)
+    try:
+        fd.fd_autotune_set_cache_dir(plan, str(tmp_path))
+        calls = []
+        fd.fd_autotune_set_timer(plan, lambda b, k, S: calls.append(S) or float(S))
+        fd.fd_autotune(plan, [4], 4096, 4096)
+        first = len(calls)
+        monkeypatch.setenv("FD_FORCE_AUTOTUNE", "1")     # adaptive for decode attention: no re-search
+        fd.fd_autotune(plan, [4], 4096, 4096)
+        assert len(calls) == first
+        files = list(tmp_path.glob("fd_splits_*.json"))
+        assert len(files) == 1
+        fd.fd_autotune_clear(plan, remove_file=True)      # a fresh search
+        assert not files[0].exists()
+        fd.fd_autotune(plan, [4], 4096, 4096)
+        assert len(calls) == 2 * first
     finally:
         fd.fd_plan_destroy(plan)

@@ -456,3 +456,64 @@ def test_autotune_on_device_then_decode(tmp_path):
     finally:
         fd.fd_set_plan(None)
         fd.fd_plan_destroy(plan)
+
+
+# ---------------------------------------------------------------------------
+# warmup phases on the device: a decode call in the decode-attention phase
+# tunes its batch at the representative length, and the graph captured after
+# it uses the tuned value; the rebuild hook sees each tuning key
+
+
+def test_warmup_decode_call_tunes_then_capture_uses_it(tmp_path, monkeypatch):
+    monkeypatch.setenv("FD_AUTOTUNE_SEQ_LEN", "2048")
+    shape = _shape("bf16", 3, 1, 16, 4, 128, 16, (5, 9, 2))    # graph-init style short requests
+    w = wl.make_workload(shape, 91, "cuda", extra_pages=200, capacity_pages=140)
+    plan = fd.fd_plan_create(0, 3, 1, 16, 4, 128, 16, "bf16", 16)
+    seen = []
+    try:
+        fd.fd_autotune_set_cache_dir(plan, str(tmp_path))
+        fd.fd_autotune_set_input_hook(plan, lambda b, k, mixed, q, kc, vc, sc: seen.append(
+            (b, k, mixed, tuple(q.shape[:4]), tuple(kc.shape[1:4]), sc is None)))
+        fd.fd_set_plan(plan)
+        out = torch.empty_like(w.q)
+        lse = torch.empty(w.q.shape[:3], dtype=torch.float32, device="cuda")
+        fd.fd_decode_paged(w.q, w.k_cache, w.v_cache, None, w.page_table, w.cache_seqlens, 1, 0, out, lse)
+        torch.cuda.synchronize()
+        assert fd.fd_autotune_stats(plan)[0] == 0                 # live phase: no tuning
+        with fd.warmup(fd.FD_PHASE_DECODE_ATTENTION):
+            fd.fd_decode_paged(w.q, w.k_cache, w.v_cache, None, w.page_table, w.cache_seqlens, 1, 0, out, lse)
+        torch.cuda.synchronize()
+        assert fd.fd_autotune_stats(plan)[0] == 2                 # (3, 2048): equal and mixed lengths
+        assert sorted(x[:3] for x in seen) == [(3, 2048, 0), (3, 2048, 1)]
+        assert all(x[3] == (3, 1, 16, 128) and x[4] == (16, 4, 128) and x[5] for x in seen)
+        S = fd.fd_query_splits(plan, 3, 9)
+        assert 1 <= S <= 16
+        # capture with num_splits = 0 after warmup; replay with longer requests
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fd.fd_decode_paged(w.q, w.k_cache, w.v_cache, None, w.page_table, w.cache_seqlens, 1, 0, out, lse)
+        rng = np.random.default_rng(8)
+        lens = rng.integers(100, 2000, size=3)
+        pages = rng.permutation(w.k_cache.shape[0])
+        pt = torch.full_like(w.page_table, -1)
+        k = 0
+        for b in range(3):
+            n = -(-int(lens[b]) // 16)
+            pt[b, :n] = torch.from_numpy(pages[k:k + n].astype(np.int32))
+            k += n
+        w.page_table.copy_(pt)
+        w.cache_seqlens.copy_(torch.from_numpy(lens.astype(np.int32)))
+        w.lengths = lens
+        g.replay()
+        torch.cuda.synchronize()
+        ref_out, ref_lse = decode_ref_inputs(wl.oracle_inputs(w))
+        assert_parity(out, lse, ref_out, ref_lse, label="graph after warmup tuning")
+        del g
+        # a hook that fails aborts the tuning with its status
+        fd.fd_autotune_clear(plan)
+        fd.fd_autotune_set_input_hook(plan, lambda *a: 1 / 0)
+        with pytest.raises(fd.FdError):
+            fd.fd_autotune(plan, [3], 1024, 1024)
+    finally:
+        fd.fd_set_plan(None)
+        fd.fd_plan_destroy(plan)
