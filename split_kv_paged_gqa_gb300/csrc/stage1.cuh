@@ -279,11 +279,11 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
   for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) sv[nt][e] = 0.f;
-  float acc8[2][4];  // int8: one accumulator over all chunks
+  float acc8[2][4];  // int8: one accumulator over all chunks, starting at -bias
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) acc8[nt][e] = 0.f;
+    for (int e = 0; e < 4; ++e) acc8[nt][e] = KIND == KV_I8 ? -qc[e >> 1][0] : 0.f;
   const int krow = row0 + ((mi >> 1) << 3) + ri;
 #pragma unroll
   for (int kc = 0; kc < CH; kc += 2) {
@@ -300,11 +300,11 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
                         __byte_perm(x, 0x64646464u, 0x7362));
         }
       } else {
-        float acc[2][4];
+        float acc[2][4];  // this group's products, starting at -bias
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+          for (int e = 0; e < 4; ++e) acc[nt][e] = -qc[e >> 1][ch];
           const uint32_t x = r[nt * 2 + hh] ^ 0x88888888u;  // nibble k = channel 32ch + 8c + k
           const uint32_t y = x >> 8;
           mma_f16_16816(acc[nt], qa[2 * ch], (x & 0x000F000Fu) | 0x64006400u,
@@ -317,7 +317,7 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int key = nt * 8 + 2 * c + (e & 1);
-            sv[nt][e] = fmaf(acc[nt][e] - qc[e >> 1][ch], ksc[(row0 + key) * NG + ch], sv[nt][e]);
+            sv[nt][e] = fmaf(acc[nt][e], ksc[(row0 + key) * NG + ch], sv[nt][e]);
           }
       }
     }
@@ -328,20 +328,29 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int key = nt * 8 + 2 * c + (e & 1);
-        sv[nt][e] = (acc8[nt][e] - qc[e >> 1][0]) * ksc[row0 + key];
+        sv[nt][e] = acc8[nt][e] * ksc[row0 + key];
       }
   }
 
-  // ---- row scale, mask by selection
+  // ---- row scale, mask by selection (a block whose 16 keys every row of the
+  // warp sees, which is every block but a split's last, needs no selection)
+  const bool full = __all_sync(0xffffffffu, tok_row0 + 16 <= min(lim0, lim1));
   float s[2][4];
+  if (full) {
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int key = nt * 8 + 2 * c + (e & 1);
-      const int hr = e >> 1;
-      const int lim = hr ? lim1 : lim0;
-      s[nt][e] = (tok_row0 + key < lim) ? sv[nt][e] * rs[hr] : -INFINITY;
+      for (int e = 0; e < 4; ++e) s[nt][e] = sv[nt][e] * rs[e >> 1];
+  } else {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = nt * 8 + 2 * c + (e & 1);
+        const int hr = e >> 1;
+        const int lim = hr ? lim1 : lim0;
+        s[nt][e] = (tok_row0 + key < lim) ? sv[nt][e] * rs[hr] : -INFINITY;
+      }
     }
   }
   float p[2][4], al[2];
@@ -384,7 +393,7 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
   const int vrows[4] = {kA, kA + 1, kB, kB + 1};
   bool valid[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) valid[i] = tok_row0 + (vrows[i] - row0) < c1;
+  for (int i = 0; i < 4; ++i) valid[i] = full || tok_row0 + (vrows[i] - row0) < c1;
   if constexpr (KIND == KV_I8) {
     static_assert(NT % 4 == 0, "int8 V words");
     constexpr int NW = NT / 4;  // 32-bit words per key
