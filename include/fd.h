@@ -311,7 +311,8 @@ FD_API fd_status fd_set_mean_seqlen_hint(fd_plan *plan, int mean_seqlen);
  *                         max_bucket (0, 0 = 1024 .. FD_AUTOTUNE_SEQ_LEN or 32768).
  *  stream                 stream for the timing launches.
  *
- * Candidates are num_splits in {1, 2, 4, ..., max_splits}, plus the counts
+ * Candidates are num_splits in {1, 2, 3, 4, 6, 8, 12, 16, 32, 64} (up to
+ * max_splits), plus the counts
  * that fill one or two waves of one CTA per SM, none cutting the bucket into
  * splits of fewer than 128 keys. For each key not already in
  * the table (loaded from the cache directory), synthetic inputs of the bucket

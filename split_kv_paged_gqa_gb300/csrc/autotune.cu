@@ -75,8 +75,8 @@ int heuristic_splits(const fd_plan *pl, int batch, int max_seqlen) {
   return std::min(s, pl->max_splits);
 }
 
-// Candidates: powers of two up to max_splits, plus the split counts that
-// fill one or two waves of one CTA per SM for this batch (e.g. 19 for one
+// Candidates: powers of two up to max_splits, 3, 6 and 12, plus the split
+// counts that fill one or two waves of one CTA per SM for this batch (e.g. 19 for one
 // request of 8 KV heads on 152 SMs), where a power of two leaves SMs idle;
 // none that cuts the bucket length into splits of fewer than 128 keys (such
 // calls take microseconds, and their timing is noise).
@@ -84,6 +84,7 @@ std::vector<int> candidate_splits(const fd_plan *pl, int batch, int bucket) {
   const int cap = std::max(1, std::min(pl->max_splits, bucket / 128));
   std::vector<int> c;
   for (int S = 1; S <= cap; S <<= 1) c.push_back(S);
+  for (int S = 3; S <= cap && S <= 12; S <<= 1) c.push_back(S);  // 3, 6, 12: between the powers of two
   const int G = pl->hq / pl->hkv;
   const long base = static_cast<long>(batch) * pl->hkv * ((G * pl->max_q + 15) / 16);
   for (int k = 1; k <= 2; ++k) {
