@@ -119,6 +119,17 @@ __device__ __forceinline__ uint32_t u8pair_to_f16_biased(uint32_t t) {
   return (t & 0x00FF00FFu) | 0x64006400u;
 }
 
+// int4 codes are stored as two's-complement nibbles n = code & 15, and
+// n ^ 8 = code + 8 = u in [0, 15]. From the nibbles at bits 0-3 and 16-19:
+// f16x2 (1024 + u, 1024 + u'); from those at bits 4-7 and 20-23:
+// f16x2 (1024 + 16u, 1024 + 16u'). Mask, bias and exponent in one LOP3.
+__device__ __forceinline__ uint32_t nib_lo_f16_biased(uint32_t t) {
+  return (t & 0x000F000Fu) ^ 0x64086408u;
+}
+__device__ __forceinline__ uint32_t nib_hi_f16_biased(uint32_t t) {
+  return (t & 0x00F000F0u) ^ 0x64806480u;
+}
+
 // ----------------------------------------------------------------------------
 // One 16-key block of one warp, bf16 cache: scores, online softmax, PV.
 //
@@ -305,12 +316,12 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
         for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[nt][e] = -qc[e >> 1][ch];
-          const uint32_t x = r[nt * 2 + hh] ^ 0x88888888u;  // nibble k = channel 32ch + 8c + k
+          // raw nibble k (= code & 15) is channel 32ch + 8c + k; masking it
+          // and XOR-ing in 8 and the exponent of 1024 is one LOP3 per pair
+          const uint32_t x = r[nt * 2 + hh];
           const uint32_t y = x >> 8;
-          mma_f16_16816(acc[nt], qa[2 * ch], (x & 0x000F000Fu) | 0x64006400u,
-                        (y & 0x000F000Fu) | 0x64006400u);
-          mma_f16_16816(acc[nt], qa[2 * ch + 1], (x & 0x00F000F0u) | 0x64006400u,
-                        (y & 0x00F000F0u) | 0x64006400u);
+          mma_f16_16816(acc[nt], qa[2 * ch], nib_lo_f16_biased(x), nib_lo_f16_biased(y));
+          mma_f16_16816(acc[nt], qa[2 * ch + 1], nib_hi_f16_biased(x), nib_hi_f16_biased(y));
         }
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
@@ -340,7 +351,11 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[nt][e] = sv[nt][e] * rs[e >> 1];
+      for (int hr = 0; hr < 2; ++hr) {
+        const float2 r2 = __fmul2_rn(make_float2(sv[nt][2 * hr], sv[nt][2 * hr + 1]), make_float2(rs[hr], rs[hr]));
+        s[nt][2 * hr] = r2.x;
+        s[nt][2 * hr + 1] = r2.y;
+      }
   } else {
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
@@ -444,8 +459,6 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
       } else {
         w[i][0] = *reinterpret_cast<const uint32_t *>(src);
       }
-#pragma unroll
-      for (int k = 0; k < NW; ++k) w[i][k] ^= 0x88888888u;
       vsf[i] = valid[i] ? vsc[vrows[i] * NG + grp] : 0.f;
     }
     const uint32_t sA = pack_f16x2(vsf[0], vsf[1]);
@@ -461,11 +474,11 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
         for (int q = 0; q < 4; ++q) {  // nibble q: channel g*NT + 8k + 4hb + q
           uint32_t xa, xb;
           if (q & 1) {  // high nibble reads 1024 + 16u: /16 - 72 = code
-            xa = hfma2_u32(((tA >> (4 * (q - 1))) & 0x00F000F0u) | 0x64006400u, 1.0f / 16.0f, -72.0f);
-            xb = hfma2_u32(((tB >> (4 * (q - 1))) & 0x00F000F0u) | 0x64006400u, 1.0f / 16.0f, -72.0f);
+            xa = hfma2_u32(nib_hi_f16_biased(tA >> (4 * (q - 1))), 1.0f / 16.0f, -72.0f);
+            xb = hfma2_u32(nib_hi_f16_biased(tB >> (4 * (q - 1))), 1.0f / 16.0f, -72.0f);
           } else {
-            xa = hsub2_u32(((tA >> (4 * q)) & 0x000F000Fu) | 0x64006400u, 1032.0f);
-            xb = hsub2_u32(((tB >> (4 * q)) & 0x000F000Fu) | 0x64006400u, 1032.0f);
+            xa = hsub2_u32(nib_lo_f16_biased(tA >> (4 * q)), 1032.0f);
+            xb = hsub2_u32(nib_lo_f16_biased(tB >> (4 * q)), 1032.0f);
           }
           mma_f16_16816(o[8 * k + 4 * hb + q], pa, hmul2_u32(xa, sA), hmul2_u32(xb, sB));
         }
