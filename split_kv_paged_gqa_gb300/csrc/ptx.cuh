@@ -218,6 +218,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// (a & MASK) ^ c in one LOP3: the mask an immediate, c a register, so a
+// constant c shared by several masks occupies one register for all of them.
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "n"(MASK), "r"(c));
+  return d;
+}
+
 // fp16x2 arithmetic on packed 32-bit registers
 __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, float v) {
   __half2 r = __hsub2(*reinterpret_cast<__half2 *>(&a), __floats2half2_rn(v, v));

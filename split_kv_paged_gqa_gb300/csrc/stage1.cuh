@@ -52,6 +52,7 @@
 #include "kernels.h"
 #include "ptx.cuh"
 #include "splitmap.cuh"
+#include "tc.cuh"
 
 namespace fd {
 
@@ -100,7 +101,12 @@ struct S1Cfg {
   // the epilogue's (request, split, length, budget | direct << 16), parked
   // here through the main loop so they hold no registers there
   static constexpr int OFF_META = OFF_FLAG + 16;
-  static constexpr int SMEM = OFF_META + 16;
+  // int4 keeps O in tensor memory between blocks: D/2 fp32 columns
+  // per thread (its lane), allocated by consumer warp 0; the address lands here
+  static constexpr bool O_TMEM = KIND == KV_I4;  // int8 measured faster with O in registers
+  static constexpr int TMEM_COLS = D / 2;
+  static constexpr int OFF_TMEM = OFF_META + 16;
+  static constexpr int SMEM = OFF_TMEM + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;         // slack to align the base to 1024
   // CTAs per SM the shared memory allows (228 KB per SM, 1 KB reserved per CTA)
   static constexpr int MIN_BLOCKS = 3 * (SMEM_ALLOC + 1024) <= 228 * 1024   ? 3
@@ -122,12 +128,14 @@ __device__ __forceinline__ uint32_t u8pair_to_f16_biased(uint32_t t) {
 // int4 codes are stored as two's-complement nibbles n = code & 15, and
 // n ^ 8 = code + 8 = u in [0, 15]. From the nibbles at bits 0-3 and 16-19:
 // f16x2 (1024 + u, 1024 + u'); from those at bits 4-7 and 20-23:
-// f16x2 (1024 + 16u, 1024 + 16u'). Mask, bias and exponent in one LOP3.
-__device__ __forceinline__ uint32_t nib_lo_f16_biased(uint32_t t) {
-  return (t & 0x000F000Fu) ^ 0x64086408u;
+// f16x2 (1024 + 16u, 1024 + 16u'). Mask, bias and exponent in one LOP3 each
+// (the XOR constant is a register: kNibLo / kNibHi).
+constexpr uint32_t kNibLo = 0x64086408u, kNibHi = 0x64806480u;
+__device__ __forceinline__ uint32_t nib_lo_f16_biased(uint32_t t, uint32_t c) {
+  return and_xor<0x000F000Fu>(t, c);
 }
-__device__ __forceinline__ uint32_t nib_hi_f16_biased(uint32_t t) {
-  return (t & 0x00F000F0u) ^ 0x64806480u;
+__device__ __forceinline__ uint32_t nib_hi_f16_biased(uint32_t t, uint32_t c) {
+  return and_xor<0x00F000F0u>(t, c);
 }
 
 // ----------------------------------------------------------------------------
@@ -274,13 +282,14 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
                                              const float *vsc, int row0,
                                              const uint32_t (&qa)[C::D / 16][4],
                                              const float (&qc)[2][C::NG], const float (&rs)[2],
-                                             float (&o)[C::NT][4], float (&m)[2], float (&l)[2],
+                                             float (&o)[C::NT][4], uint32_t tm_o, float (&m)[2], float (&l)[2],
                                              int tok_row0, int c1, int lim0, int lim1, int lane) {
   constexpr int NG = C::NG, RB = C::ROW_BYTES, SW = C::BOX_BYTES, NT = C::NT;
   constexpr int CH = RB / 16;  // 16-byte chunks per cache row
   const int g = lane >> 2, c = lane & 3;
   const int mi = lane >> 3, ri = lane & 7;
   const uint32_t kbase = smem_u32(kt);
+  const uint32_t nib_lo = kNibLo, nib_hi = kNibHi;
 
   // ---- S = Q K^T in fp16 with biased K codes. Each 16-byte chunk of a K row
   // is one scale group for int4 (32 channels); its accumulator is folded into
@@ -320,8 +329,8 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
           // and XOR-ing in 8 and the exponent of 1024 is one LOP3 per pair
           const uint32_t x = r[nt * 2 + hh];
           const uint32_t y = x >> 8;
-          mma_f16_16816(acc[nt], qa[2 * ch], nib_lo_f16_biased(x), nib_lo_f16_biased(y));
-          mma_f16_16816(acc[nt], qa[2 * ch + 1], nib_hi_f16_biased(x), nib_hi_f16_biased(y));
+          mma_f16_16816(acc[nt], qa[2 * ch], nib_lo_f16_biased(x, nib_lo), nib_lo_f16_biased(y, nib_lo));
+          mma_f16_16816(acc[nt], qa[2 * ch + 1], nib_hi_f16_biased(x, nib_hi), nib_hi_f16_biased(y, nib_hi));
         }
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
@@ -370,15 +379,20 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
   }
   float p[2][4], al[2];
   softmax_update(s, p, m, l, al);
-  if (__any_sync(0xffffffffu, al[0] != 1.f || al[1] != 1.f)) {
+  const bool rescale = __any_sync(0xffffffffu, al[0] != 1.f || al[1] != 1.f);
+  // alpha-rescale of O if the max moved
+  auto rescale_o = [&](float (&oo)[NT][4]) {
+    if (rescale) {
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      o[j][0] *= al[0];
-      o[j][1] *= al[0];
-      o[j][2] *= al[1];
-      o[j][3] *= al[1];
+      for (int j = 0; j < NT; ++j) {
+        oo[j][0] *= al[0];
+        oo[j][1] *= al[0];
+        oo[j][2] *= al[1];
+        oo[j][3] *= al[1];
+      }
     }
-  }
+  };
+  if constexpr (!C::O_TMEM) rescale_o(o);  // (O in tensor memory is rescaled once loaded)
 
   // ---- P as the fp16 A operand (int8: the per-key V scale folded in)
   uint32_t pa[4];
@@ -445,7 +459,15 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
     }
   } else {
     static_assert(NT % 8 == 0, "int4 V words");
+    static_assert(C::O_TMEM, "int4 keeps O in tensor memory");
     constexpr int NW = NT / 8;  // 32-bit words per key
+    // O from tensor memory: it waits there through the score half of the
+    // block, which then runs with D/2 fewer live registers (the previous
+    // block's store has long landed; the wait only orders it before the load)
+    float ot[NT][4];
+    tmem_wait_st();
+#pragma unroll
+    for (int i = 0; i < NT / 8; ++i) tmem_ld32(tm_o + 32 * i, &ot[8 * i][0]);
     const int grp = (g * NT) / 32;
     uint32_t w[4][NW];
     float vsf[4];
@@ -463,6 +485,8 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
     }
     const uint32_t sA = pack_f16x2(vsf[0], vsf[1]);
     const uint32_t sB = pack_f16x2(vsf[2], vsf[3]);
+    tmem_wait_ld();
+    rescale_o(ot);
 #pragma unroll
     for (int k = 0; k < NW; ++k) {
 #pragma unroll
@@ -474,16 +498,18 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
         for (int q = 0; q < 4; ++q) {  // nibble q: channel g*NT + 8k + 4hb + q
           uint32_t xa, xb;
           if (q & 1) {  // high nibble reads 1024 + 16u: /16 - 72 = code
-            xa = hfma2_u32(nib_hi_f16_biased(tA >> (4 * (q - 1))), 1.0f / 16.0f, -72.0f);
-            xb = hfma2_u32(nib_hi_f16_biased(tB >> (4 * (q - 1))), 1.0f / 16.0f, -72.0f);
+            xa = hfma2_u32(nib_hi_f16_biased(tA >> (4 * (q - 1)), nib_hi), 1.0f / 16.0f, -72.0f);
+            xb = hfma2_u32(nib_hi_f16_biased(tB >> (4 * (q - 1)), nib_hi), 1.0f / 16.0f, -72.0f);
           } else {
-            xa = hsub2_u32(nib_lo_f16_biased(tA >> (4 * q)), 1032.0f);
-            xb = hsub2_u32(nib_lo_f16_biased(tB >> (4 * q)), 1032.0f);
+            xa = hsub2_u32(nib_lo_f16_biased(tA >> (4 * q), nib_lo), 1032.0f);
+            xb = hsub2_u32(nib_lo_f16_biased(tB >> (4 * q), nib_lo), 1032.0f);
           }
-          mma_f16_16816(o[8 * k + 4 * hb + q], pa, hmul2_u32(xa, sA), hmul2_u32(xb, sB));
+          mma_f16_16816(ot[8 * k + 4 * hb + q], pa, hmul2_u32(xa, sA), hmul2_u32(xb, sB));
         }
       }
     }
+#pragma unroll
+    for (int i = 0; i < NT / 8; ++i) tmem_st32(tm_o + 32 * i, &ot[8 * i][0]);
   }
 }
 
@@ -972,6 +998,11 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
   } else {
     // ======================= consumer warps =======================
     const int g = lane >> 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEM);
+    if constexpr (C::O_TMEM) {
+      if (warp == 0) tmem_alloc(tmem_slot, C::TMEM_COLS);
+      tc_fence_before();  // the address is read after the barrier below
+    }
     // Q tile (16 rows; rows past R are zero) -> shared -> A fragments
     uint8_t *qs = smem + C::OFF_Q;
 #pragma unroll
@@ -982,6 +1013,7 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
     if (threadIdx.x == 0)
       *reinterpret_cast<int4 *>(smem + C::OFF_META) = make_int4(b, s, L, S_req | (direct ? 1 << 16 : 0));
     named_barrier(1, C::NUM_CW * 32);
+    if constexpr (C::O_TMEM) tc_fence_after();
     uint32_t qa[D / 16][4];
     float qc[2][C::NG], rs[2];
     if constexpr (C::QUANT) {
@@ -1029,6 +1061,12 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
     float o[D / 8][4];
 #pragma unroll
     for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    // warp w's threads own TMEM lanes 32w .. 32w + 31
+    const uint32_t tm_o = C::O_TMEM ? *tmem_slot + ((static_cast<uint32_t>(warp) * 32u) << 16) : 0u;
+    if constexpr (C::O_TMEM) {
+#pragma unroll
+      for (int i = 0; i < D / 64; ++i) tmem_st32(tm_o + 32 * i, &o[8 * i][0]);
+    }
     float m[2] = {-INFINITY, -INFINITY};
     float l[2] = {0.f, 0.f};
     const int row0 = warp * 16;
@@ -1056,10 +1094,10 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
               qb[ks][2] = v.z;
               qb[ks][3] = v.w;
             }
-            warp_block_q<C, KIND>(kt, vt, ksc, vsc, row0, qb, qc, rs, o, m, l, tok_row0, c1, lim[0],
+            warp_block_q<C, KIND>(kt, vt, ksc, vsc, row0, qb, qc, rs, o, tm_o, m, l, tok_row0, c1, lim[0],
                                   lim[1], lane);
           } else {
-            warp_block_q<C, KIND>(kt, vt, ksc, vsc, row0, qa, qc, rs, o, m, l, tok_row0, c1, lim[0],
+            warp_block_q<C, KIND>(kt, vt, ksc, vsc, row0, qa, qc, rs, o, tm_o, m, l, tok_row0, c1, lim[0],
                                   lim[1], lane);
           }
         } else {
@@ -1085,12 +1123,26 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
       if (lane == 0) mbar_arrive(&empty[stage]);
     }
 
+    if constexpr (C::O_TMEM) {  // O back from tensor memory; the columns are freed below
+      tmem_wait_st();
+#pragma unroll
+      for (int i = 0; i < D / 64; ++i) tmem_ld32(tm_o + 32 * i, &o[8 * i][0]);
+      tmem_wait_ld();
+      tc_fence_before();
+    }
+
     // ---- merge the consumer warps' (max, sum, O) through shared memory
     l[0] += __shfl_xor_sync(0xffffffffu, l[0], 1);
     l[0] += __shfl_xor_sync(0xffffffffu, l[0], 2);
     l[1] += __shfl_xor_sync(0xffffffffu, l[1], 1);
     l[1] += __shfl_xor_sync(0xffffffffu, l[1], 2);
     named_barrier(1, C::NUM_CW * 32);  // every consumer is done with the ring
+    if constexpr (C::O_TMEM) {
+      if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(*tmem_slot, C::TMEM_COLS);
+      }
+    }
     const int4 meta = *reinterpret_cast<const int4 *>(smem + C::OFF_META);  // after the barrier above
     const int b_e = meta.x, s_e = meta.y, L_e = meta.z, S_e = meta.w & 0xffff;
     const bool direct_e = (meta.w >> 16) != 0;
