@@ -56,10 +56,15 @@
 
 namespace fd {
 
-template <int KIND, int D_, bool DEEP = false>
+template <int KIND, int D_, bool DEEP = false, bool NARROW = false>
 struct S1Cfg {
   static constexpr int D = D_;
   static constexpr bool QUANT = KIND != KV_BF16;
+  // NARROW (quantised caches, tiles of at most 8 query rows): the keys are the
+  // M dimension of the MMAs and the rows the 8-wide N dimension (warp_block_km)
+  static_assert(!NARROW || QUANT, "the narrow variant serves quantised caches");
+  static_assert(!(NARROW && DEEP), "one variant at a time");
+  static constexpr int OT = NARROW ? D / 16 : D / 8;     // O fragments (4 fp32 each) per thread
   static constexpr int ROW_BYTES = KIND == KV_BF16 ? 2 * D : (KIND == KV_I8 ? D : D / 2);
   static constexpr int BOX_BYTES = ROW_BYTES < 128 ? ROW_BYTES : 128;  // TMA box inner extent
   static constexpr int N_BOX = ROW_BYTES / BOX_BYTES;
@@ -81,7 +86,7 @@ struct S1Cfg {
   // Quantised kinds park the (identical) Q fragments of the consumer warps in
   // shared memory and reload them per block, so they do not hold 32 registers
   // through the PV half of the loop (three CTAs per SM allow 128 registers).
-  static constexpr bool QA_SMEM = QUANT;
+  static constexpr bool QA_SMEM = QUANT && !NARROW;  // (narrow: 2 registers per k-step, kept)
   static constexpr int TILE = BLOCK_N * ROW_BYTES;       // K (or V) bytes of one stage
   static constexpr int SC = QUANT ? BLOCK_N * NG * 4 : 0;
   static constexpr int STAGE = ((2 * TILE + 2 * SC) + 1023) / 1024 * 1024;
@@ -103,7 +108,8 @@ struct S1Cfg {
   static constexpr int OFF_META = OFF_FLAG + 16;
   // int4 keeps O in tensor memory between blocks: D/2 fp32 columns
   // per thread (its lane), allocated by consumer warp 0; the address lands here
-  static constexpr bool O_TMEM = KIND == KV_I4;  // int8 measured faster with O in registers
+  // (int8 measured faster with O in registers; narrow O is half the size)
+  static constexpr bool O_TMEM = KIND == KV_I4 && !NARROW;
   static constexpr int TMEM_COLS = D / 2;
   static constexpr int OFF_TMEM = OFF_META + 16;
   static constexpr int SMEM = OFF_TMEM + 16;
@@ -513,6 +519,199 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
   }
 }
 
+// ----------------------------------------------------------------------------
+// One 16-key block of one warp, quantised cache, for tiles of at most 8 query
+// rows ("narrow"). The 16 keys are the M dimension of the MMAs and the rows
+// the 8-wide N dimension, so no tile is mostly padding:
+//   S^T (16 keys x 8 rows)  = K (keys x channels) Q^T,
+//   O^T (16 channels x 8 rows) += V^T (channels x keys) P^T.
+// The K codes become A fragments straight from ldmatrix, in the channel order
+// of warp_block_q's B fragments (qb[ks] = that order's row-g Q fragment).
+// S^T's fragment holds keys (g, g + 8) x rows (2c, 2c + 1): a row's max
+// reduces over the 8 lanes of one c. P^T reaches the B-fragment layout of PV
+// through two 8x8 transposes (movmatrix). V codes become A fragments with
+// warp_block_q's byte permutes: m-tile j, slots g / g + 8 hold channels
+// g*NT + 2j / g*NT + 2j + 1 of rows (2c, 2c + 1) in o[j][0,1] / o[j][2,3].
+// l holds the thread's partial row sums over its keys (reduced across the 8
+// lanes of a row by the caller); m is the full row max.
+template <class C, int KIND>
+__device__ __forceinline__ void warp_block_km(const uint8_t *kt, const uint8_t *vt, const float *ksc,
+                                              const float *vsc, int row0, const uint32_t (&qb)[C::D / 16][2],
+                                              const float (&qc)[2][C::NG], const float (&rs)[2],
+                                              float (&o)[C::OT][4], float (&m)[2], float (&l)[2], int tok_row0,
+                                              int c1, int lim0, int lim1, int lane) {
+  constexpr int NG = C::NG, RB = C::ROW_BYTES, SW = C::BOX_BYTES, NT = C::NT;
+  constexpr int CH = RB / 16;  // 16-byte chunks per cache row
+  const int g = lane >> 2, c = lane & 3;
+  const int mi = lane >> 3, ri = lane & 7;
+  const uint32_t kbase = smem_u32(kt);
+  const uint32_t nib_lo = kNibLo, nib_hi = kNibHi;
+
+  // ---- S^T = K Q^T: sv = (key g, row 2c), (g, 2c+1), (g+8, 2c), (g+8, 2c+1)
+  float sv[4] = {0.f, 0.f, 0.f, 0.f};
+  float acc8[4] = {-qc[0][0], -qc[1][0], -qc[0][0], -qc[1][0]};  // int8: from -bias
+  const int krow = row0 + ((mi >> 1) << 3) + ri;
+#pragma unroll
+  for (int kc = 0; kc < CH; kc += 2) {
+    uint32_t r[4];  // (key g, chunk kc), (key g, kc + 1), (key g + 8, kc), (key g + 8, kc + 1)
+    ldsm_x4(r, kbase + swz<SW>(krow * RB + (kc + (mi & 1)) * 16));
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int ch = kc + hh;
+      if constexpr (KIND == KV_I8) {
+        const uint32_t xg = r[hh] ^ 0x80808080u, x8 = r[2 + hh] ^ 0x80808080u;  // bytes u = code + 128
+        const uint32_t a[4] = {__byte_perm(xg, 0x64646464u, 0x5140), __byte_perm(x8, 0x64646464u, 0x5140),
+                               __byte_perm(xg, 0x64646464u, 0x7362), __byte_perm(x8, 0x64646464u, 0x7362)};
+        mma_f16_16816(acc8, a, qb[ch][0], qb[ch][1]);
+      } else {
+        float acc[4] = {-qc[0][ch], -qc[1][ch], -qc[0][ch], -qc[1][ch]};
+        const uint32_t xg = r[hh], x8 = r[2 + hh];
+        const uint32_t yg = xg >> 8, y8 = x8 >> 8;
+        const uint32_t alo[4] = {nib_lo_f16_biased(xg, nib_lo), nib_lo_f16_biased(x8, nib_lo),
+                                 nib_lo_f16_biased(yg, nib_lo), nib_lo_f16_biased(y8, nib_lo)};
+        const uint32_t ahi[4] = {nib_hi_f16_biased(xg, nib_hi), nib_hi_f16_biased(x8, nib_hi),
+                                 nib_hi_f16_biased(yg, nib_hi), nib_hi_f16_biased(y8, nib_hi)};
+        mma_f16_16816(acc, alo, qb[2 * ch][0], qb[2 * ch][1]);
+        mma_f16_16816(acc, ahi, qb[2 * ch + 1][0], qb[2 * ch + 1][1]);
+        const float kg = ksc[(row0 + g) * NG + ch], k8 = ksc[(row0 + g + 8) * NG + ch];
+        sv[0] = fmaf(acc[0], kg, sv[0]);
+        sv[1] = fmaf(acc[1], kg, sv[1]);
+        sv[2] = fmaf(acc[2], k8, sv[2]);
+        sv[3] = fmaf(acc[3], k8, sv[3]);
+      }
+    }
+  }
+  if constexpr (KIND == KV_I8) {
+    const float kg = ksc[row0 + g], k8 = ksc[row0 + g + 8];
+    sv[0] = acc8[0] * kg;
+    sv[1] = acc8[1] * kg;
+    sv[2] = acc8[2] * k8;
+    sv[3] = acc8[3] * k8;
+  }
+
+  // ---- row scale, mask by selection, online softmax (rows 2c, 2c + 1)
+  const bool full = __all_sync(0xffffffffu, tok_row0 + 16 <= min(lim0, lim1));
+  float s[4] = {sv[0] * rs[0], sv[1] * rs[1], sv[2] * rs[0], sv[3] * rs[1]};
+  if (!full) {
+    const int kg = tok_row0 + g, k8 = kg + 8;
+    if (kg >= lim0) s[0] = -INFINITY;
+    if (kg >= lim1) s[1] = -INFINITY;
+    if (k8 >= lim0) s[2] = -INFINITY;
+    if (k8 >= lim1) s[3] = -INFINITY;
+  }
+  float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+  for (int x = 4; x < 32; x <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, x));
+  }
+  const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+  const float b0 = mn0 == -INFINITY ? 0.f : mn0;  // a row with no key yet keeps m = -inf
+  const float b1 = mn1 == -INFINITY ? 0.f : mn1;
+  const float al0 = fast_exp2(m[0] - b0), al1 = fast_exp2(m[1] - b1);
+  m[0] = mn0;
+  m[1] = mn1;
+  float p[4] = {fast_exp2(s[0] - b0), fast_exp2(s[1] - b1), fast_exp2(s[2] - b0), fast_exp2(s[3] - b1)};
+  l[0] = fmaf(l[0], al0, p[0] + p[2]);
+  l[1] = fmaf(l[1], al1, p[1] + p[3]);
+  if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+    for (int j = 0; j < C::OT; ++j) {
+      o[j][0] *= al0;
+      o[j][1] *= al1;
+      o[j][2] *= al0;
+      o[j][3] *= al1;
+    }
+  }
+
+  // ---- P^T -> the B fragments of PV (int8: the per-key V scale folded in)
+  if constexpr (KIND == KV_I8) {
+    const float vg = vsc[row0 + g], v8 = vsc[row0 + g + 8];
+    p[0] = p[0] == 0.f ? 0.f : p[0] * vg;
+    p[1] = p[1] == 0.f ? 0.f : p[1] * vg;
+    p[2] = p[2] == 0.f ? 0.f : p[2] * v8;
+    p[3] = p[3] == 0.f ? 0.f : p[3] * v8;
+  }
+  // (keys g | g + 8) x (rows 2c, 2c + 1) -> row g x (keys 2c, 2c + 1 | 2c + 8, 2c + 9)
+  const uint32_t pb0 = movmatrix_trans(pack_f16x2(p[0], p[1]));
+  const uint32_t pb1 = movmatrix_trans(pack_f16x2(p[2], p[3]));
+
+  // ---- V^T as A fragments: keys (2c, 2c+1) and (2c+8, 2c+9), channels
+  // [g*NT, g*NT + NT). Keys at or past c1 read as 0.
+  const int kA = row0 + 2 * c, kB = kA + 8;
+  const int vrows[4] = {kA, kA + 1, kB, kB + 1};
+  bool valid[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) valid[i] = full || tok_row0 + (vrows[i] - row0) < c1;
+  if constexpr (KIND == KV_I8) {
+    static_assert(NT % 4 == 0, "int8 V words");
+    constexpr int NW = NT / 4;  // 32-bit words per key
+    uint32_t w[4][NW];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint8_t *src = vt + swz<SW>(vrows[i] * RB + g * NT);
+      if constexpr (NW == 4) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(src);
+        w[i][0] = v.x;
+        w[i][1] = v.y;
+        w[i][2] = v.z;
+        w[i][3] = v.w;
+      } else {
+        const uint2 v = *reinterpret_cast<const uint2 *>(src);
+        w[i][0] = v.x;
+        w[i][1] = v.y;
+      }
+#pragma unroll
+      for (int k = 0; k < NW; ++k) w[i][k] = valid[i] ? (w[i][k] ^ 0x80808080u) : 0x80808080u;
+    }
+    auto pair = [&](uint32_t wa, uint32_t wb, int bi) {  // byte bi of two keys -> exact f16x2 codes
+      const uint32_t sel = bi | (bi << 4) | ((4u + bi) << 8) | ((4u + bi) << 12);
+      return hsub2_u32(u8pair_to_f16_biased(__byte_perm(wa, wb, sel)), 1152.0f);
+    };
+#pragma unroll
+    for (int j = 0; j < C::OT; ++j) {  // channels g*NT + 2j, + 1: word j / 2, bytes 2 (j % 2) + {0, 1}
+      const int k = j / 2, bi = 2 * (j % 2);
+      const uint32_t a[4] = {pair(w[0][k], w[1][k], bi), pair(w[0][k], w[1][k], bi + 1),
+                             pair(w[2][k], w[3][k], bi), pair(w[2][k], w[3][k], bi + 1)};
+      mma_f16_16816(o[j], a, pb0, pb1);
+    }
+  } else {
+    static_assert(NT % 8 == 0, "int4 V words");
+    constexpr int NW = NT / 8;  // 32-bit words per key
+    const int grp = (g * NT) / 32;
+    uint32_t w[4][NW];
+    float vsf[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint8_t *src = vt + swz<SW>(vrows[i] * RB + g * (NT / 2));
+      if constexpr (NW == 2) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(src);
+        w[i][0] = v.x;
+        w[i][1] = v.y;
+      } else {
+        w[i][0] = *reinterpret_cast<const uint32_t *>(src);
+      }
+      vsf[i] = valid[i] ? vsc[vrows[i] * NG + grp] : 0.f;
+    }
+    const uint32_t sA = pack_f16x2(vsf[0], vsf[1]);
+    const uint32_t sB = pack_f16x2(vsf[2], vsf[3]);
+    auto code = [&](uint32_t t, int q) {  // nibble q of two keys -> exact f16x2 codes
+      return (q & 1) ? hfma2_u32(nib_hi_f16_biased(t >> (4 * (q - 1)), nib_hi), 1.0f / 16.0f, -72.0f)
+                     : hsub2_u32(nib_lo_f16_biased(t >> (4 * q), nib_lo), 1032.0f);
+    };
+#pragma unroll
+    for (int j = 0; j < C::OT; ++j) {  // channels g*NT + 2j, + 1: word j / 4, bytes 2 ((j / 2) % 2) + {0, 1}
+      const int k = j / 4, hb = (j / 2) % 2, q = 2 * (j % 2);
+      const uint32_t sel = hb ? 0x7632u : 0x5410u;
+      const uint32_t tA = __byte_perm(w[0][k], w[1][k], sel);
+      const uint32_t tB = __byte_perm(w[2][k], w[3][k], sel);
+      const uint32_t a[4] = {hmul2_u32(code(tA, q), sA), hmul2_u32(code(tA, q + 1), sA),
+                             hmul2_u32(code(tB, q), sB), hmul2_u32(code(tB, q + 1), sB)};
+      mma_f16_16816(o[j], a, pb0, pb1);
+    }
+  }
+}
+
 // Quantised caches run Q K^T in fp16. Each query row is scaled by an exact
 // power of two, 2^-e, so that its largest |q| lies in [2^14, 2^15): every bf16
 // value then converts to fp16 exactly (8 significant bits fit 11; values below
@@ -749,11 +948,11 @@ __device__ __forceinline__ int prefetch_first_blocks(const CUtensorMap *tmk, con
   return L;
 }
 
-template <int KIND, int D, bool FUSED, bool DEEP>
-__global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, DEEP>::MIN_BLOCKS)
+template <int KIND, int D, bool FUSED, bool DEEP, bool NARROW>
+__global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<KIND, D, DEEP, NARROW>::MIN_BLOCKS)
     fd_stage1_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                      const __grid_constant__ Stage1Params p) {
-  using C = S1Cfg<KIND, D, DEEP>;
+  using C = S1Cfg<KIND, D, DEEP, NARROW>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -1015,12 +1214,20 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
     named_barrier(1, C::NUM_CW * 32);
     if constexpr (C::O_TMEM) tc_fence_after();
     uint32_t qa[D / 16][4];
+    uint32_t qb[D / 16][2];  // narrow: the row-g Q fragments as B operands
+    // the thread's two query rows: g and g + 8, or (narrow) 2c and 2c + 1
+    const int qrow0 = NARROW ? 2 * (lane & 3) : g, qrow_step = NARROW ? 1 : 8;
     float qc[2][C::NG], rs[2];
     if constexpr (C::QUANT) {
       float *qinfo = reinterpret_cast<float *>(smem + C::OFF_QI);
       if (threadIdx.x < 128) prepare_q_rows<C, KIND>(qs, qinfo, threadIdx.x);  // 8 threads per row
       named_barrier(1, C::NUM_CW * 32);
       build_q_fragments<C, KIND>(qs, qinfo, qa, lane);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        qb[ks][0] = qa[ks][0];
+        qb[ks][1] = qa[ks][2];
+      }
       if constexpr (C::QA_SMEM) {
         if (warp == 0) {
           uint4 *qa_s = reinterpret_cast<uint4 *>(smem + C::OFF_QA);
@@ -1032,9 +1239,10 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
       }
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
-        rs[hr] = qinfo[g + 8 * hr] * p.scale_log2;
+        const int qr = qrow0 + qrow_step * hr;
+        rs[hr] = qinfo[qr] * p.scale_log2;
 #pragma unroll
-        for (int gi = 0; gi < C::NG; ++gi) qc[hr][gi] = qinfo[16 + (g + 8 * hr) * C::NG + gi];
+        for (int gi = 0; gi < C::NG; ++gi) qc[hr][gi] = qinfo[16 + qr * C::NG + gi];
       }
     } else {
       const int mi = lane >> 3, ri = lane & 7;
@@ -1045,11 +1253,11 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
         ldsm_x4(qa[ks], smem_u32(qs + row * C::QROW + col * 2));
       }
     }
-    // causal limits of this thread's two rows (g and g + 8)
+    // causal limits of this thread's two rows
     int lim[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      const int rg = rt * 16 + g + 8 * k;
+      const int rg = rt * 16 + qrow0 + qrow_step * k;
       if (rg < p.R) {
         const int t = rg / p.G;
         lim[k] = min(c1, L - (p.Tq - 1) + t);
@@ -1058,9 +1266,9 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
       }
     }
 
-    float o[D / 8][4];
+    float o[C::OT][4];
 #pragma unroll
-    for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    for (int j = 0; j < C::OT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
     // warp w's threads own TMEM lanes 32w .. 32w + 31
     const uint32_t tm_o = C::O_TMEM ? *tmem_slot + ((static_cast<uint32_t>(warp) * 32u) << 16) : 0u;
     if constexpr (C::O_TMEM) {
@@ -1083,21 +1291,22 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
         if constexpr (C::QUANT) {
           const float *ksc = reinterpret_cast<const float *>(vt + C::TILE);
           const float *vsc = ksc + C::BLOCK_N * C::NG;
-          if constexpr (C::QA_SMEM) {
-            uint32_t qb[D / 16][4];
+          if constexpr (NARROW) {
+            warp_block_km<C, KIND>(kt, vt, ksc, vsc, row0, qb, qc, rs, o, m, l, tok_row0, c1, lim[0], lim[1],
+                                   lane);
+          } else {
+            static_assert(C::QA_SMEM, "the 16-row quantised block reads its Q fragments from shared memory");
+            uint32_t qf[D / 16][4];
             const uint4 *qa_s = reinterpret_cast<const uint4 *>(smem + C::OFF_QA);
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
               const uint4 v = qa_s[ks * 32 + lane];
-              qb[ks][0] = v.x;
-              qb[ks][1] = v.y;
-              qb[ks][2] = v.z;
-              qb[ks][3] = v.w;
+              qf[ks][0] = v.x;
+              qf[ks][1] = v.y;
+              qf[ks][2] = v.z;
+              qf[ks][3] = v.w;
             }
-            warp_block_q<C, KIND>(kt, vt, ksc, vsc, row0, qb, qc, rs, o, tm_o, m, l, tok_row0, c1, lim[0],
-                                  lim[1], lane);
-          } else {
-            warp_block_q<C, KIND>(kt, vt, ksc, vsc, row0, qa, qc, rs, o, tm_o, m, l, tok_row0, c1, lim[0],
+            warp_block_q<C, KIND>(kt, vt, ksc, vsc, row0, qf, qc, rs, o, tm_o, m, l, tok_row0, c1, lim[0],
                                   lim[1], lane);
           }
         } else {
@@ -1132,10 +1341,13 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
     }
 
     // ---- merge the consumer warps' (max, sum, O) through shared memory
-    l[0] += __shfl_xor_sync(0xffffffffu, l[0], 1);
-    l[0] += __shfl_xor_sync(0xffffffffu, l[0], 2);
-    l[1] += __shfl_xor_sync(0xffffffffu, l[1], 1);
-    l[1] += __shfl_xor_sync(0xffffffffu, l[1], 2);
+    // (a row's partial sums sit in the 4 lanes of a quad, or, narrow, in the
+    // 8 lanes of one c)
+#pragma unroll
+    for (int x = NARROW ? 4 : 1; x < (NARROW ? 32 : 4); x <<= 1) {
+      l[0] += __shfl_xor_sync(0xffffffffu, l[0], x);
+      l[1] += __shfl_xor_sync(0xffffffffu, l[1], x);
+    }
     named_barrier(1, C::NUM_CW * 32);  // every consumer is done with the ring
     if constexpr (C::O_TMEM) {
       if (warp == 0) {
@@ -1150,7 +1362,25 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
     float *co = reinterpret_cast<float *>(smem);
     float *cm = reinterpret_cast<float *>(smem + C::CMB_O);
     float *cl = cm + C::NUM_CW * 16;
-    {
+    if constexpr (NARROW) {
+      // rows 2c, 2c + 1: o[j] = (channel g*NT + 2j: rows 2c, 2c+1), (g*NT + 2j + 1: rows 2c, 2c+1)
+      const int c = lane & 3;
+      float *w0 = co + (warp * 16 + 2 * c) * C::CROW + g * C::NT;
+      float *w1 = w0 + C::CROW;
+#pragma unroll
+      for (int j = 0; j < C::OT; ++j) {
+        *reinterpret_cast<float2 *>(w0 + 2 * j) = make_float2(o[j][0], o[j][2]);
+        *reinterpret_cast<float2 *>(w1 + 2 * j) = make_float2(o[j][1], o[j][3]);
+      }
+      if (g == 0) {
+        cm[warp * 16 + 2 * c] = m[0];
+        cm[warp * 16 + 2 * c + 1] = m[1];
+        cl[warp * 16 + 2 * c] = l[0];
+        cl[warp * 16 + 2 * c + 1] = l[1];
+        cm[warp * 16 + 8 + 2 * c] = cm[warp * 16 + 9 + 2 * c] = -INFINITY;  // rows 8-15 hold no query
+        cl[warp * 16 + 8 + 2 * c] = cl[warp * 16 + 9 + 2 * c] = 0.f;
+      }
+    } else {
       const int c = lane & 3;
       float *w0 = co + (warp * 16 + g) * C::CROW;
       float *w1 = co + (warp * 16 + g + 8) * C::CROW;
@@ -1232,19 +1462,22 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP>::THREADS, S1Cfg<KIND, D, 
   if constexpr (!DEEP) griddep_launch_dependents();
 }
 
-template <int KIND, int D, bool FUSED, bool DEEP>
+template <int KIND, int D, bool FUSED, bool DEEP, bool NARROW>
 cudaError_t set_smem_limit() {
-  return cudaFuncSetAttribute(fd_stage1_kernel<KIND, D, FUSED, DEEP>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, S1Cfg<KIND, D, DEEP>::SMEM_ALLOC);
+  return cudaFuncSetAttribute(fd_stage1_kernel<KIND, D, FUSED, DEEP, NARROW>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, S1Cfg<KIND, D, DEEP, NARROW>::SMEM_ALLOC);
 }
 
 template <int KIND, int D>
 cudaError_t stage1_prepare_t() {
-  cudaError_t e = set_smem_limit<KIND, D, false, false>();
-  if (e == cudaSuccess) e = set_smem_limit<KIND, D, true, false>();
+  cudaError_t e = set_smem_limit<KIND, D, false, false, false>();
+  if (e == cudaSuccess) e = set_smem_limit<KIND, D, true, false, false>();
   if constexpr (KIND == KV_BF16) {
-    if (e == cudaSuccess) e = set_smem_limit<KIND, D, false, true>();
-    if (e == cudaSuccess) e = set_smem_limit<KIND, D, true, true>();
+    if (e == cudaSuccess) e = set_smem_limit<KIND, D, false, true, false>();
+    if (e == cudaSuccess) e = set_smem_limit<KIND, D, true, true, false>();
+  } else {
+    if (e == cudaSuccess) e = set_smem_limit<KIND, D, false, false, true>();
+    if (e == cudaSuccess) e = set_smem_limit<KIND, D, true, false, true>();
   }
   return e;
 }
@@ -1253,10 +1486,10 @@ cudaError_t stage1_prepare_t() {
 // scheduled while the previous kernel drains (a previous kernel that never
 // triggers simply completes first), and griddepcontrol.wait at its start
 // orders it after that kernel's memory operations.
-template <int KIND, int D, bool DEEP>
+template <int KIND, int D, bool DEEP, bool NARROW>
 cudaError_t launch_variant(bool fused, const CUtensorMap &tmk, const CUtensorMap &tmv,
                            const Stage1Params &p, dim3 grid, cudaStream_t stream) {
-  using C = S1Cfg<KIND, D, DEEP>;
+  using C = S1Cfg<KIND, D, DEEP, NARROW>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(C::THREADS);
@@ -1267,18 +1500,21 @@ cudaError_t launch_variant(bool fused, const CUtensorMap &tmk, const CUtensorMap
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (fused) return cudaLaunchKernelEx(&cfg, fd_stage1_kernel<KIND, D, true, DEEP>, tmk, tmv, p);
-  return cudaLaunchKernelEx(&cfg, fd_stage1_kernel<KIND, D, false, DEEP>, tmk, tmv, p);
+  if (fused) return cudaLaunchKernelEx(&cfg, fd_stage1_kernel<KIND, D, true, DEEP, NARROW>, tmk, tmv, p);
+  return cudaLaunchKernelEx(&cfg, fd_stage1_kernel<KIND, D, false, DEEP, NARROW>, tmk, tmv, p);
 }
 
 // deep: one-wave grids of the bf16 cache use the deep-ring variant.
+// Quantised caches with at most 8 query rows per KV head use the narrow one.
 template <int KIND, int D>
 cudaError_t launch_stage1_t(bool fused, bool deep, const CUtensorMap &tmk, const CUtensorMap &tmv,
                             const Stage1Params &p, dim3 grid, cudaStream_t stream) {
   if constexpr (KIND == KV_BF16) {
-    if (deep) return launch_variant<KIND, D, true>(fused, tmk, tmv, p, grid, stream);
+    if (deep) return launch_variant<KIND, D, true, false>(fused, tmk, tmv, p, grid, stream);
+  } else {
+    if (p.R <= 8) return launch_variant<KIND, D, false, true>(fused, tmk, tmv, p, grid, stream);
   }
-  return launch_variant<KIND, D, false>(fused, tmk, tmv, p, grid, stream);
+  return launch_variant<KIND, D, false, false>(fused, tmk, tmv, p, grid, stream);
 }
 
 }  // namespace fd

@@ -54,6 +54,12 @@ CASES = [
     ("int4", 2, 4, 32, 8, 128, 16, (4096, 1111)),
     ("int4", 3, 1, 8, 2, 128, 64, (70, 640, 2000)),
     ("int4", 2, 1, 16, 4, 64, 16, (333, 48)),
+    # quantised tiles of <= 8 rows run keys-as-M ("narrow"): causal MTP rows,
+    # one row (MHA), and a 12-row tile that stays on the 16-row layout
+    ("int8", 2, 2, 16, 4, 128, 16, (700, 33)),          # R = 8, causal
+    ("int4", 2, 4, 8, 4, 128, 32, (260, 1500)),         # R = 8, causal
+    ("int4", 2, 1, 8, 8, 128, 16, (129, 2000)),         # R = 1
+    ("int8", 2, 3, 32, 8, 64, 16, (500, 81)),           # R = 12
 ]
 
 
