@@ -131,6 +131,13 @@ __device__ __forceinline__ uint32_t u8pair_to_f16_biased(uint32_t t) {
   return (t & 0x00FF00FFu) | 0x64006400u;
 }
 
+// The same from raw int8 codes (u = code ^ 0x80): mask, sign flip and exponent
+// in one LOP3, with c = kU8Bias in a register.
+constexpr uint32_t kU8Bias = 0x64806480u;
+__device__ __forceinline__ uint32_t i8pair_to_f16_biased(uint32_t t, uint32_t c) {
+  return and_xor<0x00FF00FFu>(t, c);
+}
+
 // int4 codes are stored as two's-complement nibbles n = code & 15, and
 // n ^ 8 = code + 8 = u in [0, 15]. From the nibbles at bits 0-3 and 16-19:
 // f16x2 (1024 + u, 1024 + u'); from those at bits 4-7 and 20-23:
@@ -662,11 +669,12 @@ __device__ __forceinline__ void warp_block_km(const uint8_t *kt, const uint8_t *
         w[i][1] = v.y;
       }
 #pragma unroll
-      for (int k = 0; k < NW; ++k) w[i][k] = valid[i] ? (w[i][k] ^ 0x80808080u) : 0x80808080u;
+      for (int k = 0; k < NW; ++k) w[i][k] = valid[i] ? w[i][k] : 0u;  // raw codes; 0 reads as code 0
     }
+    const uint32_t u8_bias = kU8Bias;
     auto pair = [&](uint32_t wa, uint32_t wb, int bi) {  // byte bi of two keys -> exact f16x2 codes
       const uint32_t sel = bi | (bi << 4) | ((4u + bi) << 8) | ((4u + bi) << 12);
-      return hsub2_u32(u8pair_to_f16_biased(__byte_perm(wa, wb, sel)), 1152.0f);
+      return hsub2_u32(i8pair_to_f16_biased(__byte_perm(wa, wb, sel), u8_bias), 1152.0f);
     };
 #pragma unroll
     for (int j = 0; j < C::OT; ++j) {  // channels g*NT + 2j, + 1: word j / 2, bytes 2 (j % 2) + {0, 1}
