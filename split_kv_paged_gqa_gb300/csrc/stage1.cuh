@@ -633,11 +633,15 @@ __device__ __forceinline__ void warp_block_km(const uint8_t *kt, const uint8_t *
 
   // ---- P^T -> the B fragments of PV (int8: the per-key V scale folded in)
   if constexpr (KIND == KV_I8) {
-    const float vg = vsc[row0 + g], v8 = vsc[row0 + g + 8];
-    p[0] = p[0] == 0.f ? 0.f : p[0] * vg;
-    p[1] = p[1] == 0.f ? 0.f : p[1] * vg;
-    p[2] = p[2] == 0.f ? 0.f : p[2] * v8;
-    p[3] = p[3] == 0.f ? 0.f : p[3] * v8;
+    float vg = vsc[row0 + g], v8 = vsc[row0 + g + 8];
+    if (!full) {  // the scale of a key past the split end may be anything: it meets p = 0
+      if (tok_row0 + g >= c1) vg = 0.f;
+      if (tok_row0 + g + 8 >= c1) v8 = 0.f;
+    }
+    p[0] *= vg;
+    p[1] *= vg;
+    p[2] *= v8;
+    p[3] *= v8;
   }
   // (keys g | g + 8) x (rows 2c, 2c + 1) -> row g x (keys 2c, 2c + 1 | 2c + 8, 2c + 9)
   const uint32_t pb0 = movmatrix_trans(pack_f16x2(p[0], p[1]));
@@ -668,8 +672,12 @@ __device__ __forceinline__ void warp_block_km(const uint8_t *kt, const uint8_t *
         w[i][0] = v.x;
         w[i][1] = v.y;
       }
+    }
+    if (!full) {  // keys past the split end read as code 0 (a raw 0)
 #pragma unroll
-      for (int k = 0; k < NW; ++k) w[i][k] = valid[i] ? w[i][k] : 0u;  // raw codes; 0 reads as code 0
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int k = 0; k < NW; ++k) w[i][k] = valid[i] ? w[i][k] : 0u;
     }
     const uint32_t u8_bias = kU8Bias;
     auto pair = [&](uint32_t wa, uint32_t wb, int bi) {  // byte bi of two keys -> exact f16x2 codes
