@@ -126,13 +126,9 @@ struct S1Cfg {
 // ----------------------------------------------------------------------------
 // In-register conversions of cache codes to fp16 (exact: |code| <= 128).
 
-// f16x2 (1024 + u_lo, 1024 + u_hi) from biased bytes at bits 0-7 and 16-23.
-__device__ __forceinline__ uint32_t u8pair_to_f16_biased(uint32_t t) {
-  return (t & 0x00FF00FFu) | 0x64006400u;
-}
-
-// The same from raw int8 codes (u = code ^ 0x80): mask, sign flip and exponent
-// in one LOP3, with c = kU8Bias in a register.
+// f16x2 (1024 + u_lo, 1024 + u_hi), u = code + 128, from the raw int8 codes
+// at bits 0-7 and 16-23 (u = code ^ 0x80): mask, sign flip and exponent in
+// one LOP3, with c = kU8Bias in a register.
 constexpr uint32_t kU8Bias = 0x64806480u;
 __device__ __forceinline__ uint32_t i8pair_to_f16_biased(uint32_t t, uint32_t c) {
   return and_xor<0x00FF00FFu>(t, c);
@@ -438,6 +434,7 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
   for (int i = 0; i < 4; ++i) valid[i] = full || tok_row0 + (vrows[i] - row0) < c1;
   if constexpr (KIND == KV_I8) {
     static_assert(NT % 4 == 0, "int8 V words");
+    static_assert(!C::O_TMEM, "int8 keeps O in registers");
     constexpr int NW = NT / 4;  // 32-bit words per key
     uint32_t w[4][NW];
 #pragma unroll
@@ -454,9 +451,14 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
         w[i][0] = v.x;
         w[i][1] = v.y;
       }
-#pragma unroll
-      for (int k = 0; k < NW; ++k) w[i][k] = valid[i] ? (w[i][k] ^ 0x80808080u) : 0x80808080u;
     }
+    if (!full) {  // keys past the split end read as code 0 (a raw 0)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int k = 0; k < NW; ++k) w[i][k] = valid[i] ? w[i][k] : 0u;
+    }
+    const uint32_t u8_bias = kU8Bias;
 #pragma unroll
     for (int k = 0; k < NW; ++k) {
 #pragma unroll
@@ -464,9 +466,9 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
         // byte bi of both keys -> bits 0-7 and 16-23: channel g*NT + 4k + bi
         const uint32_t sel = (bi) | (bi << 4) | ((4u + bi) << 8) | ((4u + bi) << 12);
         const uint32_t b0 =
-            hsub2_u32(u8pair_to_f16_biased(__byte_perm(w[0][k], w[1][k], sel)), 1152.0f);
+            hsub2_u32(i8pair_to_f16_biased(__byte_perm(w[0][k], w[1][k], sel), u8_bias), 1152.0f);
         const uint32_t b1 =
-            hsub2_u32(u8pair_to_f16_biased(__byte_perm(w[2][k], w[3][k], sel)), 1152.0f);
+            hsub2_u32(i8pair_to_f16_biased(__byte_perm(w[2][k], w[3][k], sel), u8_bias), 1152.0f);
         mma_f16_16816(o[4 * k + bi], pa, b0, b1);
       }
     }
