@@ -13,7 +13,7 @@
 //    at least chunk_min keys); split s owns keys [s * chunk, min(L_b, (s + 1) *
 //    chunk)), derived here from cache_seqlens.
 //  * producer warp: reads page ids from the page table one stage ahead, and
-//    lane 0 issues 4-D TMA loads (d, head, slot, page) of whole page segments
+//    lane i issues the 4-D TMA loads (d, head, slot, page) of page segment i
 //    of K and V into a STAGES-deep shared-memory ring, 128-byte swizzled,
 //    completing on a per-stage mbarrier. Quantised caches also copy their
 //    per-row fp32 scales with cp.async (one arrival per lane on the barrier).
@@ -25,7 +25,7 @@
 //    from the raw tile, no staging copy:
 //      - K: ldmatrix of the raw rows as 16-bit elements hands each thread 4
 //        (int8) or 8 (int4) consecutive codes of one key; they become exact
-//        bf16 B fragments, and the Q A fragments are built once per CTA with
+//        (biased) fp16 B fragments, and the Q A fragments are built once per CTA with
 //        the matching channel order (a dot product does not care about the
 //        order of its terms). K scales multiply the fp32 scores (per
 //        32-channel group for int4, from one accumulator per group).
@@ -34,7 +34,10 @@
 //        B fragments; PV output columns come out permuted and are put back in
 //        order by the epilogue. int8 folds the per-key V scale into the
 //        probabilities (fp16); int4 multiplies its per-group V scale into the
-//        fp16 V values.
+//        fp16 V values, and keeps O in tensor memory between blocks.
+//    Quantised tiles of at most 8 rows ("narrow", warp_block_km) swap the
+//    roles: keys and channels are the M dimension, the rows the 8-wide N
+//    dimension, so the MMAs and the softmax carry no empty rows.
 //  * epilogue: the consumer warps merge their (max, sum, O) through shared
 //    memory and write either fp32 partial O + LSE to the split workspace, or
 //    (num_splits == 1) the final bf16/fp32 output and LSE.
