@@ -231,6 +231,9 @@ def blas_threads():
     return None
 
 
+CPU_BASELINE_S = 10.0  # oracle time the cpu_baseline sample aims at
+
+
 def oracle_baseline(w: wl.Workload, requests, key_hi=None):
     """Time the float64 oracle on a sample of requests; returns (GB/s, seconds, bytes)."""
     from oracle import decode_ref_inputs
@@ -504,11 +507,19 @@ def run_fd(args):
     # CPU baseline: the oracle on a bounded sample of this workload, host cores
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        reqs = list(range(min(2, B)))
-        gbps, secs, nbytes = oracle_baseline(w, reqs)
+        # whole requests, in order, until about CPU_BASELINE_S of oracle time
+        reqs, secs, nbytes = [], 0.0, 0
+        for b in range(B):
+            _, dt, nb = oracle_baseline(w, [b])
+            reqs.append(b)
+            secs += dt
+            nbytes += nb
+            if secs >= CPU_BASELINE_S:
+                break
+        gbps = nbytes / secs / 1e9
         cpu = {"value": round(gbps, 4), "unit": "GB/s", "cores": len(os.sched_getaffinity(0)),
                "blas_threads": blas_threads(), "kind": "oracle",
-               "sample": f"requests {reqs} of the workload ({len(reqs)} x {int(w.lengths[0])} keys, "
+               "sample": f"requests 0..{len(reqs) - 1} of the workload ({int(sum(w.lengths[:len(reqs)]))} keys, "
                          f"{nbytes / 1e6:.0f} MB of KV), float64 full softmax, {secs:.1f} s"}
 
     fd.fd_set_plan(None)
