@@ -1198,8 +1198,11 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
           const int a0 = __shfl_sync(0xffffffffu, p0, pi & 31);
           const int a1 = __shfl_sync(0xffffffffu, p1, pi & 31);
           const int pid = pi < 32 ? a0 : a1;
-          if (tok < tend && pid < p.num_pages) {
-            const float *src = p.kv_scales + static_cast<int64_t>(pid) * p.sc_sp +
+          if (tok < tend) {
+            // a page id outside the pool (reported above; its codes read as
+            // 0) takes page 0's scales, so the result stays finite
+            const int ps = pid < p.num_pages ? pid : 0;
+            const float *src = p.kv_scales + static_cast<int64_t>(ps) * p.sc_sp +
                                static_cast<int64_t>(tok & (P - 1)) * p.sc_ss +
                                static_cast<int64_t>(h) * p.sc_sh;
             cp_async_ca<C::NG * 4>(ksc + i * C::NG, src);

@@ -510,8 +510,10 @@ __global__ void __launch_bounds__(TcCfg<KIND>::THREADS, 1)
       for (int i = lane; i < C::BLOCK_N; i += 32) {
         const int tok = tok0 + i;
         const int pid = pid_of((min(tok, tend - 1) >> p.log2_page) - fp0);
-        if (tok < tend && pid >= 0 && pid < p.num_pages) {
-          const float *src = p.kv_scales + static_cast<int64_t>(pid) * p.sc_sp +
+        if (tok < tend) {
+          // a page id outside the pool takes page 0's scales (its codes read as 0)
+          const int ps = (pid >= 0 && pid < p.num_pages) ? pid : 0;
+          const float *src = p.kv_scales + static_cast<int64_t>(ps) * p.sc_sp +
                              static_cast<int64_t>(tok & (P - 1)) * p.sc_ss + static_cast<int64_t>(h) * p.sc_sh;
           cp_async_ca<C::NG * 4>(ksc + i * C::NG, src);
           cp_async_ca<C::NG * 4>(vsc + i * C::NG, src + p.sc_sk);
