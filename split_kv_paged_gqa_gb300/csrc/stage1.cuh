@@ -85,11 +85,15 @@ struct S1Cfg {
   // bytes and blocks in flight.
   // Quantised kinds are bound by the consumer warps' latency, not by bytes in
   // flight: they run three CTAs per SM with shorter rings.
-  static constexpr int STAGES = KIND == KV_BF16 ? 3 : (KIND == KV_I8 ? 3 : 6);
+  // (the narrow int8 variant runs four CTAs per SM on a 2-stage ring)
+  static constexpr bool FOUR = KIND == KV_I8 && NARROW;
+  static constexpr int STAGES = KIND == KV_BF16 ? 3 : (KIND == KV_I8 ? (FOUR ? 2 : 3) : 6);
   // Quantised kinds park the (identical) Q fragments of the consumer warps in
   // shared memory and reload them per block, so they do not hold 32 registers
   // through the PV half of the loop (three CTAs per SM allow 128 registers).
-  static constexpr bool QA_SMEM = QUANT && !NARROW;  // (narrow: 2 registers per k-step, kept)
+  static constexpr bool QA_SMEM = QUANT && !NARROW;
+  // narrow: 2 registers per k-step, kept through the loop, or (FOUR) reloaded per block
+  static constexpr bool QB_SMEM = FOUR;
   static constexpr int TILE = BLOCK_N * ROW_BYTES;       // K (or V) bytes of one stage
   static constexpr int SC = QUANT ? BLOCK_N * NG * 4 : 0;
   static constexpr int STAGE = ((2 * TILE + 2 * SC) + 1023) / 1024 * 1024;
@@ -97,13 +101,14 @@ struct S1Cfg {
   static constexpr int QROW = D * 2 + 16;                // padded bf16 row of the Q tile
   static constexpr int QB = 16 * QROW;
   static constexpr int CROW = D + 8;                     // padded fp32 row of the combine tile
-  static constexpr int CMB_O = NUM_CW * 16 * CROW * 4;
-  static constexpr int CMB = CMB_O + NUM_CW * 16 * 2 * 4;
+  static constexpr int TR = NARROW ? 8 : 16;              // combine-tile rows per warp
+  static constexpr int CMB_O = NUM_CW * TR * CROW * 4;
+  static constexpr int CMB = CMB_O + NUM_CW * TR * 2 * 4;
   static constexpr int OFF_Q = RING;
   static constexpr int OFF_QI = OFF_Q + QB;              // per row: 2^e, then NG bias constants
   static constexpr int QI = QUANT ? 16 * (1 + NG) * 4 : 0;
   static constexpr int OFF_QA = (OFF_QI + QI + 15) / 16 * 16;  // [D/16][32 lanes] uint4
-  static constexpr int QAB = QA_SMEM ? (D / 16) * 32 * 16 : 0;
+  static constexpr int QAB = QA_SMEM ? (D / 16) * 32 * 16 : (QB_SMEM ? (D / 16) * 32 * 8 : 0);
   static constexpr int OFF_BAR = (OFF_QA + QAB + 7) / 8 * 8;
   static constexpr int OFF_FLAG = OFF_BAR + 2 * STAGES * 8;  // "this CTA merges" flag
   // the epilogue's (request, split, length, budget | direct << 16), parked
@@ -118,7 +123,8 @@ struct S1Cfg {
   static constexpr int SMEM = OFF_TMEM + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;         // slack to align the base to 1024
   // CTAs per SM the shared memory allows (228 KB per SM, 1 KB reserved per CTA)
-  static constexpr int MIN_BLOCKS = 3 * (SMEM_ALLOC + 1024) <= 228 * 1024   ? 3
+  static constexpr int MIN_BLOCKS = FOUR && 4 * (SMEM_ALLOC + 1024) <= 228 * 1024 ? 4
+                                    : 3 * (SMEM_ALLOC + 1024) <= 228 * 1024   ? 3
                                     : 2 * (SMEM_ALLOC + 1024) <= 228 * 1024 ? 2
                                                                              : 1;
   static_assert(CMB <= RING, "combine tile must fit in the ring");
@@ -1252,6 +1258,14 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
         qb[ks][0] = qa[ks][0];
         qb[ks][1] = qa[ks][2];
       }
+      if constexpr (C::QB_SMEM) {
+        if (warp == 0) {
+          uint2 *qb_s = reinterpret_cast<uint2 *>(smem + C::OFF_QA);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) qb_s[ks * 32 + lane] = make_uint2(qb[ks][0], qb[ks][1]);
+        }
+        named_barrier(1, C::NUM_CW * 32);
+      }
       if constexpr (C::QA_SMEM) {
         if (warp == 0) {
           uint4 *qa_s = reinterpret_cast<uint4 *>(smem + C::OFF_QA);
@@ -1315,7 +1329,18 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
         if constexpr (C::QUANT) {
           const float *ksc = reinterpret_cast<const float *>(vt + C::TILE);
           const float *vsc = ksc + C::BLOCK_N * C::NG;
-          if constexpr (NARROW) {
+          if constexpr (NARROW && C::QB_SMEM) {
+            uint32_t qr[D / 16][2];
+            const uint2 *qb_s = reinterpret_cast<const uint2 *>(smem + C::OFF_QA);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint2 v = qb_s[ks * 32 + lane];
+              qr[ks][0] = v.x;
+              qr[ks][1] = v.y;
+            }
+            warp_block_km<C, KIND>(kt, vt, ksc, vsc, row0, qr, qc, rs, o, m, l, tok_row0, c1, lim[0], lim[1],
+                                   lane);
+          } else if constexpr (NARROW) {
             warp_block_km<C, KIND>(kt, vt, ksc, vsc, row0, qb, qc, rs, o, m, l, tok_row0, c1, lim[0], lim[1],
                                    lane);
           } else {
@@ -1385,11 +1410,11 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
     const int h_e = p.balanced ? (blockIdx.x / p.row_tiles) % p.Hkv : blockIdx.y;
     float *co = reinterpret_cast<float *>(smem);
     float *cm = reinterpret_cast<float *>(smem + C::CMB_O);
-    float *cl = cm + C::NUM_CW * 16;
+    float *cl = cm + C::NUM_CW * C::TR;
     if constexpr (NARROW) {
       // rows 2c, 2c + 1: o[j] = (channel g*NT + 2j: rows 2c, 2c+1), (g*NT + 2j + 1: rows 2c, 2c+1)
       const int c = lane & 3;
-      float *w0 = co + (warp * 16 + 2 * c) * C::CROW + g * C::NT;
+      float *w0 = co + (warp * C::TR + 2 * c) * C::CROW + g * C::NT;
       float *w1 = w0 + C::CROW;
 #pragma unroll
       for (int j = 0; j < C::OT; ++j) {
@@ -1397,12 +1422,10 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
         *reinterpret_cast<float2 *>(w1 + 2 * j) = make_float2(o[j][1], o[j][3]);
       }
       if (g == 0) {
-        cm[warp * 16 + 2 * c] = m[0];
-        cm[warp * 16 + 2 * c + 1] = m[1];
-        cl[warp * 16 + 2 * c] = l[0];
-        cl[warp * 16 + 2 * c + 1] = l[1];
-        cm[warp * 16 + 8 + 2 * c] = cm[warp * 16 + 9 + 2 * c] = -INFINITY;  // rows 8-15 hold no query
-        cl[warp * 16 + 8 + 2 * c] = cl[warp * 16 + 9 + 2 * c] = 0.f;
+        cm[warp * C::TR + 2 * c] = m[0];
+        cm[warp * C::TR + 2 * c + 1] = m[1];
+        cl[warp * C::TR + 2 * c] = l[0];
+        cl[warp * C::TR + 2 * c + 1] = l[1];
       }
     } else {
       const int c = lane & 3;
@@ -1428,7 +1451,7 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
       }
     }
     named_barrier(1, C::NUM_CW * 32);
-    if (threadIdx.x < 128) {  // 8 threads per row of the tile
+    if (threadIdx.x < 8 * C::TR) {  // 8 threads per row of the tile (narrow: 8 rows)
       constexpr int TPR = 8;
       constexpr int DPT = D / TPR;  // columns per thread
       const int tid = threadIdx.x;
@@ -1439,14 +1462,14 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < C::NUM_CW; ++w) {
-        mw[w] = cm[w * 16 + row];
+        mw[w] = cm[w * C::TR + row];
         M = fmaxf(M, mw[w]);
       }
       float Lsum = 0.f;
 #pragma unroll
       for (int w = 0; w < C::NUM_CW; ++w) {
         wt[w] = mw[w] == -INFINITY ? 0.f : fast_exp2(mw[w] - M);
-        Lsum = fmaf(wt[w], cl[w * 16 + row], Lsum);
+        Lsum = fmaf(wt[w], cl[w * C::TR + row], Lsum);
       }
       const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
       const float lse_nat = Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
@@ -1455,7 +1478,7 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
       for (int i = 0; i < DPT; ++i) {
         float a = 0.f;
 #pragma unroll
-        for (int w = 0; w < C::NUM_CW; ++w) a = fmaf(wt[w], co[(w * 16 + row) * C::CROW + d0 + i], a);
+        for (int w = 0; w < C::NUM_CW; ++w) a = fmaf(wt[w], co[(w * C::TR + row) * C::CROW + d0 + i], a);
         vals[i] = a * inv;
       }
       if (rg < p.R) write_row_outputs<C>(p, direct_e, b_e, h_e, s_e, rg, d0, vals, DPT, lse_nat, d0 == 0);
