@@ -85,9 +85,9 @@ struct S1Cfg {
   // bytes and blocks in flight.
   // Quantised kinds are bound by the consumer warps' latency, not by bytes in
   // flight: they run three CTAs per SM with shorter rings.
-  // (the narrow int8 variant runs four CTAs per SM on a 2-stage ring)
-  static constexpr bool FOUR = KIND == KV_I8 && NARROW;
-  static constexpr int STAGES = KIND == KV_BF16 ? 3 : (KIND == KV_I8 ? (FOUR ? 2 : 3) : 6);
+  // (the narrow variants run four CTAs per SM on shorter rings)
+  static constexpr bool FOUR = NARROW;
+  static constexpr int STAGES = KIND == KV_BF16 ? 3 : (KIND == KV_I8 ? (FOUR ? 2 : 3) : (FOUR ? 4 : 6));
   // Quantised kinds park the (identical) Q fragments of the consumer warps in
   // shared memory and reload them per block, so they do not hold 32 registers
   // through the PV half of the loop (three CTAs per SM allow 128 registers).
