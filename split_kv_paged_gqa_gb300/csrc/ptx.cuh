@@ -128,10 +128,6 @@ __device__ __forceinline__ int ld_relaxed_gpu(const int *p) {
   return v;
 }
 
-__device__ __forceinline__ void prefetch_l2(const void *p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 // 4-D tiled TMA load into shared memory, completing bytes on bar.
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *tm, int c0, int c1, int c2,
                                             int c3, uint64_t *bar, uint64_t policy) {

@@ -84,16 +84,15 @@ struct S1Cfg {
   // that fit in one wave (small batches), where a single CTA must keep enough
   // bytes and blocks in flight.
   // Quantised kinds are bound by the consumer warps' latency, not by bytes in
-  // flight: they run three CTAs per SM with shorter rings.
-  // (the narrow variants run four CTAs per SM on shorter rings)
+  // flight: the 16-row variants run three CTAs per SM (128 registers), the
+  // narrow ones four (96 registers), on rings that fit.
   static constexpr bool FOUR = NARROW;
   static constexpr int STAGES = KIND == KV_BF16 ? 3 : (KIND == KV_I8 ? (FOUR ? 2 : 3) : (FOUR ? 4 : 6));
   // Quantised kinds park the (identical) Q fragments of the consumer warps in
-  // shared memory and reload them per block, so they do not hold 32 registers
-  // through the PV half of the loop (three CTAs per SM allow 128 registers).
+  // shared memory and reload them per block, so they do not hold 32 (narrow:
+  // 16) registers through the PV half of the loop.
   static constexpr bool QA_SMEM = QUANT && !NARROW;
-  // narrow: 2 registers per k-step, kept through the loop, or (FOUR) reloaded per block
-  static constexpr bool QB_SMEM = FOUR;
+  static constexpr bool QB_SMEM = NARROW;
   static constexpr int TILE = BLOCK_N * ROW_BYTES;       // K (or V) bytes of one stage
   static constexpr int SC = QUANT ? BLOCK_N * NG * 4 : 0;
   static constexpr int STAGE = ((2 * TILE + 2 * SC) + 1023) / 1024 * 1024;
@@ -1329,7 +1328,8 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
         if constexpr (C::QUANT) {
           const float *ksc = reinterpret_cast<const float *>(vt + C::TILE);
           const float *vsc = ksc + C::BLOCK_N * C::NG;
-          if constexpr (NARROW && C::QB_SMEM) {
+          if constexpr (NARROW) {
+            static_assert(C::QB_SMEM, "the narrow block reloads its Q fragments from shared memory");
             uint32_t qr[D / 16][2];
             const uint2 *qb_s = reinterpret_cast<const uint2 *>(smem + C::OFF_QA);
 #pragma unroll
@@ -1339,9 +1339,6 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
               qr[ks][1] = v.y;
             }
             warp_block_km<C, KIND>(kt, vt, ksc, vsc, row0, qr, qc, rs, o, m, l, tok_row0, c1, lim[0], lim[1],
-                                   lane);
-          } else if constexpr (NARROW) {
-            warp_block_km<C, KIND>(kt, vt, ksc, vsc, row0, qb, qc, rs, o, m, l, tok_row0, c1, lim[0], lim[1],
                                    lane);
           } else {
             static_assert(C::QA_SMEM, "the 16-row quantised block reads its Q fragments from shared memory");
