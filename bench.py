@@ -234,6 +234,21 @@ def blas_threads():
 CPU_BASELINE_S = 10.0  # oracle time the cpu_baseline sample aims at
 
 
+def cpu_baseline_sample(time_request, batch: int, budget_s: float = CPU_BASELINE_S):
+    """Whole requests 0, 1, ... timed one at a time (time_request(b) returns
+    (GB/s, seconds, bytes)) until budget_s of oracle time or the whole batch;
+    returns (requests, seconds, bytes)."""
+    reqs, secs, nbytes = [], 0.0, 0
+    for b in range(batch):
+        _, dt, nb = time_request(b)
+        reqs.append(b)
+        secs += dt
+        nbytes += nb
+        if secs >= budget_s:
+            break
+    return reqs, secs, nbytes
+
+
 def oracle_baseline(w: wl.Workload, requests, key_hi=None):
     """Time the float64 oracle on a sample of requests; returns (GB/s, seconds, bytes)."""
     from oracle import decode_ref_inputs
@@ -507,15 +522,7 @@ def run_fd(args):
     # CPU baseline: the oracle on a bounded sample of this workload, host cores
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        # whole requests, in order, until about CPU_BASELINE_S of oracle time
-        reqs, secs, nbytes = [], 0.0, 0
-        for b in range(B):
-            _, dt, nb = oracle_baseline(w, [b])
-            reqs.append(b)
-            secs += dt
-            nbytes += nb
-            if secs >= CPU_BASELINE_S:
-                break
+        reqs, secs, nbytes = cpu_baseline_sample(lambda b: oracle_baseline(w, [b]), B)
         gbps = nbytes / secs / 1e9
         cpu = {"value": round(gbps, 4), "unit": "GB/s", "cores": len(os.sched_getaffinity(0)),
                "blas_threads": blas_threads(), "kind": "oracle",

@@ -83,3 +83,17 @@ def test_stage1_sha_covers_kernel_sources_only():
 def test_nearest_pow2_matches_the_log_midpoint():
     assert [bench.nearest_pow2(v) for v in (1, 2, 3, 5, 6, 5932, 5000, 23000, 23171, 32768)] == \
         [1, 2, 4, 4, 8, 8192, 4096, 16384, 32768, 32768]
+
+
+def test_cpu_baseline_sample_takes_whole_requests_until_the_budget():
+    calls = []
+
+    def fake(b):  # request b takes b + 1 seconds and moves 100 bytes
+        calls.append(b)
+        return 0.0, float(b + 1), 100
+
+    reqs, secs, nbytes = bench.cpu_baseline_sample(fake, 64, budget_s=10.0)
+    assert reqs == [0, 1, 2, 3] and calls == reqs      # 1 + 2 + 3 + 4 = 10 s
+    assert secs == 10.0 and nbytes == 400
+    reqs, secs, nbytes = bench.cpu_baseline_sample(fake, 2, budget_s=10.0)
+    assert reqs == [0, 1] and secs == 3.0            # the whole (small) batch
