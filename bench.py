@@ -519,6 +519,47 @@ def run_fd(args):
                                "t_auto_over_t_best": round(res[auto]["us"] / res[best]["us"], 3),
                                "timing": "CUDA graph of %d rotating calls, replayed" % n_rot}
 
+    # The step before the path: one launch rebuilds this batch's page table,
+    # lengths and cumulative lengths from a request-to-token pool (timed as a
+    # replayed CUDA graph of consecutive launches).
+    meta = None
+    if rank == 0:
+        pool_np, _ = wl.make_token_pool(seed, lengths, shape.page_size)
+        pool_t = torch.from_numpy(pool_np).to(dev)
+        idx_t = torch.arange(B, dtype=torch.int32, device=dev)
+        sl_t = torch.from_numpy(np.asarray(lengths, dtype=np.int32)).to(dev)
+        width = w.page_table.shape[1]
+        pt_t = torch.empty((B, width), dtype=torch.int32, device=dev)
+        cs_t = torch.empty(B, dtype=torch.int32, device=dev)
+        cuk_t = torch.empty(B + 1, dtype=torch.int32, device=dev)
+        cuq_t = torch.empty(B + 1, dtype=torch.int32, device=dev)
+        n_meta = 100
+
+        def meta_call():
+            fd.fd_graph_metadata(pool_t, idx_t, sl_t, shape.page_size, "strided", None, shape.q_per_req, pt_t, cs_t,
+                                 cuk_t, cuq_t)
+        cap_stream = torch.cuda.Stream()
+        cap_stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cap_stream):
+            meta_call()
+        torch.cuda.current_stream().wait_stream(cap_stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(n_meta):
+                meta_call()
+        graph.replay()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(5):
+            graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        meta = {"us_per_launch": round(e0.elapsed_time(e1) / (5 * n_meta) * 1e3, 2), "batch": B,
+                "page_table_width": int(width),
+                "what": "fd_graph_metadata: page_table, cache_seqlens, cu_seqlens_k / cu_seqlens_q of the batch "
+                        "from a request-to-token pool in one launch (CUDA graph of %d launches, replayed)" % n_meta}
+        del graph
+
     # CPU baseline: the oracle on a bounded sample of this workload, host cores
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -577,6 +618,7 @@ def run_fd(args):
         "gpu_launches": gpu_launches,
         "clocks": clk,
         "sweep": sweep,
+        "graph_metadata": meta,
     }
 
 
