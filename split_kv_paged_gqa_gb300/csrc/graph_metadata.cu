@@ -30,7 +30,7 @@ namespace fd {
 
 namespace {
 
-constexpr int kMetaThreads = 128;
+constexpr int kMetaThreads = 512;
 
 __device__ __forceinline__ int64_t load_index(const void *p, int is64, int64_t i) {
   return is64 ? static_cast<const int64_t *>(p)[i] : static_cast<const int *>(p)[i];
