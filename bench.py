@@ -13,9 +13,10 @@ disjoint copies of the inputs spanning at least 4x L2.
 Also reported on the same line: the roofline of the dominant kernel (stage 1,
 live CUDA-event timing of its launches), the CPU baseline (the float64 oracle
 on a bounded sample, host cores), an end-to-end number through the public
-binding with host buffers, SM clocks sampled during the timed region, and the
+binding with host buffers, SM clocks sampled during the timed region, the
 num_splits sweep for batch 1 / 16 / 64 with the autotuned pick against the
-sweep's best.
+sweep's best, and the time of the one-launch graph-metadata rebuild of the
+batch (outside the timed region).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fd|reference]
 Multi-GPU (torchrun): each rank decodes its own batch (weak scaling, no
