@@ -445,3 +445,17 @@ def test_force_is_adaptive_and_clear_searches_afresh(tmp_path, monkeypatch):
         assert len(calls) == 2 * first
     finally:
         fd.fd_plan_destroy(plan)
+
+
+def test_descriptor_reuse_matches_a_fresh_build():
+    # the binding reuses a descriptor only for the same pointer, dtype, shape and strides
+    t = torch.zeros(6, 4, 3, dtype=torch.bfloat16)
+    a, b = fd.make_descriptor(t), fd.make_descriptor(t)
+    assert a is b
+    v = t[:, 1:3]                                    # a view: other pointer, shape and strides
+    d = fd.make_descriptor(v)
+    assert d is not a
+    assert d.data == v.data_ptr() and d.ndim == 3
+    assert list(d.shape)[:3] == [6, 2, 3] and list(d.stride)[:3] == list(v.stride())
+    assert fd.make_descriptor(t.view(6, 12)).ndim == 2
+    assert fd.make_descriptor(None) is None
