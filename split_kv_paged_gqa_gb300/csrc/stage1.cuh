@@ -17,7 +17,9 @@
 //    of K and V into a STAGES-deep shared-memory ring, 128-byte swizzled,
 //    completing on a per-stage mbarrier. Quantised caches also copy their
 //    per-row fp32 scales with cp.async (one arrival per lane on the barrier).
-//  * consumer warps: warp w takes keys [16w, 16w + 16) of each 64-key stage.
+//  * consumer warps: warp w takes keys [KPW w, KPW w + KPW) of each stage of
+//    4 KPW keys (KPW = 16; 32 for the 16-row int4 variant, as two 16-key
+//    sub-blocks that share one softmax step).
 //    QK^T and PV run on mma.sync m16n8k16 (fp32 accumulate) with the 16 query
 //    rows as M; the online softmax keeps a running max / sum per row in the
 //    log2 domain with quad shuffles. bf16 caches feed ldmatrix fragments
@@ -74,10 +76,14 @@ struct S1Cfg {
   static constexpr int BOX_ELEMS = KIND == KV_BF16 ? BOX_BYTES / 2 : BOX_BYTES;
   static constexpr int NG = KIND == KV_I4 ? D / 32 : 1;  // fp32 scales per cache row
   static constexpr int NT = D / 8;                       // PV n-tiles (channels per thread, quantised V)
-  // keys per pipeline stage; the deep (one CTA per SM) variant doubles the
-  // consumer warps so a lone CTA has more blocks in flight
-  static constexpr int BLOCK_N = DEEP ? 128 : 64;
-  static constexpr int NUM_CW = BLOCK_N / 16;            // consumer warps (16 keys each)
+  // consumer warps; the deep (one CTA per SM) variant doubles them so a lone
+  // CTA has more blocks in flight
+  static constexpr int NUM_CW = DEEP ? 8 : 4;
+  // keys per consumer warp and stage: 16, or 32 for the 16-row int4 variant
+  // (two 16-key sub-blocks share one softmax step and one round trip of O
+  // through tensor memory, and their MMA chains interleave)
+  static constexpr int KPW = KIND == KV_I4 && !NARROW && !DEEP ? 32 : 16;
+  static constexpr int BLOCK_N = NUM_CW * KPW;           // keys per pipeline stage
   static constexpr int SEG_MAX = 64;                     // slots per TMA box at most
   static constexpr int THREADS = (NUM_CW + 1) * 32;
   // DEEP: one CTA per SM with 8 consumer warps and 64 KB stages, for grids
@@ -87,7 +93,7 @@ struct S1Cfg {
   // flight: the 16-row variants run three CTAs per SM (128 registers), the
   // narrow ones four (96 registers), on rings that fit.
   static constexpr bool FOUR = NARROW;
-  static constexpr int STAGES = KIND == KV_BF16 ? 3 : (KIND == KV_I8 ? (FOUR ? 2 : 3) : (FOUR ? 4 : 6));
+  static constexpr int STAGES = KIND == KV_BF16 ? 3 : (KIND == KV_I8 ? (FOUR ? 2 : 3) : (FOUR ? 4 : 6 * 16 / KPW));
   // Quantised kinds park the (identical) Q fragments of the consumer warps in
   // shared memory and reload them per block, so they do not hold 32 (narrow:
   // 16) registers through the PV half of the loop.
@@ -287,7 +293,50 @@ __device__ __forceinline__ void softmax_update(const float (&s)[2][4], float (&p
 }
 
 // ----------------------------------------------------------------------------
-// One 16-key block of one warp, quantised cache, straight from the raw tile.
+// Online-softmax update (as softmax_update) over KB 16-key sub-blocks that
+// share one row max: the thread's scores s[kb][nt][e] of rows g (e < 2) and
+// g + 8 (e >= 2).
+template <int KB>
+__device__ __forceinline__ void softmax_update_kb(const float (&s)[KB][2][4], float (&p)[KB][2][4],
+                                                  float (&m)[2], float (&l)[2], float (&al)[2]) {
+  float mx0 = fmaxf(fmaxf(s[0][0][0], s[0][0][1]), fmaxf(s[0][1][0], s[0][1][1]));
+  float mx1 = fmaxf(fmaxf(s[0][0][2], s[0][0][3]), fmaxf(s[0][1][2], s[0][1][3]));
+#pragma unroll
+  for (int kb = 1; kb < KB; ++kb) {
+    mx0 = fmaxf(mx0, fmaxf(fmaxf(s[kb][0][0], s[kb][0][1]), fmaxf(s[kb][1][0], s[kb][1][1])));
+    mx1 = fmaxf(mx1, fmaxf(fmaxf(s[kb][0][2], s[kb][0][3]), fmaxf(s[kb][1][2], s[kb][1][3])));
+  }
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+  const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+  const float b0 = mn0 == -INFINITY ? 0.f : mn0;
+  const float b1 = mn1 == -INFINITY ? 0.f : mn1;
+  al[0] = fast_exp2(m[0] - b0);
+  al[1] = fast_exp2(m[1] - b1);
+  m[0] = mn0;
+  m[1] = mn1;
+  float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+  for (int kb = 0; kb < KB; ++kb) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      p[kb][nt][0] = fast_exp2(s[kb][nt][0] - b0);
+      p[kb][nt][1] = fast_exp2(s[kb][nt][1] - b0);
+      p[kb][nt][2] = fast_exp2(s[kb][nt][2] - b1);
+      p[kb][nt][3] = fast_exp2(s[kb][nt][3] - b1);
+    }
+    sum0 += p[kb][0][0] + p[kb][0][1] + p[kb][1][0] + p[kb][1][1];
+    sum1 += p[kb][0][2] + p[kb][0][3] + p[kb][1][2] + p[kb][1][3];
+  }
+  l[0] = l[0] * al[0] + sum0;
+  l[1] = l[1] * al[1] + sum1;
+}
+
+// ----------------------------------------------------------------------------
+// One block of C::KPW keys (KB = KPW / 16 sub-blocks of 16 sharing one
+// softmax step) of one warp, quantised cache, straight from the raw tile.
 //
 // kt / vt: the stage's raw K / V tiles (rows of ROW_BYTES, TMA-swizzled with
 // span BOX_BYTES); ksc / vsc: the stage's per-row fp32 scales (NG per row).
@@ -302,7 +351,8 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
                                              float (&o)[C::NT][4], uint32_t tm_o, float (&m)[2], float (&l)[2],
                                              int tok_row0, int c1, int lim0, int lim1, int lane) {
   constexpr int NG = C::NG, RB = C::ROW_BYTES, SW = C::BOX_BYTES, NT = C::NT;
-  constexpr int CH = RB / 16;  // 16-byte chunks per cache row
+  constexpr int KB = C::KPW / 16;  // 16-key sub-blocks
+  constexpr int CH = RB / 16;      // 16-byte chunks per cache row
   const int g = lane >> 2, c = lane & 3;
   const int mi = lane >> 3, ri = lane & 7;
   const uint32_t kbase = smem_u32(kt);
@@ -311,91 +361,111 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
   // ---- S = Q K^T in fp16 with biased K codes. Each 16-byte chunk of a K row
   // is one scale group for int4 (32 channels); its accumulator is folded into
   // the scores as soon as its products are done: sv = sum_g ks_g (acc_g - c_g).
-  float sv[2][4];
+  // The sub-blocks' products are independent: their MMA chains interleave.
+  float sv[KB][2][4];
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
+  for (int kb = 0; kb < KB; ++kb)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) sv[nt][e] = 0.f;
-  float acc8[2][4];  // int8: one accumulator over all chunks, starting at -bias
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
+      for (int e = 0; e < 4; ++e) sv[kb][nt][e] = 0.f;
+  float acc8[KB][2][4];  // int8: one accumulator over all chunks, starting at -bias
 #pragma unroll
-    for (int e = 0; e < 4; ++e) acc8[nt][e] = KIND == KV_I8 ? -qc[e >> 1][0] : 0.f;
+  for (int kb = 0; kb < KB; ++kb)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc8[kb][nt][e] = KIND == KV_I8 ? -qc[e >> 1][0] : 0.f;
   const int krow = row0 + ((mi >> 1) << 3) + ri;
 #pragma unroll
   for (int kc = 0; kc < CH; kc += 2) {
-    uint32_t r[4];  // (n-tile 0, chunk kc), (n-tile 0, kc+1), (n-tile 1, kc), (n-tile 1, kc+1)
-    ldsm_x4(r, kbase + swz<SW>(krow * RB + (kc + (mi & 1)) * 16));
+    uint32_t r[KB][4];  // (n-tile 0, chunk kc), (n-tile 0, kc+1), (n-tile 1, kc), (n-tile 1, kc+1)
+#pragma unroll
+    for (int kb = 0; kb < KB; ++kb) ldsm_x4(r[kb], kbase + swz<SW>((krow + 16 * kb) * RB + (kc + (mi & 1)) * 16));
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int ch = kc + hh;
       if constexpr (KIND == KV_I8) {
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const uint32_t x = r[nt * 2 + hh] ^ 0x80808080u;  // bytes u = code + 128
-          mma_f16_16816(acc8[nt], qa[ch], __byte_perm(x, 0x64646464u, 0x5140),
-                        __byte_perm(x, 0x64646464u, 0x7362));
-        }
-      } else {
-        float acc[2][4];  // this group's products, starting at -bias
+        for (int kb = 0; kb < KB; ++kb)
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[nt][e] = -qc[e >> 1][ch];
-          // raw nibble k (= code & 15) is channel 32ch + 8c + k; masking it
-          // and XOR-ing in 8 and the exponent of 1024 is one LOP3 per pair
-          const uint32_t x = r[nt * 2 + hh];
-          const uint32_t y = x >> 8;
-          mma_f16_16816(acc[nt], qa[2 * ch], nib_lo_f16_biased(x, nib_lo), nib_lo_f16_biased(y, nib_lo));
-          mma_f16_16816(acc[nt], qa[2 * ch + 1], nib_hi_f16_biased(x, nib_hi), nib_hi_f16_biased(y, nib_hi));
-        }
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int key = nt * 8 + 2 * c + (e & 1);
-            sv[nt][e] = fmaf(acc[nt][e], ksc[(row0 + key) * NG + ch], sv[nt][e]);
+          for (int nt = 0; nt < 2; ++nt) {
+            const uint32_t x = r[kb][nt * 2 + hh] ^ 0x80808080u;  // bytes u = code + 128
+            mma_f16_16816(acc8[kb][nt], qa[ch], __byte_perm(x, 0x64646464u, 0x5140),
+                          __byte_perm(x, 0x64646464u, 0x7362));
           }
+      } else {
+        float acc[KB][2][4];  // this group's products, starting at -bias
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[kb][nt][e] = -qc[e >> 1][ch];
+            // raw nibble k (= code & 15) is channel 32ch + 8c + k; masking it
+            // and XOR-ing in 8 and the exponent of 1024 is one LOP3 per pair
+            const uint32_t x = r[kb][nt * 2 + hh];
+            const uint32_t y = x >> 8;
+            mma_f16_16816(acc[kb][nt], qa[2 * ch], nib_lo_f16_biased(x, nib_lo), nib_lo_f16_biased(y, nib_lo));
+            mma_f16_16816(acc[kb][nt], qa[2 * ch + 1], nib_hi_f16_biased(x, nib_hi),
+                          nib_hi_f16_biased(y, nib_hi));
+          }
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int key = 16 * kb + nt * 8 + 2 * c + (e & 1);
+              sv[kb][nt][e] = fmaf(acc[kb][nt][e], ksc[(row0 + key) * NG + ch], sv[kb][nt][e]);
+            }
       }
     }
   }
   if constexpr (KIND == KV_I8) {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int kb = 0; kb < KB; ++kb)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = nt * 8 + 2 * c + (e & 1);
-        sv[nt][e] = acc8[nt][e] * ksc[row0 + key];
-      }
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = 16 * kb + nt * 8 + 2 * c + (e & 1);
+          sv[kb][nt][e] = acc8[kb][nt][e] * ksc[row0 + key];
+        }
   }
 
-  // ---- row scale, mask by selection (a block whose 16 keys every row of the
+  // ---- row scale, mask by selection (a block whose keys every row of the
   // warp sees, which is every block but a split's last, needs no selection)
-  const bool full = __all_sync(0xffffffffu, tok_row0 + 16 <= min(lim0, lim1));
-  float s[2][4];
+  const bool full = __all_sync(0xffffffffu, tok_row0 + C::KPW <= min(lim0, lim1));
+  float s[KB][2][4];
   if (full) {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int kb = 0; kb < KB; ++kb)
 #pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const float2 r2 = __fmul2_rn(make_float2(sv[nt][2 * hr], sv[nt][2 * hr + 1]), make_float2(rs[hr], rs[hr]));
-        s[nt][2 * hr] = r2.x;
-        s[nt][2 * hr + 1] = r2.y;
-      }
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const float2 r2 = __fmul2_rn(make_float2(sv[kb][nt][2 * hr], sv[kb][nt][2 * hr + 1]),
+                                       make_float2(rs[hr], rs[hr]));
+          s[kb][nt][2 * hr] = r2.x;
+          s[kb][nt][2 * hr + 1] = r2.y;
+        }
   } else {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
+    for (int kb = 0; kb < KB; ++kb)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = nt * 8 + 2 * c + (e & 1);
-        const int hr = e >> 1;
-        const int lim = hr ? lim1 : lim0;
-        s[nt][e] = (tok_row0 + key < lim) ? sv[nt][e] * rs[hr] : -INFINITY;
+      for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = 16 * kb + nt * 8 + 2 * c + (e & 1);
+          const int hr = e >> 1;
+          const int lim = hr ? lim1 : lim0;
+          s[kb][nt][e] = (tok_row0 + key < lim) ? sv[kb][nt][e] * rs[hr] : -INFINITY;
+        }
       }
-    }
   }
-  float p[2][4], al[2];
-  softmax_update(s, p, m, l, al);
+  float p[KB][2][4], al[2];
+  softmax_update_kb<KB>(s, p, m, l, al);
   const bool rescale = __any_sync(0xffffffffu, al[0] != 1.f || al[1] != 1.f);
   // alpha-rescale of O if the max moved
   auto rescale_o = [&](float (&oo)[NT][4]) {
@@ -412,72 +482,86 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
   if constexpr (!C::O_TMEM) rescale_o(o);  // (O in tensor memory is rescaled once loaded)
 
   // ---- P as the fp16 A operand (int8: the per-key V scale folded in)
-  uint32_t pa[4];
-  if constexpr (KIND == KV_I8) {
-    float pv[2][4];
+  uint32_t pa[KB][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+  for (int kb = 0; kb < KB; ++kb) {
+    if constexpr (KIND == KV_I8) {
+      float pv[2][4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float vs = vsc[row0 + nt * 8 + 2 * c + (e & 1)];
-        pv[nt][e] = p[nt][e] == 0.f ? 0.f : p[nt][e] * vs;
-      }
-    pa[0] = pack_f16x2(pv[0][0], pv[0][1]);
-    pa[1] = pack_f16x2(pv[0][2], pv[0][3]);
-    pa[2] = pack_f16x2(pv[1][0], pv[1][1]);
-    pa[3] = pack_f16x2(pv[1][2], pv[1][3]);
-  } else {
-    pa[0] = pack_f16x2(p[0][0], p[0][1]);
-    pa[1] = pack_f16x2(p[0][2], p[0][3]);
-    pa[2] = pack_f16x2(p[1][0], p[1][1]);
-    pa[3] = pack_f16x2(p[1][2], p[1][3]);
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float vs = vsc[row0 + 16 * kb + nt * 8 + 2 * c + (e & 1)];
+          pv[nt][e] = p[kb][nt][e] == 0.f ? 0.f : p[kb][nt][e] * vs;
+        }
+      pa[kb][0] = pack_f16x2(pv[0][0], pv[0][1]);
+      pa[kb][1] = pack_f16x2(pv[0][2], pv[0][3]);
+      pa[kb][2] = pack_f16x2(pv[1][0], pv[1][1]);
+      pa[kb][3] = pack_f16x2(pv[1][2], pv[1][3]);
+    } else {
+      pa[kb][0] = pack_f16x2(p[kb][0][0], p[kb][0][1]);
+      pa[kb][1] = pack_f16x2(p[kb][0][2], p[kb][0][3]);
+      pa[kb][2] = pack_f16x2(p[kb][1][0], p[kb][1][1]);
+      pa[kb][3] = pack_f16x2(p[kb][1][2], p[kb][1][3]);
+    }
   }
 
-  // ---- V fragments: keys (2c, 2c+1) -> b0b1, (2c+8, 2c+9) -> b2b3, channels
-  // [g*NT, g*NT + NT), one channel per n-tile. Keys at or past c1 read as 0.
-  const int kA = row0 + 2 * c, kB = kA + 8;
-  const int vrows[4] = {kA, kA + 1, kB, kB + 1};
-  bool valid[4];
+  // ---- V fragments: keys (2c, 2c+1) -> b0b1, (2c+8, 2c+9) -> b2b3 of each
+  // sub-block, channels [g*NT, g*NT + NT), one channel per n-tile. Keys at or
+  // past c1 read as 0.
+  int vrows[KB][4];
+  bool valid[KB][4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) valid[i] = full || tok_row0 + (vrows[i] - row0) < c1;
+  for (int kb = 0; kb < KB; ++kb) {
+    const int kA = row0 + 16 * kb + 2 * c, kB = kA + 8;
+    vrows[kb][0] = kA;
+    vrows[kb][1] = kA + 1;
+    vrows[kb][2] = kB;
+    vrows[kb][3] = kB + 1;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) valid[kb][i] = full || tok_row0 + (vrows[kb][i] - row0) < c1;
+  }
   if constexpr (KIND == KV_I8) {
     static_assert(NT % 4 == 0, "int8 V words");
     static_assert(!C::O_TMEM, "int8 keeps O in registers");
     constexpr int NW = NT / 4;  // 32-bit words per key
-    uint32_t w[4][NW];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint8_t *src = vt + swz<SW>(vrows[i] * RB + g * NT);
-      if constexpr (NW == 4) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(src);
-        w[i][0] = v.x;
-        w[i][1] = v.y;
-        w[i][2] = v.z;
-        w[i][3] = v.w;
-      } else {
-        const uint2 v = *reinterpret_cast<const uint2 *>(src);
-        w[i][0] = v.x;
-        w[i][1] = v.y;
+    for (int kb = 0; kb < KB; ++kb) {
+      uint32_t w[4][NW];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint8_t *src = vt + swz<SW>(vrows[kb][i] * RB + g * NT);
+        if constexpr (NW == 4) {
+          const uint4 v = *reinterpret_cast<const uint4 *>(src);
+          w[i][0] = v.x;
+          w[i][1] = v.y;
+          w[i][2] = v.z;
+          w[i][3] = v.w;
+        } else {
+          const uint2 v = *reinterpret_cast<const uint2 *>(src);
+          w[i][0] = v.x;
+          w[i][1] = v.y;
+        }
       }
-    }
-    if (!full) {  // keys past the split end read as code 0 (a raw 0)
+      if (!full) {  // keys past the split end read as code 0 (a raw 0)
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int k = 0; k < NW; ++k) w[i][k] = valid[i] ? w[i][k] : 0u;
-    }
-    const uint32_t u8_bias = kU8Bias;
+          for (int k = 0; k < NW; ++k) w[i][k] = valid[kb][i] ? w[i][k] : 0u;
+      }
+      const uint32_t u8_bias = kU8Bias;
 #pragma unroll
-    for (int k = 0; k < NW; ++k) {
+      for (int k = 0; k < NW; ++k) {
 #pragma unroll
-      for (int bi = 0; bi < 4; ++bi) {
-        // byte bi of both keys -> bits 0-7 and 16-23: channel g*NT + 4k + bi
-        const uint32_t sel = (bi) | (bi << 4) | ((4u + bi) << 8) | ((4u + bi) << 12);
-        const uint32_t b0 =
-            hsub2_u32(i8pair_to_f16_biased(__byte_perm(w[0][k], w[1][k], sel), u8_bias), 1152.0f);
-        const uint32_t b1 =
-            hsub2_u32(i8pair_to_f16_biased(__byte_perm(w[2][k], w[3][k], sel), u8_bias), 1152.0f);
-        mma_f16_16816(o[4 * k + bi], pa, b0, b1);
+        for (int bi = 0; bi < 4; ++bi) {
+          // byte bi of both keys -> bits 0-7 and 16-23: channel g*NT + 4k + bi
+          const uint32_t sel = (bi) | (bi << 4) | ((4u + bi) << 8) | ((4u + bi) << 12);
+          const uint32_t b0 =
+              hsub2_u32(i8pair_to_f16_biased(__byte_perm(w[0][k], w[1][k], sel), u8_bias), 1152.0f);
+          const uint32_t b1 =
+              hsub2_u32(i8pair_to_f16_biased(__byte_perm(w[2][k], w[3][k], sel), u8_bias), 1152.0f);
+          mma_f16_16816(o[4 * k + bi], pa[kb], b0, b1);
+        }
       }
     }
   } else {
@@ -492,42 +576,49 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
 #pragma unroll
     for (int i = 0; i < NT / 8; ++i) tmem_ld32(tm_o + 32 * i, &ot[8 * i][0]);
     const int grp = (g * NT) / 32;
-    uint32_t w[4][NW];
-    float vsf[4];
+    uint32_t w[KB][4][NW];
+    uint32_t sA[KB], sB[KB];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint8_t *src = vt + swz<SW>(vrows[i] * RB + g * (NT / 2));
-      if constexpr (NW == 2) {
-        const uint2 v = *reinterpret_cast<const uint2 *>(src);
-        w[i][0] = v.x;
-        w[i][1] = v.y;
-      } else {
-        w[i][0] = *reinterpret_cast<const uint32_t *>(src);
+    for (int kb = 0; kb < KB; ++kb) {
+      float vsf[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint8_t *src = vt + swz<SW>(vrows[kb][i] * RB + g * (NT / 2));
+        if constexpr (NW == 2) {
+          const uint2 v = *reinterpret_cast<const uint2 *>(src);
+          w[kb][i][0] = v.x;
+          w[kb][i][1] = v.y;
+        } else {
+          w[kb][i][0] = *reinterpret_cast<const uint32_t *>(src);
+        }
+        vsf[i] = valid[kb][i] ? vsc[vrows[kb][i] * NG + grp] : 0.f;
       }
-      vsf[i] = valid[i] ? vsc[vrows[i] * NG + grp] : 0.f;
+      sA[kb] = pack_f16x2(vsf[0], vsf[1]);
+      sB[kb] = pack_f16x2(vsf[2], vsf[3]);
     }
-    const uint32_t sA = pack_f16x2(vsf[0], vsf[1]);
-    const uint32_t sB = pack_f16x2(vsf[2], vsf[3]);
     tmem_wait_ld();
     rescale_o(ot);
 #pragma unroll
-    for (int k = 0; k < NW; ++k) {
+    for (int kb = 0; kb < KB; ++kb) {
 #pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {  // bytes 0-1, then 2-3, of each key's word
-        const uint32_t sel = hb ? 0x7632u : 0x5410u;
-        const uint32_t tA = __byte_perm(w[0][k], w[1][k], sel);
-        const uint32_t tB = __byte_perm(w[2][k], w[3][k], sel);
+      for (int k = 0; k < NW; ++k) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {  // nibble q: channel g*NT + 8k + 4hb + q
-          uint32_t xa, xb;
-          if (q & 1) {  // high nibble reads 1024 + 16u: /16 - 72 = code
-            xa = hfma2_u32(nib_hi_f16_biased(tA >> (4 * (q - 1)), nib_hi), 1.0f / 16.0f, -72.0f);
-            xb = hfma2_u32(nib_hi_f16_biased(tB >> (4 * (q - 1)), nib_hi), 1.0f / 16.0f, -72.0f);
-          } else {
-            xa = hsub2_u32(nib_lo_f16_biased(tA >> (4 * q), nib_lo), 1032.0f);
-            xb = hsub2_u32(nib_lo_f16_biased(tB >> (4 * q), nib_lo), 1032.0f);
+        for (int hb = 0; hb < 2; ++hb) {  // bytes 0-1, then 2-3, of each key's word
+          const uint32_t sel = hb ? 0x7632u : 0x5410u;
+          const uint32_t tA = __byte_perm(w[kb][0][k], w[kb][1][k], sel);
+          const uint32_t tB = __byte_perm(w[kb][2][k], w[kb][3][k], sel);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {  // nibble q: channel g*NT + 8k + 4hb + q
+            uint32_t xa, xb;
+            if (q & 1) {  // high nibble reads 1024 + 16u: /16 - 72 = code
+              xa = hfma2_u32(nib_hi_f16_biased(tA >> (4 * (q - 1)), nib_hi), 1.0f / 16.0f, -72.0f);
+              xb = hfma2_u32(nib_hi_f16_biased(tB >> (4 * (q - 1)), nib_hi), 1.0f / 16.0f, -72.0f);
+            } else {
+              xa = hsub2_u32(nib_lo_f16_biased(tA >> (4 * q), nib_lo), 1032.0f);
+              xb = hsub2_u32(nib_lo_f16_biased(tB >> (4 * q), nib_lo), 1032.0f);
+            }
+            mma_f16_16816(ot[8 * k + 4 * hb + q], pa[kb], hmul2_u32(xa, sA[kb]), hmul2_u32(xb, sB[kb]));
           }
-          mma_f16_16816(ot[8 * k + 4 * hb + q], pa, hmul2_u32(xa, sA), hmul2_u32(xb, sB));
         }
       }
     }
@@ -1314,7 +1405,7 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
     }
     float m[2] = {-INFINITY, -INFINITY};
     float l[2] = {0.f, 0.f};
-    const int row0 = warp * 16;
+    const int row0 = warp * C::KPW;  // the warp's first key in each stage
 
     for (int it = 0; it < n_iters; ++it) {
       const int stage = it % C::STAGES;
