@@ -82,7 +82,7 @@ struct S1Cfg {
   // keys per consumer warp and stage: 16, or 32 for the 16-row int4 variant
   // (two 16-key sub-blocks share one softmax step and one round trip of O
   // through tensor memory, and their MMA chains interleave)
-  static constexpr int KPW = KIND == KV_I4 && !NARROW && !DEEP ? 32 : 16;
+  static constexpr int KPW = (KIND == KV_I4 && !NARROW && !DEEP) || (KIND == KV_I8 && NARROW) ? 32 : 16;
   static constexpr int BLOCK_N = NUM_CW * KPW;           // keys per pipeline stage
   static constexpr int SEG_MAX = 64;                     // slots per TMA box at most
   static constexpr int THREADS = (NUM_CW + 1) * 32;
@@ -93,7 +93,7 @@ struct S1Cfg {
   // flight: the 16-row variants run three CTAs per SM (128 registers), the
   // narrow ones four (96 registers), on rings that fit.
   static constexpr bool FOUR = NARROW;
-  static constexpr int STAGES = KIND == KV_BF16 ? 3 : (KIND == KV_I8 ? (FOUR ? 2 : 3) : (FOUR ? 4 : 6 * 16 / KPW));
+  static constexpr int STAGES = KIND == KV_BF16 ? 3 : (KIND == KV_I8 ? (FOUR ? 2 : 3) : (FOUR ? 4 : 6) * 16 / KPW);
   // Quantised kinds park the (identical) Q fragments of the consumer warps in
   // shared memory and reload them per block, so they do not hold 32 (narrow:
   // 16) registers through the PV half of the loop.
@@ -628,9 +628,10 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
 }
 
 // ----------------------------------------------------------------------------
-// One 16-key block of one warp, quantised cache, for tiles of at most 8 query
-// rows ("narrow"). The 16 keys are the M dimension of the MMAs and the rows
-// the 8-wide N dimension, so no tile is mostly padding:
+// One block of C::KPW keys (KB = KPW / 16 sub-blocks of 16 sharing one
+// softmax step) of one warp, quantised cache, for tiles of at most 8 query
+// rows ("narrow"). The 16 keys of a sub-block are the M dimension of the MMAs
+// and the rows the 8-wide N dimension, so no tile is mostly padding:
 //   S^T (16 keys x 8 rows)  = K (keys x channels) Q^T,
 //   O^T (16 channels x 8 rows) += V^T (channels x keys) P^T.
 // The K codes become A fragments straight from ldmatrix, in the channel order
@@ -649,65 +650,91 @@ __device__ __forceinline__ void warp_block_km(const uint8_t *kt, const uint8_t *
                                               float (&o)[C::OT][4], float (&m)[2], float (&l)[2], int tok_row0,
                                               int c1, int lim0, int lim1, int lane) {
   constexpr int NG = C::NG, RB = C::ROW_BYTES, SW = C::BOX_BYTES, NT = C::NT;
-  constexpr int CH = RB / 16;  // 16-byte chunks per cache row
+  constexpr int KB = C::KPW / 16;  // 16-key sub-blocks
+  constexpr int CH = RB / 16;      // 16-byte chunks per cache row
   const int g = lane >> 2, c = lane & 3;
   const int mi = lane >> 3, ri = lane & 7;
   const uint32_t kbase = smem_u32(kt);
   const uint32_t nib_lo = kNibLo, nib_hi = kNibHi;
 
-  // ---- S^T = K Q^T: sv = (key g, row 2c), (g, 2c+1), (g+8, 2c), (g+8, 2c+1)
-  float sv[4] = {0.f, 0.f, 0.f, 0.f};
-  float acc8[4] = {-qc[0][0], -qc[1][0], -qc[0][0], -qc[1][0]};  // int8: from -bias
+  // ---- S^T = K Q^T: sv[kb] = (key g, row 2c), (g, 2c+1), (g+8, 2c), (g+8, 2c+1)
+  float sv[KB][4];
+  float acc8[KB][4];  // int8: from -bias
+#pragma unroll
+  for (int kb = 0; kb < KB; ++kb) {
+    sv[kb][0] = sv[kb][1] = sv[kb][2] = sv[kb][3] = 0.f;
+    acc8[kb][0] = acc8[kb][2] = -qc[0][0];
+    acc8[kb][1] = acc8[kb][3] = -qc[1][0];
+  }
   const int krow = row0 + ((mi >> 1) << 3) + ri;
 #pragma unroll
   for (int kc = 0; kc < CH; kc += 2) {
-    uint32_t r[4];  // (key g, chunk kc), (key g, kc + 1), (key g + 8, kc), (key g + 8, kc + 1)
-    ldsm_x4(r, kbase + swz<SW>(krow * RB + (kc + (mi & 1)) * 16));
+    uint32_t r[KB][4];  // (key g, chunk kc), (key g, kc + 1), (key g + 8, kc), (key g + 8, kc + 1)
+#pragma unroll
+    for (int kb = 0; kb < KB; ++kb) ldsm_x4(r[kb], kbase + swz<SW>((krow + 16 * kb) * RB + (kc + (mi & 1)) * 16));
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int ch = kc + hh;
-      if constexpr (KIND == KV_I8) {
-        const uint32_t xg = r[hh] ^ 0x80808080u, x8 = r[2 + hh] ^ 0x80808080u;  // bytes u = code + 128
-        const uint32_t a[4] = {__byte_perm(xg, 0x64646464u, 0x5140), __byte_perm(x8, 0x64646464u, 0x5140),
-                               __byte_perm(xg, 0x64646464u, 0x7362), __byte_perm(x8, 0x64646464u, 0x7362)};
-        mma_f16_16816(acc8, a, qb[ch][0], qb[ch][1]);
-      } else {
-        float acc[4] = {-qc[0][ch], -qc[1][ch], -qc[0][ch], -qc[1][ch]};
-        const uint32_t xg = r[hh], x8 = r[2 + hh];
-        const uint32_t yg = xg >> 8, y8 = x8 >> 8;
-        const uint32_t alo[4] = {nib_lo_f16_biased(xg, nib_lo), nib_lo_f16_biased(x8, nib_lo),
-                                 nib_lo_f16_biased(yg, nib_lo), nib_lo_f16_biased(y8, nib_lo)};
-        const uint32_t ahi[4] = {nib_hi_f16_biased(xg, nib_hi), nib_hi_f16_biased(x8, nib_hi),
-                                 nib_hi_f16_biased(yg, nib_hi), nib_hi_f16_biased(y8, nib_hi)};
-        mma_f16_16816(acc, alo, qb[2 * ch][0], qb[2 * ch][1]);
-        mma_f16_16816(acc, ahi, qb[2 * ch + 1][0], qb[2 * ch + 1][1]);
-        const float kg = ksc[(row0 + g) * NG + ch], k8 = ksc[(row0 + g + 8) * NG + ch];
-        sv[0] = fmaf(acc[0], kg, sv[0]);
-        sv[1] = fmaf(acc[1], kg, sv[1]);
-        sv[2] = fmaf(acc[2], k8, sv[2]);
-        sv[3] = fmaf(acc[3], k8, sv[3]);
+#pragma unroll
+      for (int kb = 0; kb < KB; ++kb) {
+        if constexpr (KIND == KV_I8) {
+          const uint32_t xg = r[kb][hh] ^ 0x80808080u, x8 = r[kb][2 + hh] ^ 0x80808080u;  // bytes u = code + 128
+          const uint32_t a[4] = {__byte_perm(xg, 0x64646464u, 0x5140), __byte_perm(x8, 0x64646464u, 0x5140),
+                                 __byte_perm(xg, 0x64646464u, 0x7362), __byte_perm(x8, 0x64646464u, 0x7362)};
+          mma_f16_16816(acc8[kb], a, qb[ch][0], qb[ch][1]);
+        } else {
+          float acc[4] = {-qc[0][ch], -qc[1][ch], -qc[0][ch], -qc[1][ch]};
+          const uint32_t xg = r[kb][hh], x8 = r[kb][2 + hh];
+          const uint32_t yg = xg >> 8, y8 = x8 >> 8;
+          const uint32_t alo[4] = {nib_lo_f16_biased(xg, nib_lo), nib_lo_f16_biased(x8, nib_lo),
+                                   nib_lo_f16_biased(yg, nib_lo), nib_lo_f16_biased(y8, nib_lo)};
+          const uint32_t ahi[4] = {nib_hi_f16_biased(xg, nib_hi), nib_hi_f16_biased(x8, nib_hi),
+                                   nib_hi_f16_biased(yg, nib_hi), nib_hi_f16_biased(y8, nib_hi)};
+          mma_f16_16816(acc, alo, qb[2 * ch][0], qb[2 * ch][1]);
+          mma_f16_16816(acc, ahi, qb[2 * ch + 1][0], qb[2 * ch + 1][1]);
+          const float kg = ksc[(row0 + 16 * kb + g) * NG + ch], k8 = ksc[(row0 + 16 * kb + g + 8) * NG + ch];
+          sv[kb][0] = fmaf(acc[0], kg, sv[kb][0]);
+          sv[kb][1] = fmaf(acc[1], kg, sv[kb][1]);
+          sv[kb][2] = fmaf(acc[2], k8, sv[kb][2]);
+          sv[kb][3] = fmaf(acc[3], k8, sv[kb][3]);
+        }
       }
     }
   }
   if constexpr (KIND == KV_I8) {
-    const float kg = ksc[row0 + g], k8 = ksc[row0 + g + 8];
-    sv[0] = acc8[0] * kg;
-    sv[1] = acc8[1] * kg;
-    sv[2] = acc8[2] * k8;
-    sv[3] = acc8[3] * k8;
+#pragma unroll
+    for (int kb = 0; kb < KB; ++kb) {
+      const float kg = ksc[row0 + 16 * kb + g], k8 = ksc[row0 + 16 * kb + g + 8];
+      sv[kb][0] = acc8[kb][0] * kg;
+      sv[kb][1] = acc8[kb][1] * kg;
+      sv[kb][2] = acc8[kb][2] * k8;
+      sv[kb][3] = acc8[kb][3] * k8;
+    }
   }
 
   // ---- row scale, mask by selection, online softmax (rows 2c, 2c + 1)
-  const bool full = __all_sync(0xffffffffu, tok_row0 + 16 <= min(lim0, lim1));
-  float s[4] = {sv[0] * rs[0], sv[1] * rs[1], sv[2] * rs[0], sv[3] * rs[1]};
-  if (!full) {
-    const int kg = tok_row0 + g, k8 = kg + 8;
-    if (kg >= lim0) s[0] = -INFINITY;
-    if (kg >= lim1) s[1] = -INFINITY;
-    if (k8 >= lim0) s[2] = -INFINITY;
-    if (k8 >= lim1) s[3] = -INFINITY;
+  const bool full = __all_sync(0xffffffffu, tok_row0 + C::KPW <= min(lim0, lim1));
+  float s[KB][4];
+#pragma unroll
+  for (int kb = 0; kb < KB; ++kb) {
+    s[kb][0] = sv[kb][0] * rs[0];
+    s[kb][1] = sv[kb][1] * rs[1];
+    s[kb][2] = sv[kb][2] * rs[0];
+    s[kb][3] = sv[kb][3] * rs[1];
+    if (!full) {
+      const int kg = tok_row0 + 16 * kb + g, k8 = kg + 8;
+      if (kg >= lim0) s[kb][0] = -INFINITY;
+      if (kg >= lim1) s[kb][1] = -INFINITY;
+      if (k8 >= lim0) s[kb][2] = -INFINITY;
+      if (k8 >= lim1) s[kb][3] = -INFINITY;
+    }
   }
-  float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+  float mx0 = fmaxf(s[0][0], s[0][2]), mx1 = fmaxf(s[0][1], s[0][3]);
+#pragma unroll
+  for (int kb = 1; kb < KB; ++kb) {
+    mx0 = fmaxf(mx0, fmaxf(s[kb][0], s[kb][2]));
+    mx1 = fmaxf(mx1, fmaxf(s[kb][1], s[kb][3]));
+  }
 #pragma unroll
   for (int x = 4; x < 32; x <<= 1) {
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
@@ -719,9 +746,19 @@ __device__ __forceinline__ void warp_block_km(const uint8_t *kt, const uint8_t *
   const float al0 = fast_exp2(m[0] - b0), al1 = fast_exp2(m[1] - b1);
   m[0] = mn0;
   m[1] = mn1;
-  float p[4] = {fast_exp2(s[0] - b0), fast_exp2(s[1] - b1), fast_exp2(s[2] - b0), fast_exp2(s[3] - b1)};
-  l[0] = fmaf(l[0], al0, p[0] + p[2]);
-  l[1] = fmaf(l[1], al1, p[1] + p[3]);
+  float p[KB][4];
+  float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+  for (int kb = 0; kb < KB; ++kb) {
+    p[kb][0] = fast_exp2(s[kb][0] - b0);
+    p[kb][1] = fast_exp2(s[kb][1] - b1);
+    p[kb][2] = fast_exp2(s[kb][2] - b0);
+    p[kb][3] = fast_exp2(s[kb][3] - b1);
+    ps0 += p[kb][0] + p[kb][2];
+    ps1 += p[kb][1] + p[kb][3];
+  }
+  l[0] = fmaf(l[0], al0, ps0);
+  l[1] = fmaf(l[1], al1, ps1);
   if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
     for (int j = 0; j < C::OT; ++j) {
@@ -733,98 +770,105 @@ __device__ __forceinline__ void warp_block_km(const uint8_t *kt, const uint8_t *
   }
 
   // ---- P^T -> the B fragments of PV (int8: the per-key V scale folded in)
-  if constexpr (KIND == KV_I8) {
-    float vg = vsc[row0 + g], v8 = vsc[row0 + g + 8];
-    if (!full) {  // the scale of a key past the split end may be anything: it meets p = 0
-      if (tok_row0 + g >= c1) vg = 0.f;
-      if (tok_row0 + g + 8 >= c1) v8 = 0.f;
+  uint32_t pb0[KB], pb1[KB];
+#pragma unroll
+  for (int kb = 0; kb < KB; ++kb) {
+    if constexpr (KIND == KV_I8) {
+      float vg = vsc[row0 + 16 * kb + g], v8 = vsc[row0 + 16 * kb + g + 8];
+      if (!full) {  // the scale of a key past the split end may be anything: it meets p = 0
+        if (tok_row0 + 16 * kb + g >= c1) vg = 0.f;
+        if (tok_row0 + 16 * kb + g + 8 >= c1) v8 = 0.f;
+      }
+      p[kb][0] *= vg;
+      p[kb][1] *= vg;
+      p[kb][2] *= v8;
+      p[kb][3] *= v8;
     }
-    p[0] *= vg;
-    p[1] *= vg;
-    p[2] *= v8;
-    p[3] *= v8;
+    // (keys g | g + 8) x (rows 2c, 2c + 1) -> row g x (keys 2c, 2c + 1 | 2c + 8, 2c + 9)
+    pb0[kb] = movmatrix_trans(pack_f16x2(p[kb][0], p[kb][1]));
+    pb1[kb] = movmatrix_trans(pack_f16x2(p[kb][2], p[kb][3]));
   }
-  // (keys g | g + 8) x (rows 2c, 2c + 1) -> row g x (keys 2c, 2c + 1 | 2c + 8, 2c + 9)
-  const uint32_t pb0 = movmatrix_trans(pack_f16x2(p[0], p[1]));
-  const uint32_t pb1 = movmatrix_trans(pack_f16x2(p[2], p[3]));
 
-  // ---- V^T as A fragments: keys (2c, 2c+1) and (2c+8, 2c+9), channels
-  // [g*NT, g*NT + NT). Keys at or past c1 read as 0.
-  const int kA = row0 + 2 * c, kB = kA + 8;
-  const int vrows[4] = {kA, kA + 1, kB, kB + 1};
-  bool valid[4];
+  // ---- V^T as A fragments: keys (2c, 2c+1) and (2c+8, 2c+9) of each
+  // sub-block, channels [g*NT, g*NT + NT). Keys at or past c1 read as 0.
 #pragma unroll
-  for (int i = 0; i < 4; ++i) valid[i] = full || tok_row0 + (vrows[i] - row0) < c1;
-  if constexpr (KIND == KV_I8) {
-    static_assert(NT % 4 == 0, "int8 V words");
-    constexpr int NW = NT / 4;  // 32-bit words per key
-    uint32_t w[4][NW];
+  for (int kb = 0; kb < KB; ++kb) {
+    const int kA = row0 + 16 * kb + 2 * c, kB = kA + 8;
+    const int vrows[4] = {kA, kA + 1, kB, kB + 1};
+    bool valid[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint8_t *src = vt + swz<SW>(vrows[i] * RB + g * NT);
-      if constexpr (NW == 4) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(src);
-        w[i][0] = v.x;
-        w[i][1] = v.y;
-        w[i][2] = v.z;
-        w[i][3] = v.w;
-      } else {
-        const uint2 v = *reinterpret_cast<const uint2 *>(src);
-        w[i][0] = v.x;
-        w[i][1] = v.y;
+    for (int i = 0; i < 4; ++i) valid[i] = full || tok_row0 + (vrows[i] - row0) < c1;
+    if constexpr (KIND == KV_I8) {
+      static_assert(NT % 4 == 0, "int8 V words");
+      constexpr int NW = NT / 4;  // 32-bit words per key
+      uint32_t w[4][NW];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint8_t *src = vt + swz<SW>(vrows[i] * RB + g * NT);
+        if constexpr (NW == 4) {
+          const uint4 v = *reinterpret_cast<const uint4 *>(src);
+          w[i][0] = v.x;
+          w[i][1] = v.y;
+          w[i][2] = v.z;
+          w[i][3] = v.w;
+        } else {
+          const uint2 v = *reinterpret_cast<const uint2 *>(src);
+          w[i][0] = v.x;
+          w[i][1] = v.y;
+        }
       }
-    }
-    if (!full) {  // keys past the split end read as code 0 (a raw 0)
+      if (!full) {  // keys past the split end read as code 0 (a raw 0)
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int k = 0; k < NW; ++k) w[i][k] = valid[i] ? w[i][k] : 0u;
-    }
-    const uint32_t u8_bias = kU8Bias;
-    auto pair = [&](uint32_t wa, uint32_t wb, int bi) {  // byte bi of two keys -> exact f16x2 codes
-      const uint32_t sel = bi | (bi << 4) | ((4u + bi) << 8) | ((4u + bi) << 12);
-      return hsub2_u32(i8pair_to_f16_biased(__byte_perm(wa, wb, sel), u8_bias), 1152.0f);
-    };
-#pragma unroll
-    for (int j = 0; j < C::OT; ++j) {  // channels g*NT + 2j, + 1: word j / 2, bytes 2 (j % 2) + {0, 1}
-      const int k = j / 2, bi = 2 * (j % 2);
-      const uint32_t a[4] = {pair(w[0][k], w[1][k], bi), pair(w[0][k], w[1][k], bi + 1),
-                             pair(w[2][k], w[3][k], bi), pair(w[2][k], w[3][k], bi + 1)};
-      mma_f16_16816(o[j], a, pb0, pb1);
-    }
-  } else {
-    static_assert(NT % 8 == 0, "int4 V words");
-    constexpr int NW = NT / 8;  // 32-bit words per key
-    const int grp = (g * NT) / 32;
-    uint32_t w[4][NW];
-    float vsf[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint8_t *src = vt + swz<SW>(vrows[i] * RB + g * (NT / 2));
-      if constexpr (NW == 2) {
-        const uint2 v = *reinterpret_cast<const uint2 *>(src);
-        w[i][0] = v.x;
-        w[i][1] = v.y;
-      } else {
-        w[i][0] = *reinterpret_cast<const uint32_t *>(src);
+          for (int k = 0; k < NW; ++k) w[i][k] = valid[i] ? w[i][k] : 0u;
       }
-      vsf[i] = valid[i] ? vsc[vrows[i] * NG + grp] : 0.f;
-    }
-    const uint32_t sA = pack_f16x2(vsf[0], vsf[1]);
-    const uint32_t sB = pack_f16x2(vsf[2], vsf[3]);
-    auto code = [&](uint32_t t, int q) {  // nibble q of two keys -> exact f16x2 codes
-      return (q & 1) ? hfma2_u32(nib_hi_f16_biased(t >> (4 * (q - 1)), nib_hi), 1.0f / 16.0f, -72.0f)
-                     : hsub2_u32(nib_lo_f16_biased(t >> (4 * q), nib_lo), 1032.0f);
-    };
+      const uint32_t u8_bias = kU8Bias;
+      auto pair = [&](uint32_t wa, uint32_t wb, int bi) {  // byte bi of two keys -> exact f16x2 codes
+        const uint32_t sel = bi | (bi << 4) | ((4u + bi) << 8) | ((4u + bi) << 12);
+        return hsub2_u32(i8pair_to_f16_biased(__byte_perm(wa, wb, sel), u8_bias), 1152.0f);
+      };
 #pragma unroll
-    for (int j = 0; j < C::OT; ++j) {  // channels g*NT + 2j, + 1: word j / 4, bytes 2 ((j / 2) % 2) + {0, 1}
-      const int k = j / 4, hb = (j / 2) % 2, q = 2 * (j % 2);
-      const uint32_t sel = hb ? 0x7632u : 0x5410u;
-      const uint32_t tA = __byte_perm(w[0][k], w[1][k], sel);
-      const uint32_t tB = __byte_perm(w[2][k], w[3][k], sel);
-      const uint32_t a[4] = {hmul2_u32(code(tA, q), sA), hmul2_u32(code(tA, q + 1), sA),
-                             hmul2_u32(code(tB, q), sB), hmul2_u32(code(tB, q + 1), sB)};
-      mma_f16_16816(o[j], a, pb0, pb1);
+      for (int j = 0; j < C::OT; ++j) {  // channels g*NT + 2j, + 1: word j / 2, bytes 2 (j % 2) + {0, 1}
+        const int k = j / 2, bi = 2 * (j % 2);
+        const uint32_t a[4] = {pair(w[0][k], w[1][k], bi), pair(w[0][k], w[1][k], bi + 1),
+                               pair(w[2][k], w[3][k], bi), pair(w[2][k], w[3][k], bi + 1)};
+        mma_f16_16816(o[j], a, pb0[kb], pb1[kb]);
+      }
+    } else {
+      static_assert(NT % 8 == 0, "int4 V words");
+      constexpr int NW = NT / 8;  // 32-bit words per key
+      const int grp = (g * NT) / 32;
+      uint32_t w[4][NW];
+      float vsf[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint8_t *src = vt + swz<SW>(vrows[i] * RB + g * (NT / 2));
+        if constexpr (NW == 2) {
+          const uint2 v = *reinterpret_cast<const uint2 *>(src);
+          w[i][0] = v.x;
+          w[i][1] = v.y;
+        } else {
+          w[i][0] = *reinterpret_cast<const uint32_t *>(src);
+        }
+        vsf[i] = valid[i] ? vsc[vrows[i] * NG + grp] : 0.f;
+      }
+      const uint32_t sA = pack_f16x2(vsf[0], vsf[1]);
+      const uint32_t sB = pack_f16x2(vsf[2], vsf[3]);
+      auto code = [&](uint32_t t, int q) {  // nibble q of two keys -> exact f16x2 codes
+        return (q & 1) ? hfma2_u32(nib_hi_f16_biased(t >> (4 * (q - 1)), nib_hi), 1.0f / 16.0f, -72.0f)
+                       : hsub2_u32(nib_lo_f16_biased(t >> (4 * q), nib_lo), 1032.0f);
+      };
+#pragma unroll
+      for (int j = 0; j < C::OT; ++j) {  // channels g*NT + 2j, + 1: word j / 4, bytes 2 ((j / 2) % 2) + {0, 1}
+        const int k = j / 4, hb = (j / 2) % 2, q = 2 * (j % 2);
+        const uint32_t sel = hb ? 0x7632u : 0x5410u;
+        const uint32_t tA = __byte_perm(w[0][k], w[1][k], sel);
+        const uint32_t tB = __byte_perm(w[2][k], w[3][k], sel);
+        const uint32_t a[4] = {hmul2_u32(code(tA, q), sA), hmul2_u32(code(tA, q + 1), sA),
+                               hmul2_u32(code(tB, q), sB), hmul2_u32(code(tB, q + 1), sB)};
+        mma_f16_16816(o[j], a, pb0[kb], pb1[kb]);
+      }
     }
   }
 }
