@@ -77,6 +77,28 @@ def test_parity_cases(case, S):
     assert_needles(w, out, inp)
 
 
+# Stage tails. The 16-row INT4 tile and the narrow INT8 tile take 32 keys per
+# consumer warp in two 16-key sub-blocks (128-key stages), so a split's last
+# stage can end inside a warp's first or second sub-block, on a sub-block
+# edge, or leave whole warps idle. One length for each of those residues
+# (mod 128), with causal MTP rows whose limits fall inside the last stage.
+TAIL_LENGTHS = tuple(256 + r for r in (1, 2, 15, 16, 17, 31, 32, 33, 47, 63, 64, 65, 95, 96, 97, 111, 127, 128))
+
+
+@pytest.mark.parametrize("kind,Tq,Hq", [("int4", 4, 32), ("int4", 1, 128), ("int8", 1, 32), ("int8", 2, 32)])
+@pytest.mark.parametrize("S", [1, 3])
+def test_stage_tail_residues(kind, Tq, Hq, S):
+    shape = _shape(kind, len(TAIL_LENGTHS), Tq, Hq, 8, 128, 16, TAIL_LENGTHS)
+    w = wl.make_workload(shape, 7 + Tq + S, "cuda", poison=True, needles=True, extra_pages=2)
+    inp = wl.oracle_inputs(w)
+    ref_out, ref_lse = decode_ref_inputs(inp)
+    out32, lse32 = run(w, S, torch.float32)
+    assert_parity(out32, lse32, ref_out, ref_lse, label=f"{kind} Tq={Tq} Hq={Hq} S={S} tails fp32 out")
+    out, lse = run(w, S)
+    assert_parity(out, lse, ref_out, ref_lse, label=f"{kind} Tq={Tq} Hq={Hq} S={S} tails", bf16_rounding=True)
+    assert_needles(w, out, inp)
+
+
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-B{c[1]}-T{c[2]}-H{c[3]}/{c[4]}-D{c[5]}-P{c[6]}")
 @pytest.mark.parametrize("S", [3, 8])
 def test_parity_cases_equal_policy(case, S):
