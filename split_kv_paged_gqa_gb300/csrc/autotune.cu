@@ -116,8 +116,9 @@ std::string cache_path(const fd_plan *pl) {
 
 // -------------------------------------------------------------- tuning inputs
 
-// Integer mixer ("lowbias32", C. Wellons) for reproducible synthetic fills.
-__device__ __forceinline__ uint32_t mix32(uint32_t x) {
+// Integer mixer ("lowbias32", C. Wellons) for reproducible synthetic fills
+// and the tuning inputs' page placement.
+__host__ __device__ __forceinline__ uint32_t mix32(uint32_t x) {
   x ^= x >> 16;
   x *= 0x7feb352du;
   x ^= x >> 15;
@@ -217,12 +218,21 @@ fd_status tune_alloc(fd_plan *pl, TuneBuffers &tb, int bmax, int max_bucket, cud
     fill_u8_kernel<<<4096, 256, 0, st>>>(static_cast<uint8_t *>(tb.v), kvn, 31u);
   }
   TRY_CUDA(cudaGetLastError());
-  // row r holds pages r * width ... (mod pool): rows of different calls of a
-  // sequence name different pages while the pool lasts
+  // row r holds pages perm[r * width ...] (mod pool): rows of different calls
+  // of a sequence name different pages while the pool lasts, and, as in a
+  // serving engine's page pool, a request's pages lie scattered over the pool
+  // (a fixed Fisher-Yates shuffle driven by the mixer above, so every tuning
+  // run sees the same placement)
+  std::vector<int> perm(static_cast<size_t>(tb.pool_pages));
+  for (long i = 0; i < tb.pool_pages; ++i) perm[i] = static_cast<int>(i);
+  for (long i = tb.pool_pages - 1; i > 0; --i) {
+    const uint32_t h = mix32(static_cast<uint32_t>(i) * 2654435761u ^ 0x5bd1e995u);
+    std::swap(perm[i], perm[static_cast<long>(h % static_cast<uint32_t>(i + 1))]);
+  }
   std::vector<int> pt(pt_rows * tb.width);
   for (size_t r = 0; r < pt_rows; ++r)
     for (int p = 0; p < tb.width; ++p)
-      pt[r * tb.width + p] = static_cast<int>((static_cast<long>(r) * tb.width + p) % tb.pool_pages);
+      pt[r * tb.width + p] = perm[(static_cast<long>(r) * tb.width + p) % tb.pool_pages];
   TRY_CUDA(cudaMemcpyAsync(tb.pt, pt.data(), pt.size() * 4, cudaMemcpyHostToDevice, st));
   TRY_CUDA(cudaStreamSynchronize(st));
   return FD_OK;
