@@ -410,6 +410,19 @@ FD_API fd_status fd_autotune_stats(fd_plan *plan, int *searches, int *cache_hits
  * graph capture. Returns FD_ERR_DEVICE_STATUS when any bit was set. */
 FD_API fd_status fd_read_device_status(fd_plan *plan, int *code);
 
+/* fd_selftest_wait_timeout - run the decode kernels' bounded-wait failure
+ * path on purpose. The pages have no counterpart: this checks this library's
+ * own guard against a pipeline that never delivers. One CTA of one warp
+ * waits, with the decode kernels' wait routine, on a fresh mbarrier that
+ * nothing arrives on, and gives up after limit_us microseconds of
+ * %globaltimer time (1 .. 2,000,000; the decode kernels use 2 s). It records
+ * FD_DEVSTAT_WAIT_TIMEOUT in the plan's status word and returns. No fault, no
+ * trap, and the context stays usable. The launch is asynchronous on `stream`;
+ * fd_read_device_status reports the bit. Returns FD_ERR_INVALID_ARG for a
+ * NULL plan or a limit outside the range, FD_ERR_WORKSPACE for a plan without
+ * a device, FD_ERR_CUDA if the launch fails. */
+FD_API fd_status fd_selftest_wait_timeout(fd_plan *plan, unsigned limit_us, fd_stream_t stream);
+
 /* fd_plan_workspace_bytes - device bytes the plan's split workspace holds. */
 FD_API fd_status fd_plan_workspace_bytes(fd_plan *plan, size_t *bytes);
 

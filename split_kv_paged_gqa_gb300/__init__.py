@@ -19,7 +19,8 @@ __all__ = [
     "fd_set_mean_seqlen_hint", "fd_graph_metadata", "fd_warmup_enter", "fd_warmup_exit", "fd_warmup_current",
     "warmup", "fd_autotune_set_input_hook", "fd_autotune_clear", "fd_autotune", "fd_query_splits",
     "fd_autotune_set_timer", "fd_autotune_set_cache_dir", "fd_autotune_stats",
-    "fd_read_device_status", "fd_plan_workspace_bytes", "fd_profile_begin", "fd_profile_end",
+    "fd_read_device_status", "fd_selftest_wait_timeout", "fd_plan_workspace_bytes", "fd_profile_begin",
+    "fd_profile_end",
     "fd_status_string", "fd_last_error",
     "FD_OK", "FD_ERR_INVALID_ARG", "FD_ERR_UNSUPPORTED", "FD_ERR_WORKSPACE", "FD_ERR_CAPTURING",
     "FD_ERR_CUDA", "FD_ERR_DEVICE_STATUS", "FD_ERR_TIMEOUT", "FD_ERR_NO_PLAN", "FD_ERR_IO",
@@ -101,6 +102,7 @@ def load_library(path: Optional[str] = None):
         "fd_autotune_set_cache_dir": (I, [P, ctypes.c_char_p]),
         "fd_autotune_stats": (I, [P, ctypes.POINTER(I), ctypes.POINTER(I)]),
         "fd_read_device_status": (I, [P, ctypes.POINTER(I)]),
+        "fd_selftest_wait_timeout": (I, [P, ctypes.c_uint, P]),
         "fd_plan_workspace_bytes": (I, [P, ctypes.POINTER(ctypes.c_size_t)]),
         "fd_profile_begin": (I, [P]),
         "fd_profile_end": (I, [P, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double),
@@ -373,6 +375,12 @@ def fd_read_device_status(plan: int) -> int:
     if s not in (FD_OK, FD_ERR_DEVICE_STATUS):
         _check(s)
     return v.value
+
+
+def fd_selftest_wait_timeout(plan: int, limit_us: int, stream=None) -> None:
+    """Enqueue the bounded-wait self-test: a wait that nothing completes gives
+    up after limit_us and sets FD_DEVSTAT_WAIT_TIMEOUT in the plan's status."""
+    _check(load_library().fd_selftest_wait_timeout(plan, limit_us, _stream_handle(stream)))
 
 
 def fd_plan_workspace_bytes(plan: int) -> int:

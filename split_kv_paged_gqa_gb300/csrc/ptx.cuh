@@ -72,13 +72,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity; false (and a status bit) on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity, unsigned *status) {
+// Wait for the phase with the given parity; false (and a status bit) after
+// limit_ns of %globaltimer time (kWaitLimitNs in the decode kernels; the
+// wait self-test passes a short limit).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity, unsigned *status,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       atomicOr(status, FD_DEVSTAT_WAIT_TIMEOUT);
       return false;
     }
@@ -87,8 +90,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity, unsign
 
 // Every lane waits (bounded); the warp proceeds only if all lanes saw the
 // phase complete, so a timeout leaves the warp converged.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, unsigned parity, unsigned *status) {
-  const bool ok = mbar_wait(bar, parity, status);
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, unsigned parity, unsigned *status,
+                                               unsigned long long limit_ns = kWaitLimitNs) {
+  const bool ok = mbar_wait(bar, parity, status, limit_ns);
   return __all_sync(0xffffffffu, ok) != 0;
 }
 

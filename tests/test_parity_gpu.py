@@ -372,6 +372,33 @@ def test_seqlen_over_capacity_sets_status():
     assert fd.fd_read_device_status(plan) & fd.FD_DEVSTAT_SEQLEN_OVERFLOW
 
 
+def test_wait_that_never_completes_times_out_and_the_context_stays_usable():
+    # The kernels' bounded wait on a barrier that nothing arrives on gives up
+    # after its limit, records the status bit and returns; a decode call on the
+    # same plan afterwards still matches the oracle.
+    import time
+    shape = _shape("bf16", 2, 1, 8, 2, 64, 16, (100, 40))
+    w = wl.make_workload(shape, 23, "cuda")
+    plan = fd.fd_plan_create(0, 2, 1, 8, 2, 64, 16, "bf16", 4)
+    try:
+        assert fd.fd_read_device_status(plan) == 0
+        t0 = time.perf_counter()
+        fd.fd_selftest_wait_timeout(plan, 2000)
+        torch.cuda.synchronize()
+        elapsed = time.perf_counter() - t0
+        assert fd.fd_read_device_status(plan) == fd.FD_DEVSTAT_WAIT_TIMEOUT
+        assert elapsed < 1.0, f"the 2 ms wait took {elapsed:.3f} s"
+        ref_out, ref_lse = decode_ref_inputs(wl.oracle_inputs(w))
+        out, lse = run(w, 4, plan=plan)
+        assert_parity(out, lse, ref_out, ref_lse, label="decode after a timed-out wait")
+        assert fd.fd_read_device_status(plan) == 0
+        with pytest.raises(fd.FdError):
+            fd.fd_selftest_wait_timeout(plan, 0)
+    finally:
+        fd.fd_set_plan(None)
+        fd.fd_plan_destroy(plan)
+
+
 # ---------------------------------------------------------------------------
 # CUDA graph capture and replay with new metadata contents
 
