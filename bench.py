@@ -117,11 +117,40 @@ def measured_peaks():
 STAGE1_SOURCES = ("stage1.cuh", "stage1_bf16.cu", "stage1_i8.cu", "stage1_i4.cu", "ptx.cuh", "kernels.h")
 
 
+def strip_c_comments(src: str) -> str:
+    """C/C++ source without its comments, whitespace runs collapsed to one
+    space: what the compiler sees, so an edit to a comment keeps the hash.
+    String and character literals are kept verbatim."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        ch = src[i]
+        if ch in "\"'":
+            j = i + 1
+            while j < n and src[j] != ch:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(ch)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def stage1_source_sha() -> str:
-    """Hash of the files the stage-1 kernel is compiled from (host code excluded)."""
+    """Hash of the code of the files the stage-1 kernel is compiled from (host
+    code excluded; comments and layout do not count)."""
     h = hashlib.sha256()
     for name in STAGE1_SOURCES:
-        h.update(open(os.path.join(ROOT, "split_kv_paged_gqa_gb300", "csrc", name), "rb").read())
+        txt = open(os.path.join(ROOT, "split_kv_paged_gqa_gb300", "csrc", name), encoding="utf-8").read()
+        h.update(strip_c_comments(txt).encode())
+        h.update(b"\0")
     return h.hexdigest()[:16]
 
 

@@ -79,9 +79,10 @@ struct S1Cfg {
   // consumer warps; the deep (one CTA per SM) variant doubles them so a lone
   // CTA has more blocks in flight
   static constexpr int NUM_CW = DEEP ? 8 : 4;
-  // keys per consumer warp and stage: 16, or 32 for the 16-row int4 variant
-  // (two 16-key sub-blocks share one softmax step and one round trip of O
-  // through tensor memory, and their MMA chains interleave)
+  // keys per consumer warp and stage: 16, or 32 for the 16-row int4 and the
+  // narrow int8 variants (two 16-key sub-blocks share one softmax step, one
+  // reload of the Q fragments and, int4, one round trip of O through tensor
+  // memory, and their MMA chains interleave)
   static constexpr int KPW = (KIND == KV_I4 && !NARROW && !DEEP) || (KIND == KV_I8 && NARROW) ? 32 : 16;
   static constexpr int BLOCK_N = NUM_CW * KPW;           // keys per pipeline stage
   static constexpr int SEG_MAX = 64;                     // slots per TMA box at most
@@ -90,8 +91,9 @@ struct S1Cfg {
   // that fit in one wave (small batches), where a single CTA must keep enough
   // bytes and blocks in flight.
   // Quantised kinds are bound by the consumer warps' latency, not by bytes in
-  // flight: the 16-row variants run three CTAs per SM (128 registers), the
-  // narrow ones four (96 registers), on rings that fit.
+  // flight: the 16-row variants and the narrow int8 one (its 128-key stages)
+  // run three CTAs per SM (128 registers), the narrow int4 one four (96
+  // registers), on rings that fit (FOUR asks for four where they fit).
   static constexpr bool FOUR = NARROW;
   static constexpr int STAGES = KIND == KV_BF16 ? 3 : (KIND == KV_I8 ? (FOUR ? 2 : 3) : (FOUR ? 4 : 6) * 16 / KPW);
   // Quantised kinds park the (identical) Q fragments of the consumer warps in

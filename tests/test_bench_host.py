@@ -80,6 +80,14 @@ def test_stage1_sha_covers_kernel_sources_only():
     assert "fd_api.cu" not in bench.STAGE1_SOURCES and "stage1.cuh" in bench.STAGE1_SOURCES
 
 
+def test_source_hash_ignores_comments_and_layout_but_not_code():
+    src = 'int a = 1; // note\n/* block\n comment */ const char *s = "x // kept /* kept */";\nint  b;'
+    assert bench.strip_c_comments(src) == 'int a = 1; const char *s = "x // kept /* kept */"; int b;'
+    assert bench.strip_c_comments("a /* x */ b") == bench.strip_c_comments("a   b")
+    assert bench.strip_c_comments("x = 1;") != bench.strip_c_comments("x = 2;")
+    assert bench.strip_c_comments("c = '\\'';// q") == "c = '\\'';"
+
+
 def test_nearest_pow2_matches_the_log_midpoint():
     assert [bench.nearest_pow2(v) for v in (1, 2, 3, 5, 6, 5932, 5000, 23000, 23171, 32768)] == \
         [1, 2, 4, 4, 8, 8192, 4096, 16384, 32768, 32768]
