@@ -81,11 +81,13 @@ def test_parity_cases(case, S):
 # consumer warp in two 16-key sub-blocks (128-key stages), so a split's last
 # stage can end inside a warp's first or second sub-block, on a sub-block
 # edge, or leave whole warps idle. One length for each of those residues
-# (mod 128), with causal MTP rows whose limits fall inside the last stage.
+# (mod 128), with causal MTP rows whose limits fall inside the last stage. The
+# narrow INT4 tile (16 keys per warp, 64-key stages) runs the same lengths.
 TAIL_LENGTHS = tuple(256 + r for r in (1, 2, 15, 16, 17, 31, 32, 33, 47, 63, 64, 65, 95, 96, 97, 111, 127, 128))
 
 
-@pytest.mark.parametrize("kind,Tq,Hq", [("int4", 4, 32), ("int4", 1, 128), ("int8", 1, 32), ("int8", 2, 32)])
+@pytest.mark.parametrize("kind,Tq,Hq", [("int4", 4, 32), ("int4", 1, 128), ("int4", 1, 32), ("int4", 2, 32),
+                                        ("int8", 1, 32), ("int8", 2, 32)])
 @pytest.mark.parametrize("S", [1, 3])
 def test_stage_tail_residues(kind, Tq, Hq, S):
     shape = _shape(kind, len(TAIL_LENGTHS), Tq, Hq, 8, 128, 16, TAIL_LENGTHS)
