@@ -86,18 +86,20 @@ def test_parity_cases(case, S):
 TAIL_LENGTHS = tuple(256 + r for r in (1, 2, 15, 16, 17, 31, 32, 33, 47, 63, 64, 65, 95, 96, 97, 111, 127, 128))
 
 
-@pytest.mark.parametrize("kind,Tq,Hq", [("int4", 4, 32), ("int4", 1, 128), ("int4", 1, 32), ("int4", 2, 32),
-                                        ("int8", 1, 32), ("int8", 2, 32)])
+@pytest.mark.parametrize("kind,Tq,Hq,D", [("int4", 4, 32, 128), ("int4", 1, 128, 128), ("int4", 4, 32, 64),
+                                          ("int4", 1, 32, 128), ("int4", 2, 32, 128),
+                                          ("int8", 1, 32, 128), ("int8", 2, 32, 128), ("int8", 1, 32, 64)])
 @pytest.mark.parametrize("S", [1, 3])
-def test_stage_tail_residues(kind, Tq, Hq, S):
-    shape = _shape(kind, len(TAIL_LENGTHS), Tq, Hq, 8, 128, 16, TAIL_LENGTHS)
+def test_stage_tail_residues(kind, Tq, Hq, D, S):
+    shape = _shape(kind, len(TAIL_LENGTHS), Tq, Hq, 8, D, 16, TAIL_LENGTHS)
     w = wl.make_workload(shape, 7 + Tq + S, "cuda", poison=True, needles=True, extra_pages=2)
     inp = wl.oracle_inputs(w)
     ref_out, ref_lse = decode_ref_inputs(inp)
+    label = f"{kind} Tq={Tq} Hq={Hq} D={D} S={S} tails"
     out32, lse32 = run(w, S, torch.float32)
-    assert_parity(out32, lse32, ref_out, ref_lse, label=f"{kind} Tq={Tq} Hq={Hq} S={S} tails fp32 out")
+    assert_parity(out32, lse32, ref_out, ref_lse, label=label + " fp32 out")
     out, lse = run(w, S)
-    assert_parity(out, lse, ref_out, ref_lse, label=f"{kind} Tq={Tq} Hq={Hq} S={S} tails", bf16_rounding=True)
+    assert_parity(out, lse, ref_out, ref_lse, label=label, bf16_rounding=True)
     assert_needles(w, out, inp)
 
 
