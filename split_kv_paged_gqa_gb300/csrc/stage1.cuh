@@ -18,8 +18,8 @@
 //    completing on a per-stage mbarrier. Quantised caches also copy their
 //    per-row fp32 scales with cp.async (one arrival per lane on the barrier).
 //  * consumer warps: warp w takes keys [KPW w, KPW w + KPW) of each stage of
-//    4 KPW keys (KPW = 16; 32 for the 16-row int4 variant, as two 16-key
-//    sub-blocks that share one softmax step).
+//    4 KPW keys (KPW = 16; 32 for the 16-row int4 and the narrow int8
+//    variants, as two 16-key sub-blocks that share one softmax step).
 //    QK^T and PV run on mma.sync m16n8k16 (fp32 accumulate) with the 16 query
 //    rows as M; the online softmax keeps a running max / sum per row in the
 //    log2 domain with quad shuffles. bf16 caches feed ldmatrix fragments
