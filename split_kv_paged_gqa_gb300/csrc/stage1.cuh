@@ -297,9 +297,15 @@ __device__ __forceinline__ void softmax_update(const float (&s)[2][4], float (&p
 // ----------------------------------------------------------------------------
 // Online-softmax update (as softmax_update) over KB 16-key sub-blocks that
 // share one row max: the thread's scores s[kb][nt][e] of rows g (e < 2) and
-// g + 8 (e >= 2).
-template <int KB>
-__device__ __forceinline__ void softmax_update_kb(const float (&s)[KB][2][4], float (&p)[KB][2][4],
+// g + 8 (e >= 2). Returns whether O must be rescaled by al (warp-uniform).
+// LAZY: the rows keep their running max m until some row of the warp sees a
+// score above its m + kLazyMax (log2 units); until then p = 2^(s - m) may
+// reach 2^kLazyMax, and al = 1. The result is the same up to rounding (l, O
+// and the LSE all use the same m), and the 64-multiply rescale of O runs
+// about once per split instead of on a third of its blocks.
+constexpr float kLazyMax = 8.f;
+template <int KB, bool LAZY>
+__device__ __forceinline__ bool softmax_update_kb(const float (&s)[KB][2][4], float (&p)[KB][2][4],
                                                   float (&m)[2], float (&l)[2], float (&al)[2]) {
   float mx0 = fmaxf(fmaxf(s[0][0][0], s[0][0][1]), fmaxf(s[0][1][0], s[0][1][1]));
   float mx1 = fmaxf(fmaxf(s[0][0][2], s[0][0][3]), fmaxf(s[0][1][2], s[0][1][3]));
@@ -312,13 +318,23 @@ __device__ __forceinline__ void softmax_update_kb(const float (&s)[KB][2][4], fl
   mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
   mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
   mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-  const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+  float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+  bool rescale;
+  if constexpr (LAZY) {
+    // (a row's first finite score always moves it: -inf + kLazyMax = -inf)
+    rescale = __any_sync(0xffffffffu, mn0 > m[0] + kLazyMax || mn1 > m[1] + kLazyMax);
+    if (!rescale) {
+      mn0 = m[0];
+      mn1 = m[1];
+    }
+  }
   const float b0 = mn0 == -INFINITY ? 0.f : mn0;
   const float b1 = mn1 == -INFINITY ? 0.f : mn1;
   al[0] = fast_exp2(m[0] - b0);
   al[1] = fast_exp2(m[1] - b1);
   m[0] = mn0;
   m[1] = mn1;
+  if constexpr (!LAZY) rescale = __any_sync(0xffffffffu, al[0] != 1.f || al[1] != 1.f);
   float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
   for (int kb = 0; kb < KB; ++kb) {
@@ -334,6 +350,7 @@ __device__ __forceinline__ void softmax_update_kb(const float (&s)[KB][2][4], fl
   }
   l[0] = l[0] * al[0] + sum0;
   l[1] = l[1] * al[1] + sum1;
+  return rescale;
 }
 
 // ----------------------------------------------------------------------------
@@ -467,8 +484,9 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
       }
   }
   float p[KB][2][4], al[2];
-  softmax_update_kb<KB>(s, p, m, l, al);
-  const bool rescale = __any_sync(0xffffffffu, al[0] != 1.f || al[1] != 1.f);
+  // int4 may let p reach 2^kLazyMax (fp16 P; its V scale stays with V); int8
+  // folds the V scale into P, so it keeps the exact running max
+  const bool rescale = softmax_update_kb<KB, KIND == KV_I4>(s, p, m, l, al);
   // alpha-rescale of O if the max moved
   auto rescale_o = [&](float (&oo)[NT][4]) {
     if (rescale) {
