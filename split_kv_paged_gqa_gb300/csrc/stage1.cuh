@@ -265,39 +265,13 @@ __device__ __forceinline__ void warp_block(uint32_t kbase, uint32_t vbase, uint3
   }
 }
 
-// Online-softmax update in the log2 domain for a thread's two rows (g, g+8):
-// row max over the quad, alpha = 2^(m_old - m_new), p = 2^(s - m_new), running
-// sum rescaled by alpha. Rows that have seen no key keep m = -inf and p = 0.
-__device__ __forceinline__ void softmax_update(const float (&s)[2][4], float (&p)[2][4], float (&m)[2],
-                                               float (&l)[2], float (&al)[2]) {
-  float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
-  float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
-  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-  const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
-  const float b0 = mn0 == -INFINITY ? 0.f : mn0;
-  const float b1 = mn1 == -INFINITY ? 0.f : mn1;
-  al[0] = fast_exp2(m[0] - b0);
-  al[1] = fast_exp2(m[1] - b1);
-  m[0] = mn0;
-  m[1] = mn1;
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    p[nt][0] = fast_exp2(s[nt][0] - b0);
-    p[nt][1] = fast_exp2(s[nt][1] - b0);
-    p[nt][2] = fast_exp2(s[nt][2] - b1);
-    p[nt][3] = fast_exp2(s[nt][3] - b1);
-  }
-  l[0] = l[0] * al[0] + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-  l[1] = l[1] * al[1] + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
-}
-
 // ----------------------------------------------------------------------------
-// Online-softmax update (as softmax_update) over KB 16-key sub-blocks that
-// share one row max: the thread's scores s[kb][nt][e] of rows g (e < 2) and
-// g + 8 (e >= 2). Returns whether O must be rescaled by al (warp-uniform).
+// Online-softmax update in the log2 domain for a thread's two rows (g, g+8)
+// over KB 16-key sub-blocks that share one row max (scores s[kb][nt][e], row
+// g for e < 2, g + 8 for e >= 2): row max over the quad, alpha = 2^(m_old -
+// m_new), p = 2^(s - m_new), running sum rescaled by alpha. Rows that have
+// seen no key keep m = -inf and p = 0. Returns whether O must be rescaled by
+// al (warp-uniform).
 // LAZY: the rows keep their running max m until some row of the warp sees a
 // score above its m + kLazyMax (log2 units); until then p = 2^(s - m) may
 // reach 2^kLazyMax, and al = 1. The result is the same up to rounding (l, O
