@@ -15,8 +15,11 @@ live CUDA-event timing of its launches), the CPU baseline (the float64 oracle
 on a bounded sample, host cores), an end-to-end number through the public
 binding with host buffers, SM clocks sampled during the timed region, the
 num_splits sweep for batch 1 / 16 / 64 with the autotuned pick against the
-sweep's best, and the time of the one-launch graph-metadata rebuild of the
-batch (outside the timed region).
+sweep's best, the time of the one-launch graph-metadata rebuild of the
+batch, the HBM read-only and copy bandwidth from this library's probe kernels
+("peaks_probe"), and one entry per other workload of the study ("configs":
+us/call median / p10 / p90, KV GB/s, stage-1 roofline fraction, the tuned
+num_splits, the profiled DRAM traffic ratio) -- all outside the timed region.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fd|reference]
 Multi-GPU (torchrun): each rank decodes its own batch (weak scaling, no
@@ -297,6 +300,43 @@ def oracle_baseline(w: wl.Workload, requests, key_hi=None):
 # the CUDA arm
 
 
+GB300_L2_BYTES = 126 << 20  # L2 size of a GB300 (used where no GPU is visible)
+
+
+def l2_size(dev=None) -> int:
+    """L2 bytes of the GPU (the same figure for both arms on one box)."""
+    try:
+        import torch
+        if torch.cuda.is_available():
+            d = dev if dev is not None else torch.device("cuda", torch.cuda.current_device())
+            return int(getattr(torch.cuda.get_device_properties(d), "L2_cache_size", 0) or GB300_L2_BYTES)
+    except Exception:
+        pass
+    return GB300_L2_BYTES
+
+
+def l2_note(call_bytes: int, n_copy: int, l2_bytes: int) -> str:
+    """How the timed calls avoid finding their KV in L2."""
+    if n_copy == 1:
+        return "inputs larger than L2 (%.2f GB of KV per step), no flush" % (call_bytes / 1e9)
+    return ("calls rotate over %d disjoint copies of the step's inputs (%.2f GB of KV together, at least "
+            "4x the %.0f MB L2), no flush" % (n_copy, n_copy * call_bytes / 1e9, l2_bytes / 1e6))
+
+
+def workload_config(name: str, shape: wl.DecodeShape, lengths: np.ndarray, world: int, l2_bytes: int) -> dict:
+    """The ``config`` object of a bench line: what the workload is (both arms
+    print the same one for the same workload)."""
+    _, call_bytes = algorithmic_bytes(shape, lengths)
+    n_copy = rotation_copies(call_bytes, l2_bytes)
+    Lmax = int(lengths.max())
+    return {"workload": f"{name}: batch {shape.batch}, KV lengths {shape.lengths} (max {Lmax}), "
+                        f"Hq {shape.num_q_heads}, Hkv {shape.num_kv_heads}, head_dim {shape.head_dim}, "
+                        f"page {shape.page_size}, Tq {shape.q_per_req}, {shape.kv_dtype} KV",
+            "batch_per_gpu": shape.batch, "kv_len": Lmax, "kv_len_mean": max(1, int(round(float(lengths.mean())))),
+            "bytes_per_step": call_bytes, "l2": l2_note(call_bytes, n_copy, l2_bytes),
+            "parallelism": f"replicas x{world}"}
+
+
 def rotation_copies(call_bytes: int, l2_bytes: int, limit: int = 4096) -> int:
     """How many disjoint copies of a step's inputs the timed calls rotate over.
 
@@ -306,6 +346,156 @@ def rotation_copies(call_bytes: int, l2_bytes: int, limit: int = 4096) -> int:
     if call_bytes >= 4 * l2_bytes:
         return 1
     return int(min(limit, -(-4 * l2_bytes // max(call_bytes, 1))))
+
+
+PROBE_BYTES = 2 << 30   # probe buffer: 1 Gi bf16 elements, as the driver's copy measurement
+
+
+def measure_probes(fd, dev, trials: int = 10) -> dict:
+    """HBM read-only and copy bandwidth from this library's probe kernels
+    (16-byte vector accesses over 2 GiB, far above L2), best and median of
+    ``trials`` CUDA-event timings each; copy counts read + write bytes."""
+    import torch
+    src = torch.empty(PROBE_BYTES // 2, dtype=torch.bfloat16, device=dev)
+    src.view(torch.int16).random_(generator=torch.Generator(device=dev).manual_seed(0))
+    dst = torch.empty_like(src)
+    sink = torch.zeros(4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, nbytes):
+        for _ in range(3):
+            fn()
+        gbs = []
+        for _ in range(trials):
+            torch.cuda.synchronize()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            gbs.append(nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+        return max(gbs), statistics.median(gbs)
+
+    rd, rd_med = timed(lambda: fd.fd_probe_hbm_read(src, sink), PROBE_BYTES)
+    cp, cp_med = timed(lambda: fd.fd_probe_hbm_copy(src, dst), 2 * PROBE_BYTES)
+    ok = bool(torch.equal(src.view(torch.int16), dst.view(torch.int16)))
+    del src, dst, sink
+    torch.cuda.empty_cache()
+    return {"read_gbs": round(rd, 1), "read_gbs_median": round(rd_med, 1), "copy_gbs": round(cp, 1),
+            "copy_gbs_median": round(cp_med, 1), "copy_verified": ok, "buffer_bytes": PROBE_BYTES,
+            "trials": trials,
+            "what": "fd_probe_hbm_read (XOR-fold of 16-byte loads) and fd_probe_hbm_copy (16-byte loads and "
+                    "stores), 4 CTAs of 512 threads per SM, 8 loads in flight per thread; best of the trials; "
+                    "copy counts read + write bytes"}
+
+
+# Workloads measured beside the headline in the default run (one entry each
+# in the line's "configs" object).
+EXTRA_CONFIGS = ("tiny_bf16", "mixed_bf16", "long_bf16_b1", "long_bf16_b16", "int8_lognormal", "int4_mtp")
+
+
+def measure_config(name: str, fd, dev, local: int, l2_bytes: int, peak: float, trials: int = 10,
+                   per_trial: int = 50) -> dict:
+    """One workload in the bench's launch configuration: startup-tuned
+    num_splits, calls replayed from CUDA graphs rotating over disjoint copies
+    of the inputs (>= 4x L2 of KV together); per-call median / p10 / p90 over
+    ``trials`` graphs of ``per_trial`` calls, and the stage-1 roofline from
+    live per-stage events."""
+    import dataclasses
+
+    import torch
+    shape = wl.CONFIGS[name]
+    seed = wl.CONFIG_SEEDS[name]
+    B = shape.batch
+    lengths = wl.draw_lengths(shape.lengths, B, np.random.default_rng(seed))
+    _, call_bytes0 = algorithmic_bytes(shape, lengths)
+    n_copy = rotation_copies(call_bytes0, l2_bytes)
+    if n_copy == 1:
+        w = wl.make_workload(shape, seed, dev)
+    else:
+        big = dataclasses.replace(shape, batch=B * n_copy,
+                                  pool_pages=shape.pool_pages * n_copy if shape.pool_pages else None)
+        w = wl.make_workload(big, seed, dev, lengths=np.tile(lengths, n_copy))
+    Lmax = int(lengths.max())
+    Lmean = max(1, int(round(float(lengths.mean()))))
+    plan = fd.fd_plan_create(local, B, shape.q_per_req, shape.num_q_heads, shape.num_kv_heads, shape.head_dim,
+                             shape.page_size, shape.kv_dtype, 64)
+    try:
+        fd.fd_set_plan(plan)
+        bucket = 1 << (Lmax - 1).bit_length()
+        t0 = time.perf_counter()
+        fd.fd_autotune(plan, [B], min(nearest_pow2(Lmean), bucket), bucket)
+        tune_s = time.perf_counter() - t0
+        fd.fd_set_max_seqlen_hint(plan, Lmax)
+        fd.fd_set_mean_seqlen_hint(plan, Lmean)
+        S = fd.fd_query_splits(plan, B, Lmax)
+        out = torch.empty((B,) + tuple(w.q.shape[1:]), dtype=w.q.dtype, device=dev)
+        lse = torch.empty(out.shape[:3], dtype=torch.float32, device=dev)
+
+        def step(i):
+            g0 = (i % n_copy) * B
+            fd.fd_decode_paged(w.q[g0:g0 + B], w.k_cache, w.v_cache, w.kv_scales, w.page_table[g0:g0 + B],
+                               w.cache_seqlens[g0:g0 + B], shape.q_per_req, 0, out, lse)
+
+        stream = torch.cuda.current_stream()
+        cap_stream = torch.cuda.Stream()
+        cap_stream.wait_stream(stream)
+        with torch.cuda.stream(cap_stream):
+            for i in range(3):
+                step(i)
+        stream.wait_stream(cap_stream)
+        torch.cuda.synchronize()
+
+        def capture(n, first):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(n):
+                    step(first + i)
+            return g
+
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g_w = capture(per_trial, 0)
+        g_w.replay()
+        del g_w
+        trial_us = []
+        for t in range(trials):
+            g = capture(per_trial, (t + 1) * per_trial)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            trial_us.append(e0.elapsed_time(e1) / per_trial * 1e3)
+            del g
+        fd.fd_profile_begin(plan)
+        g = capture(per_trial, 0)
+        g.replay()
+        torch.cuda.synchronize()
+        del g
+        calls, s1_ms, s2_ms = fd.fd_profile_end(plan)
+    finally:
+        fd.fd_set_plan(None)
+        fd.fd_plan_destroy(plan)
+    del w
+    torch.cuda.empty_cache()
+    nv = split_counts(lengths, shape.page_size, S)
+    stage1_bytes, call_bytes = algorithmic_bytes(shape, lengths, direct=(nv == 1))
+    med = statistics.median(trial_us)
+    s1_avg = s1_ms / max(calls, 1)
+    achieved = stage1_bytes / (s1_avg * 1e-3) / 1e9
+    traffic = profiled_traffic(name)
+    return {"us_per_call_median": round(med, 2), "us_per_call_p10": round(float(np.percentile(trial_us, 10)), 2),
+            "us_per_call_p90": round(float(np.percentile(trial_us, 90)), 2),
+            "kv_gbs": round(call_bytes / (med * 1e-6) / 1e9, 1),
+            "frac_of_measured_peak_per_call": round(call_bytes / (med * 1e-6) / 1e9 / peak, 4),
+            "stage1": {"avg_launch_us": round(s1_avg * 1e3, 2), "achieved_gbs": round(achieved, 1),
+                       "frac": round(achieved / peak, 4), "algorithmic_bytes": stage1_bytes,
+                       "stage2_avg_us": round(s2_ms / max(calls, 1) * 1e3, 2)},
+            "num_splits": S, "num_splits_source": "autotuned", "autotune_s": round(tune_s, 2),
+            "traffic_over_algorithmic": None if traffic is None else round(traffic / stage1_bytes, 4),
+            "bytes_per_call": call_bytes, "kv_len_max": Lmax, "kv_len_mean": Lmean,
+            "l2": l2_note(call_bytes0, n_copy, l2_bytes),
+            "timing": f"{trials} CUDA graphs of {per_trial} rotating calls, replayed between CUDA events"}
 
 
 def run_fd(args):
@@ -327,7 +517,7 @@ def run_fd(args):
     # the step's lengths, drawn as the workload generator draws them
     lengths = wl.draw_lengths(shape.lengths, B, np.random.default_rng(seed))
     _, call_bytes0 = algorithmic_bytes(shape, lengths)
-    l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (126 << 20))
+    l2_bytes = l2_size(dev)
     n_copy = rotation_copies(call_bytes0, l2_bytes)
     if n_copy == 1:
         w = wl.make_workload(shape, seed, dev)
@@ -590,6 +780,29 @@ def run_fd(args):
                         "from a request-to-token pool in one launch (CUDA graph of %d launches, replayed)" % n_meta}
         del graph
 
+    # HBM probes and the other workloads of the study, on this GPU (rank 0 of
+    # a single-GPU run: the per-workload table is a one-GPU measurement)
+    probes = None
+    configs = None
+    peak_read = None
+    if rank == 0 and not args.no_probes:
+        probes = measure_probes(fd, dev)
+        probes["copy_over_measured_peaks"] = round(probes["copy_gbs"] / peak, 4) if peak_kind == "measured" else None
+        peak_read = probes["read_gbs"]
+    if rank == 0 and world == 1 and not args.no_configs:
+        configs = {}
+        for name in EXTRA_CONFIGS:
+            if name == args.config:
+                continue
+            try:
+                configs[name] = measure_config(name, fd, dev, local, l2_bytes, peak)
+                if peak_read:
+                    st1 = configs[name]["stage1"]
+                    st1["frac_of_read_probe"] = round(st1["achieved_gbs"] / peak_read, 4)
+            except Exception as exc:
+                configs[name] = {"error": f"{type(exc).__name__}: {exc}"[:300]}
+        fd.fd_set_plan(plan)
+
     # CPU baseline: the oracle on a bounded sample of this workload, host cores
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -605,11 +818,6 @@ def run_fd(args):
     if rank != 0:
         return None
     gpu_launches = args.steps * launches_per_call(B, S)
-    if n_copy == 1:
-        l2_note = "inputs larger than L2 (%.2f GB of KV per step), no flush" % (call_bytes / 1e9)
-    else:
-        l2_note = ("calls rotate over %d disjoint copies of the step's inputs (%.2f GB of KV together, at least "
-                   "4x the %.0f MB L2), no flush" % (n_copy, n_copy * call_bytes / 1e9, l2_bytes / 1e6))
     return {
         "metric": METRIC,
         "value": round(value, 1),
@@ -624,15 +832,11 @@ def run_fd(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V, random page permutation)",
-        "config": {"workload": f"{args.config}: batch {B}, KV lengths {shape.lengths} (max {Lmax}), "
-                               f"Hq {shape.num_q_heads}, Hkv {shape.num_kv_heads}, head_dim {shape.head_dim}, "
-                               f"page {shape.page_size}, Tq {shape.q_per_req}, {shape.kv_dtype} KV",
-                   "batch_per_gpu": B, "kv_len": Lmax, "kv_len_mean": Lmean, "num_splits": S,
-                   "num_splits_source": "autotuned", "split_policy": "balanced",
-                   "autotune_s": round(tune_s, 2), "l2": l2_note,
-                   "timing": f"each step one decode call (stage 1 + stage 2); {args.steps} calls replayed from "
-                             f"one CUDA graph between CUDA events",
-                   "bytes_per_step": call_bytes, "parallelism": f"replicas x{world}"},
+        "config": workload_config(args.config, shape, lengths, world, l2_bytes),
+        "run": {"num_splits": S, "num_splits_source": "autotuned", "split_policy": "balanced",
+                "autotune_s": round(tune_s, 2),
+                "timing": f"each step one decode call (stage 1 + stage 2); {args.steps} calls replayed from "
+                          f"one CUDA graph between CUDA events"},
         "spread": trials,
         "fraction_of_hbm_peak": round(value / world / peak, 4),
         "fraction_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
@@ -641,7 +845,8 @@ def run_fd(args):
                      "measured" else "fallback 6.8 TB/s", "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "algorithmic_bytes_per_launch": stage1_bytes,
                      "avg_launch_ms": round(s1_avg_ms, 5), "stage2_avg_ms": round(s2_ms / max(calls, 1), 5),
-                     "profiled_calls": calls},
+                     "profiled_calls": calls, "peak_read_probe": peak_read,
+                     "frac_of_read_probe": round(achieved / peak_read, 4) if peak_read else None},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "e2e_kv_from_host": kv_host,
@@ -649,6 +854,8 @@ def run_fd(args):
         "clocks": clk,
         "sweep": sweep,
         "graph_metadata": meta,
+        "peaks_probe": probes,
+        "configs": configs,
     }
 
 
@@ -687,9 +894,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / max(len(times), 1) * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V, random page permutation)",
-        "config": {"workload": f"{args.config}: batch {shape.batch}, KV length {L} each, Hq {shape.num_q_heads}, "
-                               f"Hkv {shape.num_kv_heads}, head_dim {shape.head_dim}, page {shape.page_size}, "
-                               f"Tq {shape.q_per_req}, {shape.kv_dtype} KV"},
+        "config": workload_config(args.config, shape, w.lengths, world, l2_size()),
         "cpu_baseline": cpu,
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -705,6 +910,8 @@ def main(argv=None):
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-kv-host", action="store_true")
+    ap.add_argument("--no-probes", action="store_true", help="skip the HBM read / copy probes")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' entries")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

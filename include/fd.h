@@ -117,6 +117,11 @@ typedef struct fd_plan fd_plan;
 
 /*
  * fd_plan_create - build a plan for one decode geometry, OUTSIDE graph capture.
+ * No passage defines it (plain reading): the pages' kernels need split
+ * scratch, and a captured call cannot allocate it ("sglang PR 29843"
+ * summary, section 实现拆解 and its test: a captured decode graph reads
+ * metadata buffers prepared per batch size before capture), so it is
+ * allocated once here, with the tuning table beside it.
  *
  *  device          CUDA device ordinal; -1 makes a host-only plan that holds a
  *                  tuning table and validates descriptors but cannot decode
@@ -226,13 +231,16 @@ FD_API fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cache, c
  *
  * Arguments are those of fd_decode_paged, with these differences:
  *  - num_splits must be 1..64 (there is no tuning table), and splits are
- *    always FD_SPLIT_EQUAL;
+ *    always FD_SPLIT_EQUAL, merged by the stage-2 kernel;
  *  - softmax_scale is explicit (0 = 1/sqrt(D));
- *  - the device is the current one.
+ *  - Hq is at most 4096;
+ *  - the device is the current one (compute capability 10.x or later, else
+ *    FD_ERR_UNSUPPORTED).
  *
  * The first call on a device does a one-time set-up: it looks up the array's
- * address and raises the kernels' shared-memory limit. Make that first call
- * before any stream capture.
+ * address, reads the device's SM count and compute capability, and raises
+ * the kernels' shared-memory limit. Make that first call before any stream
+ * capture.
  *
  * All calls share the array. Calls that overlap on the GPU race on it, so
  * serialise them on one stream. Kernel status bits go to an internal word
@@ -309,7 +317,9 @@ FD_API fd_status fd_set_mean_seqlen_hint(fd_plan *plan, int mean_seqlen);
  *  batch_sizes / n_batch  batch sizes to tune (each 1..max_batch).
  *  min_bucket, max_bucket KV-length buckets: powers of two from min_bucket to
  *                         max_bucket (0, 0 = 1024 .. FD_AUTOTUNE_SEQ_LEN or 32768).
- *  stream                 stream for the timing launches.
+ *  stream                 stream whose queued work the timing launches follow
+ *                         (an argument of this library's own: the page tunes
+ *                         inside the engine's process and names no stream).
  *
  * Candidates are num_splits in {1, 2, 3, 4, 6, 8, 12, 16, 32, 64} (up to
  * max_splits), plus the counts
@@ -335,7 +345,8 @@ FD_API fd_status fd_autotune(fd_plan *plan, const int *batch_sizes, int n_batch,
 /* fd_query_splits - the num_splits a num_splits = 0 call would use for
  * (batch, max_seqlen) and the plan's mean-length hint: the tuned entry of the
  * nearest tuned batch and the lookup bucket (see fd_set_mean_seqlen_hint),
- * else the built-in heuristic. Host only. */
+ * else the built-in heuristic. Host only. No passage defines it (plain
+ * reading): it exposes the lookup that fd_decode_paged makes. */
 FD_API fd_status fd_query_splits(fd_plan *plan, int batch, int max_seqlen, int *num_splits);
 
 /* Timer hook for fd_autotune: returns the time of one call with num_splits
@@ -407,7 +418,9 @@ FD_API fd_status fd_autotune_stats(fd_plan *plan, int *searches, int *cache_hits
 
 /* fd_read_device_status - copy the plan's status word (FD_DEVSTAT_* bits) to
  * *code and clear it. Synchronises the plan's device; not for use inside
- * graph capture. Returns FD_ERR_DEVICE_STATUS when any bit was set. */
+ * graph capture. Returns FD_ERR_DEVICE_STATUS when any bit was set. No
+ * passage defines it (plain reading): the kernels record bad page ids and
+ * lengths instead of faulting, and this reads the record. */
 FD_API fd_status fd_read_device_status(fd_plan *plan, int *code);
 
 /* fd_selftest_wait_timeout - run the decode kernels' bounded-wait failure
@@ -423,7 +436,9 @@ FD_API fd_status fd_read_device_status(fd_plan *plan, int *code);
  * a device, FD_ERR_CUDA if the launch fails. */
 FD_API fd_status fd_selftest_wait_timeout(fd_plan *plan, unsigned limit_us, fd_stream_t stream);
 
-/* fd_plan_workspace_bytes - device bytes the plan's split workspace holds. */
+/* fd_plan_workspace_bytes - device bytes the plan's split workspace holds.
+ * No passage defines it (plain reading): introspection of fd_plan_create's
+ * allocation. */
 FD_API fd_status fd_plan_workspace_bytes(fd_plan *plan, size_t *bytes);
 
 /* fd_profile_begin / fd_profile_end - per-stage device time of decode calls.
@@ -440,6 +455,27 @@ FD_API fd_status fd_plan_workspace_bytes(fd_plan *plan, size_t *bytes);
  * graph capture. */
 FD_API fd_status fd_profile_begin(fd_plan *plan);
 FD_API fd_status fd_profile_end(fd_plan *plan, int *calls, double *stage1_ms, double *stage2_ms);
+
+/*
+ * fd_probe_hbm_read / fd_probe_hbm_copy - HBM bandwidth probes. No passage
+ * defines them: they measure, on the same GPU and in the same process, the
+ * denominator of the decode kernels' roofline (the path is bound by HBM
+ * bandwidth on the KV bytes). Both walk the buffer with 16-byte vector
+ * accesses, eight loads in flight per thread, on a grid of four 512-thread
+ * CTAs per SM.
+ *
+ *  fd_probe_hbm_read  reads bytes from src (device) and XORs every 16-byte
+ *                     word of it into sink (device, uint32 [4], 16-byte
+ *                     aligned), so sink ^= XOR of all words: zero sink first
+ *                     to read back the XOR of the buffer.
+ *  fd_probe_hbm_copy  copies bytes from src to dst (device, not overlapping).
+ *
+ * Pointers must be 16-byte aligned and bytes a multiple of 16
+ * (FD_ERR_UNSUPPORTED otherwise); NULL pointers give FD_ERR_INVALID_ARG.
+ * Enqueued on stream on the current device; no allocation, no sync. Time them
+ * with CUDA events over a buffer much larger than L2. */
+FD_API fd_status fd_probe_hbm_read(const void *src, size_t bytes, uint32_t *sink, fd_stream_t stream);
+FD_API fd_status fd_probe_hbm_copy(const void *src, void *dst, size_t bytes, fd_stream_t stream);
 
 /* Static strings; never NULL. */
 FD_API const char *fd_status_string(fd_status status);

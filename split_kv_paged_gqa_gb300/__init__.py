@@ -20,7 +20,7 @@ __all__ = [
     "warmup", "fd_autotune_set_input_hook", "fd_autotune_clear", "fd_autotune", "fd_query_splits",
     "fd_autotune_set_timer", "fd_autotune_set_cache_dir", "fd_autotune_stats",
     "fd_read_device_status", "fd_selftest_wait_timeout", "fd_plan_workspace_bytes", "fd_profile_begin",
-    "fd_profile_end",
+    "fd_profile_end", "fd_probe_hbm_read", "fd_probe_hbm_copy",
     "fd_status_string", "fd_last_error",
     "FD_OK", "FD_ERR_INVALID_ARG", "FD_ERR_UNSUPPORTED", "FD_ERR_WORKSPACE", "FD_ERR_CAPTURING",
     "FD_ERR_CUDA", "FD_ERR_DEVICE_STATUS", "FD_ERR_TIMEOUT", "FD_ERR_NO_PLAN", "FD_ERR_IO",
@@ -107,6 +107,8 @@ def load_library(path: Optional[str] = None):
         "fd_profile_begin": (I, [P]),
         "fd_profile_end": (I, [P, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double),
                                ctypes.POINTER(ctypes.c_double)]),
+        "fd_probe_hbm_read": (I, [P, ctypes.c_size_t, P, P]),
+        "fd_probe_hbm_copy": (I, [P, P, ctypes.c_size_t, P]),
         "fd_status_string": (ctypes.c_char_p, [I]),
         "fd_last_error": (ctypes.c_char_p, []),
     }
@@ -398,3 +400,24 @@ def fd_profile_end(plan: int) -> Tuple[int, float, float]:
     n, a, b = ctypes.c_int(), ctypes.c_double(), ctypes.c_double()
     _check(load_library().fd_profile_end(plan, ctypes.byref(n), ctypes.byref(a), ctypes.byref(b)))
     return n.value, a.value, b.value
+
+
+def fd_probe_hbm_read(src, sink, stream=None) -> None:
+    """Enqueue the read-only HBM probe over all of ``src`` (a contiguous device
+    tensor of a multiple of 16 bytes); every 16-byte word is XORed into
+    ``sink`` (a device tensor of 4 int32 / uint32)."""
+    if not src.is_contiguous() or not sink.is_contiguous():
+        raise ValueError("src and sink must be contiguous")
+    _check(load_library().fd_probe_hbm_read(src.data_ptr(), src.numel() * src.element_size(), sink.data_ptr(),
+                                            _stream_handle(stream)))
+
+
+def fd_probe_hbm_copy(src, dst, stream=None) -> None:
+    """Enqueue the HBM copy probe: all bytes of ``src`` into ``dst`` (contiguous
+    device tensors of the same byte size)."""
+    if not src.is_contiguous() or not dst.is_contiguous():
+        raise ValueError("src and dst must be contiguous")
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("src and dst byte sizes differ")
+    _check(load_library().fd_probe_hbm_copy(src.data_ptr(), dst.data_ptr(), nbytes, _stream_handle(stream)))

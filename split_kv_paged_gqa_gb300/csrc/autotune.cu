@@ -26,6 +26,7 @@
 // the uneven last splits of a mixed batch leave SMs idle that an equal-length
 // batch keeps busy, so the two want different counts. Without any entry a
 // heuristic sizes the grid to two CTAs per SM.
+#include <nvtx3/nvToolsExt.h>
 #include <cuda_runtime.h>
 #include <sys/stat.h>
 
@@ -585,8 +586,18 @@ fd_status fd_autotune(fd_plan *plan, const int *batch_sizes, int n_batch, int mi
     fd_status s = tune_alloc(plan, tb, bmax, max_bucket, st);
     if (s != FD_OK) return s;
   }
+  // NVTX range over the search, one nested range per key (visible to nsys / ncu)
+  nvtxRangePushA("fd_autotune");
+  struct PopRange {
+    ~PopRange() { nvtxRangePop(); }
+  } pop_outer;
   for (auto &key : todo) {
     ++plan->searches;
+    char label[64];
+    std::snprintf(label, sizeof(label), "fd_autotune B=%d K=%d%s", key.first, std::abs(key.second),
+                  key.second < 0 ? " mixed" : "");
+    nvtxRangePushA(label);
+    PopRange pop_key;
     if (!plan->timer && plan->input_hook) {  // representative inputs from the caller
       const int rowe = plan->kv_dtype == FD_INT4X2 ? plan->d / 2 : plan->d;
       const int ng = plan->kv_dtype == FD_INT4X2 ? plan->d / 32 : 1;

@@ -9,6 +9,7 @@
 // cache_seqlens / page_table on the device, with no .item()).
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cmath>
@@ -527,8 +528,11 @@ extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cach
   const bool deep = ctas <= pl->num_sms;
   // the tcgen05 kernel: quantised caches, head_dim 128, one row tile per CTA, merge by stage 2
   const bool tc = pl->quant_tc && pl->kind != fd::KV_BF16 && D == 128 && !p.counters;
+  // NVTX ranges mark each stage's enqueue on the host timeline (nsys / ncu)
+  nvtxRangePushA("fd_stage1");
   cudaError_t e = tc ? fd::launch_stage1_tc(pl->kind, !merge, tmk, tmv, p, grid, st)
                      : fd::launch_stage1(pl->kind, D, !merge, deep, tmk, tmv, p, grid, st);
+  nvtxRangePop();
   if (pl->profiling) FD_CUDA_TRY(cudaEventRecordWithFlags(ev[1], st, rec_flags));
   if (e != cudaSuccess) return fail(FD_ERR_CUDA, "stage-1 launch failed: %s (%d)", cudaGetErrorString(e), (int)e);
   if (merge && !p.counters) {
@@ -556,7 +560,9 @@ extern "C" fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cach
     p2.l_sb = p.l_sb;
     p2.l_st = p.l_st;
     p2.l_sh = p.l_sh;
+    nvtxRangePushA("fd_stage2");
     e = fd::launch_stage2(p2, st, !pl->profiling);
+    nvtxRangePop();
     if (e != cudaSuccess) return fail(FD_ERR_CUDA, "stage-2 launch failed: %s (%d)", cudaGetErrorString(e), (int)e);
   }
   if (pl->profiling) FD_CUDA_TRY(cudaEventRecordWithFlags(ev[2], st, rec_flags));

@@ -11,13 +11,13 @@
 // On the first call on a device, with that device current, the call does a
 // one-time set-up:
 //  * it looks up the array's device address with cudaGetSymbolAddress;
+//  * it reads the device's SM count and compute capability (attribute
+//    queries, which allocate nothing);
 //  * it raises the kernels' shared-memory limit.
 // Make that first call before any stream capture.
 //
-// The array holds the fp32 split partials and, after them, one merge counter
-// per (request, KV head, tile of 16 query rows). The counters start at zero
-// (the array is zeroed when the library's device code loads) and every
-// completed call leaves them at zero.
+// This path always merges splits with the stage-2 kernel: the array holds
+// only the fp32 split partials and their LSEs.
 //
 // The call never allocates. It rejects a workspace need larger than the array
 // with FD_ERR_WORKSPACE. All calls share the array; calls that overlap on the
@@ -37,6 +37,7 @@ namespace {
 
 constexpr size_t kStaticScratchBytes = 32ull << 20;
 constexpr int kMaxDevices = 64;
+constexpr int kMaxHeads = 4096;
 
 // The scratch lives here, in device global memory, one copy per device.
 static __device__ __align__(256) float g_static_scratch[kStaticScratchBytes / sizeof(float)];
@@ -46,6 +47,7 @@ static __device__ __align__(256) unsigned g_static_status;
 struct DeviceSetup {
   float *scratch = nullptr;
   unsigned *status = nullptr;
+  int num_sms = 0;        // the stage-1 variant choice depends on it, as in a plan
   unsigned prepared = 0;  // bit (kind * 2 + (D == 128)) : shared-memory limit raised
 };
 
@@ -66,8 +68,17 @@ fd_status setup_device(int dev, int kind, int head_dim, DeviceSetup *out) {
     e = cudaGetSymbolAddress(&q, g_static_status);
     if (e != cudaSuccess)
       return fd::fail(FD_ERR_CUDA, "cudaGetSymbolAddress(status) failed: %s", cudaGetErrorString(e));
+    int sms = 0, major = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e != cudaSuccess)
+      return fd::fail(FD_ERR_CUDA, "device attribute query failed: %s", cudaGetErrorString(e));
+    if (major < 10)
+      return fd::fail(FD_ERR_UNSUPPORTED, "device %d has compute capability %d.x; the kernels need 10.x or later",
+                      dev, major);
     s.scratch = static_cast<float *>(p);
     s.status = static_cast<unsigned *>(q);
+    s.num_sms = sms;
   }
   const unsigned bit = 1u << (kind * 2 + (head_dim == 128 ? 1 : 0));
   if (!(s.prepared & bit)) {
@@ -107,12 +118,11 @@ extern "C" fd_status fd_decode_paged_static(const fd_tensor *q, const fd_tensor 
   if (D != 64 && D != 128) return fd::fail(FD_ERR_UNSUPPORTED, "head_dim %d not supported (64 or 128)", D);
   if (P < 8 || P > 256 || (P & (P - 1)))
     return fd::fail(FD_ERR_UNSUPPORTED, "page_size %d must be a power of two in [8, 256]", P);
-  if (B < 1 || B > 65535 || Tq < 1 || Tq > 64 || Hkv < 1 || Hq < 1 || Hq % Hkv)
-    return fd::fail(FD_ERR_INVALID_ARG, "bad batch / query tokens / head counts");
+  // (the head bound keeps the size product below in range: < 2^51)
+  if (B < 1 || B > 65535 || Tq < 1 || Tq > 64 || Hkv < 1 || Hq < 1 || Hq > kMaxHeads || Hq % Hkv)
+    return fd::fail(FD_ERR_INVALID_ARG, "bad batch / query tokens / head counts (Hq at most %d)", kMaxHeads);
   const size_t rows = static_cast<size_t>(B) * Tq * Hq * num_splits;
-  const size_t n_ctr = static_cast<size_t>(B) * Hkv * ((Hq / Hkv * Tq + 15) / 16);
-  const size_t need =
-      num_splits > 1 ? rows * (static_cast<size_t>(D) + 1) * sizeof(float) + n_ctr * sizeof(unsigned) : 0;
+  const size_t need = num_splits > 1 ? rows * (static_cast<size_t>(D) + 1) * sizeof(float) : 0;
   if (need > kStaticScratchBytes)
     return fd::fail(FD_ERR_WORKSPACE,
                     "this call needs %zu bytes of split workspace (batch x tokens x heads x splits = %zu rows "
@@ -130,6 +140,7 @@ extern "C" fd_status fd_decode_paged_static(const fd_tensor *q, const fd_tensor 
   // A plan on the stack whose workspace is the static scratch (no allocation).
   fd_plan pl;
   pl.device = dev;
+  pl.num_sms = s.num_sms;
   pl.max_batch = B;
   pl.max_q = Tq;
   pl.hq = Hq;
@@ -148,10 +159,9 @@ extern "C" fd_status fd_decode_paged_static(const fd_tensor *q, const fd_tensor 
   pl.lse_part = s.scratch + rows * D;
   pl.ws_rows = rows;
   pl.status = s.status;
-  // merge counters after the partials: zero when the array is loaded, and every
-  // call leaves them at zero again (the last split of a tile resets its counter)
-  pl.counters = reinterpret_cast<unsigned *>(s.scratch + rows * (D + 1));
-  pl.n_counters = n_ctr;
+  pl.merge_kernel = true;  // splits merge in the stage-2 kernel: no counters
+  pl.counters = nullptr;
+  pl.n_counters = 0;
 
   fd_plan *prev = fd_get_plan();
   fd_set_plan(&pl);

@@ -497,6 +497,72 @@ def test_full_size_sampled(name):
 
 
 # ---------------------------------------------------------------------------
+# the long-context sweep at full size: one 32768-key request, and two requests
+# of the 16-request batch, against the oracle at every num_splits of the sweep
+# (batch 1 at 16 splits runs the one-wave deep variant the tuner picks there),
+# plus agreement between split counts on the whole 16-request batch
+
+
+SWEEP_S = (1, 2, 4, 8, 16, 32, 64)
+
+
+@pytest.fixture(scope="module")
+def long_b1():
+    name = "long_bf16_b1"
+    w = wl.make_workload(wl.CONFIGS[name], wl.CONFIG_SEEDS[name], "cuda", needles=True)
+    inp = wl.oracle_inputs(w)
+    ref = decode_ref_inputs(inp)
+    yield w, inp, ref
+    del w
+    torch.cuda.empty_cache()
+
+
+@pytest.fixture(scope="module")
+def long_b16():
+    name = "long_bf16_b16"
+    w = wl.make_workload(wl.CONFIGS[name], wl.CONFIG_SEEDS[name], "cuda")
+    sample = [3, 12]
+    ref = decode_ref_inputs(wl.oracle_inputs(w, requests=sample))
+    yield w, sample, ref
+    del w
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("S", SWEEP_S)
+def test_full_size_long_b1_every_split_count(long_b1, S):
+    w, inp, (ref_out, ref_lse) = long_b1
+    plan = plan_for(w.shape, max_splits=64)
+    out32, lse32 = run(w, S, torch.float32, plan=plan)
+    assert_parity(out32, lse32, ref_out, ref_lse, label=f"B1 x 32K S={S} fp32 out")
+    out, lse = run(w, S, plan=plan)
+    assert_parity(out, lse, ref_out, ref_lse, label=f"B1 x 32K S={S} bf16 out", bf16_rounding=True)
+    assert_needles(w, out, inp)
+
+
+@pytest.mark.parametrize("S", SWEEP_S)
+def test_full_size_long_b16_every_split_count(long_b16, S):
+    w, sample, (ref_out, ref_lse) = long_b16
+    plan = plan_for(w.shape, max_splits=64)
+    out, lse = run(w, S, plan=plan)
+    assert_parity(out, lse, ref_out, ref_lse, requests=sample, label=f"B16 x 32K S={S}")
+
+
+@pytest.mark.parametrize("policy", ["balanced", "equal"])
+def test_full_size_long_b16_split_agreement(long_b16, policy):
+    w, _, _ = long_b16
+    plan = plan_for(w.shape, max_splits=64)
+    fd.fd_plan_set_split_policy(plan, policy)
+    try:
+        base_f, base_l = run(w, 1, torch.float32, plan=plan)
+        for S in SWEEP_S[1:]:
+            of, lf = run(w, S, torch.float32, plan=plan)
+            assert (of - base_f).abs().max().item() <= SPLIT_ATOL, f"fp32 out S={S}"
+            assert (lf - base_l).abs().max().item() <= SPLIT_ATOL, f"lse S={S}"
+    finally:
+        fd.fd_plan_set_split_policy(plan, "balanced")
+
+
+# ---------------------------------------------------------------------------
 # the startup tuner on the device: both tables, then decode with its pick
 
 

@@ -3,22 +3,26 @@
 Some callers cannot call cudaMalloc: an engine that has reserved all GPU memory
 for its own pool, or a plugin in a process that forbids foreign allocations.
 They call fd_decode_paged_static, which runs the same kernels with a fixed
-scratch array inside the library. Here it is checked, through the C ABI,
-against the plan-based fd_decode_paged on the same inputs, on two calls in a
-row (the second reuses the scratch the first left behind). This file is
-collected last and must pass alone in a fresh process too.
+scratch array inside the library. Here it is checked, through the C ABI, on
+two calls in a row (the second reuses the scratch the first left behind):
+
+* against the float64 oracle, with the parity bar, the tighter gates and the
+  needle rows of the other parity tests;
+* against the plan-based fd_decode_paged on the same inputs;
+* for allocations: after the first calls, further calls leave the device's
+  free memory unchanged.
+
+This file is collected last and must pass alone in a fresh process too.
 """
-import numpy as np
 import pytest
 import torch
 
 import split_kv_paged_gqa_gb300 as fd
+from oracle import decode_ref_inputs
 from split_kv_paged_gqa_gb300 import workloads as wl
+from tests.gpu_common import LSE_ATOL, OUT_ATOL, assert_needles, assert_parity
 
 pytestmark = pytest.mark.gpu
-
-OUT_ATOL = 8e-3
-LSE_ATOL = 1e-3
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -33,6 +37,7 @@ def _plan_call(w, S):
                              s.kv_dtype, 64)
     try:
         fd.fd_set_plan(plan)
+        fd.fd_plan_set_split_policy(plan, "equal")   # the static path always splits equally
         out = torch.empty_like(w.q)
         lse = torch.empty(w.q.shape[:3], dtype=torch.float32, device=w.q.device)
         fd.fd_decode_paged(w.q, w.k_cache, w.v_cache, w.kv_scales, w.page_table, w.cache_seqlens,
@@ -51,6 +56,11 @@ def _close(a_out, a_lse, b_out, b_lse):
     assert (a_lse[fin] - b_lse[fin]).abs().max().item() <= LSE_ATOL
 
 
+def _static_call(w, S, out, lse):
+    fd.fd_decode_paged_static(w.q, w.k_cache, w.v_cache, w.kv_scales, w.page_table, w.cache_seqlens,
+                              w.shape.q_per_req, S, 0.0, out, lse)
+
+
 CASES = [
     # kind, B, Tq, Hq, Hkv, D, P, lengths, num_splits
     ("bf16", 3, 1, 16, 4, 128, 16, (700, 1500, 33), 4),
@@ -61,18 +71,38 @@ CASES = [
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-D{c[5]}-S{c[8]}")
-def test_static_entry_matches_plan_entry_on_two_calls(case):
+def test_static_entry_matches_oracle_and_plan_entry_on_two_calls(case):
     kind, B, Tq, Hq, Hkv, D, P, lengths, S = case
     shape = wl.DecodeShape("static", B, Hq, Hkv, D, P, Tq, kind, "fixed:" + ",".join(map(str, lengths)))
-    w = wl.make_workload(shape, 500 + CASES.index(case), "cuda", poison=True)
-    ref_out, ref_lse = _plan_call(w, S)
-    for _ in range(2):
+    w = wl.make_workload(shape, 500 + CASES.index(case), "cuda", poison=True, needles=True, extra_pages=2)
+    inp = wl.oracle_inputs(w)
+    ref_out, ref_lse = decode_ref_inputs(inp)
+    plan_out, plan_lse = _plan_call(w, S)
+    for call in range(2):
         out = torch.full_like(w.q, float("nan"))
         lse = torch.full(w.q.shape[:3], float("nan"), dtype=torch.float32, device="cuda")
-        fd.fd_decode_paged_static(w.q, w.k_cache, w.v_cache, w.kv_scales, w.page_table, w.cache_seqlens,
-                                  Tq, S, 0.0, out, lse)
+        _static_call(w, S, out, lse)
         torch.cuda.synchronize()
-        _close(out, lse, ref_out, ref_lse)
+        assert_parity(out, lse, ref_out, ref_lse, label=f"static {kind} S={S} call {call}", bf16_rounding=True)
+        assert_needles(w, out, inp)
+        _close(out, lse, plan_out, plan_lse)
+
+
+def test_static_entry_allocates_nothing_on_later_calls():
+    shape = wl.DecodeShape("static", 3, 32, 8, 128, 16, 4, "int4", "fixed:1500,333,2600")
+    w = wl.make_workload(shape, 509, "cuda")
+    out = torch.empty_like(w.q)
+    lse = torch.empty(w.q.shape[:3], dtype=torch.float32, device="cuda")
+    for S in (1, 3):                         # first calls: set-up, both kernels loaded
+        _static_call(w, S, out, lse)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        for S in (1, 3, 8):
+            _static_call(w, S, out, lse)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, f"device free memory moved by {free0 - free1} bytes across static calls"
 
 
 def test_static_entry_rejects_workspace_beyond_its_array():
