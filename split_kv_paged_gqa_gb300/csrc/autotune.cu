@@ -253,6 +253,23 @@ void make_desc(fd_tensor &t, void *data, fd_dtype dt, std::initializer_list<int6
   }
 }
 
+// The tuner's scale buffer: logical [2, N, P, Hkv, ng], stored head-major
+// within a page ([2, N, Hkv, P, ng] in memory) as the workloads store them, so
+// the scales of one (page, head) are contiguous.
+void make_scale_desc(fd_tensor &t, void *data, int64_t pool, int page, int hkv, int ng) {
+  std::memset(&t, 0, sizeof(t));
+  t.data = data;
+  t.dtype = FD_FP32;
+  t.ndim = 5;
+  const int64_t shape[5] = {2, pool, page, hkv, ng};
+  const int64_t stride[5] = {pool * hkv * page * ng, static_cast<int64_t>(hkv) * page * ng, ng,
+                             static_cast<int64_t>(page) * ng, 1};
+  for (int i = 0; i < 5; ++i) {
+    t.shape[i] = shape[i];
+    t.stride[i] = stride[i];
+  }
+}
+
 // Device time of one call with `S` splits in the steady state of a decode
 // loop: a CUDA graph of n_seq calls, each on pages of its own, replayed back
 // to back (each call's start overlaps the previous call's end). The calls of
@@ -278,7 +295,7 @@ fd_status tune_time(fd_plan *pl, TuneBuffers &tb, int batch, int bucket, bool mi
   make_desc(q, tb.q, FD_BF16, {batch, tb.tq, pl->hq, pl->d});
   make_desc(k, tb.k, pl->kv_dtype, {tb.pool_pages, pl->page, pl->hkv, rowe});
   make_desc(v, tb.v, pl->kv_dtype, {tb.pool_pages, pl->page, pl->hkv, rowe});
-  make_desc(sc, tb.scales, FD_FP32, {2, tb.pool_pages, pl->page, pl->hkv, ng});
+  make_scale_desc(sc, tb.scales, tb.pool_pages, pl->page, pl->hkv, ng);
   make_desc(sq, tb.sl, FD_INT32, {batch});
   make_desc(out, tb.out, FD_BF16, {batch, tb.tq, pl->hq, pl->d});
   make_desc(lse, tb.lse, FD_FP32, {batch, tb.tq, pl->hq});
@@ -605,7 +622,7 @@ fd_status fd_autotune(fd_plan *plan, const int *batch_sizes, int n_batch, int mi
       make_desc(q, tb.q, FD_BF16, {key.first, tb.tq, plan->hq, plan->d});
       make_desc(k, tb.k, plan->kv_dtype, {tb.pool_pages, plan->page, plan->hkv, rowe});
       make_desc(v, tb.v, plan->kv_dtype, {tb.pool_pages, plan->page, plan->hkv, rowe});
-      make_desc(sc, tb.scales, FD_FP32, {2, tb.pool_pages, plan->page, plan->hkv, ng});
+      make_scale_desc(sc, tb.scales, tb.pool_pages, plan->page, plan->hkv, ng);
       fd_status hs = plan->input_hook(plan->input_user, key.first, std::abs(key.second), key.second < 0 ? 1 : 0, &q,
                                       &k, &v, tb.scales ? &sc : nullptr, reinterpret_cast<fd_stream_t>(st));
       if (hs != FD_OK) return fail(hs, "autotune: the input hook returned %d", (int)hs);

@@ -6,9 +6,9 @@
 // stream reaches; a copy moves as many bytes out as in and pays the bus
 // turnarounds between reads and writes, so it sits a little lower.
 //
-// Both kernels walk the buffer with 16-byte vector accesses in a grid-stride
-// loop, eight independent loads in flight per thread, on a grid of a whole
-// number of CTAs per SM. The read kernel folds every word it loads into an
+// Both kernels walk the buffer with 16-byte vector accesses, eight
+// independent loads in flight per thread, on a grid of a whole number of CTAs
+// per SM, each CTA streaming through 64 KiB tiles of consecutive memory. The read kernel folds every word it loads into an
 // XOR per thread and combines those into the caller's 16-byte sink with one
 // atomic per warp, so no load can be dropped by the compiler and the sink
 // holds a checkable value: the XOR of all 16-byte words of the buffer.
@@ -33,14 +33,21 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
   return v;
 }
 
+// The buffer is cut into tiles of kThreads * kUnroll words (64 KiB), dealt to
+// the CTAs round robin; within a tile, load u of thread t takes word
+// u * kThreads + t, so each of a CTA's kUnroll loads in flight covers 8 KiB of
+// consecutive memory (DRAM pages stay open, as with the decode kernels' TMA
+// boxes of whole cache pages).
+constexpr size_t kTile = static_cast<size_t>(kThreads) * kUnroll;
+
 __global__ void __launch_bounds__(kThreads) hbm_read_kernel(const uint4 *__restrict__ src, size_t n, uint32_t *sink) {
   uint4 acc = make_uint4(0u, 0u, 0u, 0u);
-  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-  size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (; i + (kUnroll - 1) * stride < n; i += kUnroll * stride) {
+  const size_t full_tiles = n / kTile;
+  for (size_t t = blockIdx.x; t < full_tiles; t += gridDim.x) {
+    const uint4 *p = src + t * kTile + threadIdx.x;
     uint4 v[kUnroll];
 #pragma unroll
-    for (int k = 0; k < kUnroll; ++k) v[k] = ld_stream(src + i + k * stride);
+    for (int k = 0; k < kUnroll; ++k) v[k] = ld_stream(p + k * kThreads);
 #pragma unroll
     for (int k = 0; k < kUnroll; ++k) {
       acc.x ^= v[k].x;
@@ -49,12 +56,15 @@ __global__ void __launch_bounds__(kThreads) hbm_read_kernel(const uint4 *__restr
       acc.w ^= v[k].w;
     }
   }
-  for (; i < n; i += stride) {
-    const uint4 v = ld_stream(src + i);
-    acc.x ^= v.x;
-    acc.y ^= v.y;
-    acc.z ^= v.z;
-    acc.w ^= v.w;
+  // the partial last tile, word by word
+  if (blockIdx.x == full_tiles % gridDim.x) {
+    for (size_t i = full_tiles * kTile + threadIdx.x; i < n; i += kThreads) {
+      const uint4 v = ld_stream(src + i);
+      acc.x ^= v.x;
+      acc.y ^= v.y;
+      acc.z ^= v.z;
+      acc.w ^= v.w;
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -71,18 +81,25 @@ __global__ void __launch_bounds__(kThreads) hbm_read_kernel(const uint4 *__restr
   }
 }
 
+__device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads) hbm_copy_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
                                                           size_t n) {
-  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-  size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (; i + (kUnroll - 1) * stride < n; i += kUnroll * stride) {
+  const size_t full_tiles = n / kTile;
+  for (size_t t = blockIdx.x; t < full_tiles; t += gridDim.x) {
+    const size_t base = t * kTile + threadIdx.x;
     uint4 v[kUnroll];
 #pragma unroll
-    for (int k = 0; k < kUnroll; ++k) v[k] = ld_stream(src + i + k * stride);
+    for (int k = 0; k < kUnroll; ++k) v[k] = ld_stream(src + base + k * kThreads);
 #pragma unroll
-    for (int k = 0; k < kUnroll; ++k) dst[i + k * stride] = v[k];
+    for (int k = 0; k < kUnroll; ++k) st_stream(dst + base + k * kThreads, v[k]);
   }
-  for (; i < n; i += stride) dst[i] = ld_stream(src + i);
+  if (blockIdx.x == full_tiles % gridDim.x) {
+    for (size_t i = full_tiles * kTile + threadIdx.x; i < n; i += kThreads) st_stream(dst + i, ld_stream(src + i));
+  }
 }
 
 fd_status probe_grid(size_t n16, unsigned *grid) {
@@ -92,7 +109,7 @@ fd_status probe_grid(size_t n16, unsigned *grid) {
   if (e != cudaSuccess) return fd::fail(FD_ERR_CUDA, "device query failed: %s", cudaGetErrorString(e));
   // a whole number of CTAs per SM, fewer when the buffer is small
   const size_t full = static_cast<size_t>(sms) * kCtasPerSm;
-  const size_t need = (n16 + kThreads - 1) / kThreads;
+  const size_t need = (n16 + kTile - 1) / kTile;
   *grid = static_cast<unsigned>(need < full ? (need > 0 ? need : 1) : full);
   return FD_OK;
 }

@@ -27,7 +27,11 @@ Recipe (every draw is seeded):
   An all-zero group gets scale 0 and codes 0.
 * ``kv_scales`` is fp32 ``[2, num_pages, P, Hkv, n_g]`` (index 0 = K, 1 = V),
   ``n_g = 1`` for int8 and ``D / 32`` for int4: the scale of a cache row sits
-  at the same (page, slot, head) index as the row.
+  at the same (page, slot, head) index as the row. In memory the scales are
+  stored head-major within a page (``[2, num_pages, Hkv, P, n_g]``, handed
+  out as a strided view with the logical index order above), so the scales of
+  one (page, head) are one contiguous run, as a cache writer that keeps a
+  page's per-head metadata together stores them.
 
 Optional structure used by the parity tests:
 
@@ -113,7 +117,7 @@ class Workload:
     q: torch.Tensor                 # bf16 [B, Tq, Hq, D]
     k_cache: torch.Tensor           # bf16/int8 [N, P, Hkv, D] or uint8 [N, P, Hkv, D/2]
     v_cache: torch.Tensor
-    kv_scales: Optional[torch.Tensor]  # fp32 [2, N, P, Hkv, n_g] or None
+    kv_scales: Optional[torch.Tensor]  # fp32 [2, N, P, Hkv, n_g] (head-major in memory) or None
     page_table: torch.Tensor        # int32 [B, max_pages], -1 padded
     cache_seqlens: torch.Tensor     # int32 [B]
     lengths: np.ndarray             # int64 [B], host copy
@@ -268,7 +272,7 @@ def make_workload(shape: DecodeShape, seed: int, device="cpu", *, poison: bool =
     k_cache = torch.empty((pool, P, Hkv, row_dim), dtype=cache_dtype, device=device)
     v_cache = torch.empty_like(k_cache)
     n_g = 1 if shape.kv_dtype == "int8" else D // 32
-    kv_scales = (torch.empty((2, pool, P, Hkv, n_g), dtype=torch.float32, device=device)
+    kv_scales = (torch.empty((2, pool, Hkv, P, n_g), dtype=torch.float32, device=device).permute(0, 1, 3, 2, 4)
                  if shape.kv_dtype != "bf16" else None)
 
     pages_per_chunk = max(1, chunk_elems // (P * Hkv * D))

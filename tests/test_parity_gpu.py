@@ -1,4 +1,6 @@
 """GPU parity of the CUDA path (through the C ABI) against the float64 oracle."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -75,6 +77,25 @@ def test_parity_cases(case, S):
     out, lse = run(w, S)
     assert_parity(out, lse, ref_out, ref_lse, label=f"{case} S={S} bf16 out", bf16_rounding=True)
     assert_needles(w, out, inp)
+
+
+# The scales of a quantised cache in two memory orders: head-major within a
+# page (the workloads' order: the scales of one (page, head) are contiguous)
+# and the logical order [2, N, P, Hkv, n_g] made contiguous (the 8 heads of a
+# slot interleaved).
+@pytest.mark.parametrize("case", [c for c in CASES if c[0] != "bf16"],
+                         ids=lambda c: f"{c[0]}-B{c[1]}-T{c[2]}-H{c[3]}/{c[4]}-D{c[5]}-P{c[6]}")
+def test_parity_scale_memory_orders(case):
+    shape = _shape(*case)
+    w = wl.make_workload(shape, 300 + CASES.index(case), "cuda", poison=True, needles=True, extra_pages=2)
+    inp = wl.oracle_inputs(w)
+    ref_out, ref_lse = decode_ref_inputs(inp)
+    assert w.kv_scales.stride(2) == w.kv_scales.shape[4]          # head-major: slots contiguous
+    for scales in (w.kv_scales, w.kv_scales.contiguous()):
+        w2 = dataclasses.replace(w, kv_scales=scales)
+        for S in (1, 3):
+            out32, lse32 = run(w2, S, torch.float32)
+            assert_parity(out32, lse32, ref_out, ref_lse, label=f"{case} S={S} strides {scales.stride()}")
 
 
 # Stage tails. The 16-row INT4 tile and the narrow INT8 tile take 32 keys per
