@@ -353,8 +353,8 @@ PROBE_BYTES = 2 << 30   # probe buffer: 1 Gi bf16 elements, as the driver's copy
 
 def measure_probes(fd, dev, trials: int = 10) -> dict:
     """HBM read-only and copy bandwidth from this library's probe kernels
-    (16-byte vector accesses over 2 GiB, far above L2), best and median of
-    ``trials`` CUDA-event timings each; copy counts read + write bytes."""
+    over 2 GiB (far above L2), best and median of ``trials`` CUDA-event
+    timings each; copy counts read + write bytes."""
     import torch
     src = torch.empty(PROBE_BYTES // 2, dtype=torch.bfloat16, device=dev)
     src.view(torch.int16).random_(generator=torch.Generator(device=dev).manual_seed(0))
@@ -384,9 +384,9 @@ def measure_probes(fd, dev, trials: int = 10) -> dict:
     return {"read_gbs": round(rd, 1), "read_gbs_median": round(rd_med, 1), "copy_gbs": round(cp, 1),
             "copy_gbs_median": round(cp_med, 1), "copy_verified": ok, "buffer_bytes": PROBE_BYTES,
             "trials": trials,
-            "what": "fd_probe_hbm_read (XOR-fold of 16-byte loads) and fd_probe_hbm_copy (16-byte loads and "
-                    "stores), 4 CTAs of 512 threads per SM, 8 loads in flight per thread; best of the trials; "
-                    "copy counts read + write bytes"}
+            "what": "fd_probe_hbm_read (bulk copies of 32 KiB chunks into a 6-stage shared-memory ring per SM, "
+                    "folded by XOR, as the decode kernels read) and fd_probe_hbm_copy (16-byte loads and streaming "
+                    "stores, 4 CTAs of 512 threads per SM); best of the trials; copy counts read + write bytes"}
 
 
 # Workloads measured beside the headline in the default run (one entry each

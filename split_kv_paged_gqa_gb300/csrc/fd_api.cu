@@ -309,8 +309,13 @@ fd_status encode_cache_map(CUtensorMap *map, const fd_tensor *c, const fd_plan *
   CUtensorMapDataType dt = c->dtype == FD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(FD_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  CUresult r = fn(map, dt, 4, c->data, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  // L2 promotion: whole 256-byte lines, except for 64-byte rows (int4, head
+  // dim 128), where a 256-byte line spans four heads' rows of a slot and the
+  // neighbours' CTAs often find it evicted (evict-first) before they read it
+  const CUtensorMapL2promotion promo =
+      box_bytes <= 64 ? CU_TENSOR_MAP_L2_PROMOTION_L2_64B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
+  CUresult r = fn(map, dt, 4, c->data, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, promo,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FD_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled rejected the cache layout (%d)", (int)r);
   return FD_OK;
 }
