@@ -385,8 +385,9 @@ def measure_probes(fd, dev, trials: int = 10) -> dict:
             "copy_gbs_median": round(cp_med, 1), "copy_verified": ok, "buffer_bytes": PROBE_BYTES,
             "trials": trials,
             "what": "fd_probe_hbm_read (bulk copies of 32 KiB chunks into a 6-stage shared-memory ring per SM, "
-                    "folded by XOR, as the decode kernels read) and fd_probe_hbm_copy (16-byte loads and streaming "
-                    "stores, 4 CTAs of 512 threads per SM); best of the trials; copy counts read + write bytes"}
+                    "one run of consecutive chunks per CTA, folded by XOR, as the decode kernels read) and "
+                    "fd_probe_hbm_copy (16-byte loads and stores, 4 CTAs of 512 threads per SM); best of the "
+                    "trials; copy counts read + write bytes"}
 
 
 # Workloads measured beside the headline in the default run (one entry each

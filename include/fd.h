@@ -462,9 +462,9 @@ FD_API fd_status fd_profile_end(fd_plan *plan, int *calls, double *stage1_ms, do
  * denominator of the decode kernels' roofline (the path is bound by HBM
  * bandwidth on the KV bytes). The read probe reads as the decode kernels do:
  * bulk copies (TMA) of 32 KiB chunks into a six-stage shared-memory ring per
- * SM, folded by the CTA's other warps. The copy probe moves 16-byte vectors
- * with plain loads and streaming stores, eight loads in flight per thread,
- * four 512-thread CTAs per SM.
+ * SM, each CTA streaming one run of consecutive chunks, folded by the CTA's
+ * other warps. The copy probe moves 16-byte vectors, eight loads in flight
+ * per thread, four 512-thread CTAs per SM.
  *
  *  fd_probe_hbm_read  reads bytes from src (device) and XORs every 16-byte
  *                     word of it into sink (device, uint32 [4], 16-byte
