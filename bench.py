@@ -513,6 +513,8 @@ def run_fd(args):
     __graft_entry__.build()
     dev = torch.device("cuda", local)
     shape = wl.CONFIGS[args.config]
+    if args.batch:  # a smaller (or larger) batch of the same workload, e.g. for small profiling cases
+        shape = shape.with_(batch=args.batch)
     seed = wl.CONFIG_SEEDS[args.config] + rank
     B = shape.batch
     # the step's lengths, drawn as the workload generator draws them
@@ -913,6 +915,8 @@ def main(argv=None):
     ap.add_argument("--skip-kv-host", action="store_true")
     ap.add_argument("--no-probes", action="store_true", help="skip the HBM read / copy probes")
     ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' entries")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="run the workload with this batch instead of its own (small profiling cases)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

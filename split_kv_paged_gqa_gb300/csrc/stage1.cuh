@@ -31,12 +31,18 @@
 //        the matching channel order (a dot product does not care about the
 //        order of its terms). K scales multiply the fp32 scores (per
 //        32-channel group for int4, from one accumulator per group).
-//      - V: thread (g, c) owns D/8 consecutive channels of its 4 keys; a
-//        byte permute pairs two keys' codes at one channel, giving exact fp16
-//        B fragments; PV output columns come out permuted and are put back in
-//        order by the epilogue. int8 folds the per-key V scale into the
-//        probabilities (fp16); int4 multiplies its per-group V scale into the
-//        fp16 V values, and keeps O in tensor memory between blocks.
+//      - V, int8: thread (g, c) owns D/8 consecutive channels of its 4 keys;
+//        a byte permute pairs two keys' codes at one channel, giving exact
+//        fp16 B fragments; the per-key V scale is folded into the
+//        probabilities (fp16).
+//      - V, int4: ldmatrix.trans of 8 keys x one scale group's 16 bytes hands
+//        each thread the 4 nibbles of two keys at 4 channels of the group, so
+//        every PV n-tile lies inside one 32-channel group; the group's V
+//        scale multiplies the probabilities (one P operand per group) and the
+//        codes need only their bias removed. O stays in tensor memory between
+//        blocks.
+//        PV output columns come out permuted and are put back in order by the
+//        epilogue.
 //    Quantised tiles of at most 8 rows ("narrow", warp_block_km) swap the
 //    roles: keys and channels are the M dimension, the rows the 8-wide N
 //    dimension, so the MMAs and the softmax carry no empty rows.
@@ -559,9 +565,8 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
       }
     }
   } else {
-    static_assert(NT % 8 == 0, "int4 V words");
+    static_assert(NT == 4 * NG, "int4: four n-tiles per 32-channel scale group");
     static_assert(C::O_TMEM, "int4 keeps O in tensor memory");
-    constexpr int NW = NT / 8;  // 32-bit words per key
     // O from tensor memory: it waits there through the score half of the
     // block, which then runs with D/2 fewer live registers (the previous
     // block's store has long landed; the wait only orders it before the load)
@@ -569,50 +574,53 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
     tmem_wait_st();
 #pragma unroll
     for (int i = 0; i < NT / 8; ++i) tmem_ld32(tm_o + 32 * i, &ot[8 * i][0]);
-    const int grp = (g * NT) / 32;
-    uint32_t w[KB][4][NW];
-    uint32_t sA[KB], sB[KB];
+    // V-scale pairs per group of the thread's keys (2c, 2c + 1) and
+    // (2c + 8, 2c + 9) of each sub-block; 0 for keys past the split end
+    uint32_t sp0[KB][NG], sp1[KB][NG];
 #pragma unroll
     for (int kb = 0; kb < KB; ++kb) {
-      float vsf[4];
+      float sk[4][NG];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint8_t *src = vt + swz<SW>(vrows[kb][i] * RB + g * (NT / 2));
-        if constexpr (NW == 2) {
-          const uint2 v = *reinterpret_cast<const uint2 *>(src);
-          w[kb][i][0] = v.x;
-          w[kb][i][1] = v.y;
-        } else {
-          w[kb][i][0] = *reinterpret_cast<const uint32_t *>(src);
-        }
-        vsf[i] = valid[kb][i] ? vsc[vrows[kb][i] * NG + grp] : 0.f;
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) sk[i][gi] = valid[kb][i] ? vsc[vrows[kb][i] * NG + gi] : 0.f;
       }
-      sA[kb] = pack_f16x2(vsf[0], vsf[1]);
-      sB[kb] = pack_f16x2(vsf[2], vsf[3]);
+#pragma unroll
+      for (int gi = 0; gi < NG; ++gi) {
+        sp0[kb][gi] = pack_f16x2(sk[0][gi], sk[1][gi]);
+        sp1[kb][gi] = pack_f16x2(sk[2][gi], sk[3][gi]);
+      }
     }
     tmem_wait_ld();
     rescale_o(ot);
+    // V codes paired by ldmatrix.trans: matrix (keys 8h .. 8h + 7 of the
+    // sub-block, 16 bytes of group gi) gives thread (g, c) the 4 nibbles
+    // (channels 32 gi + 4 g .. + 3) of keys 8h + 2c and 8h + 2c + 1; n-tile
+    // 4 gi + q holds channel 32 gi + 4 n + q at MMA column n. Each group's V
+    // scale multiplies the probabilities (the A operand) instead of V.
+    const uint32_t vbase = smem_u32(vt);
 #pragma unroll
     for (int kb = 0; kb < KB; ++kb) {
 #pragma unroll
-      for (int k = 0; k < NW; ++k) {
+      for (int gp = 0; gp < NG; gp += 2) {  // two groups per ldmatrix.x4
+        uint32_t R[4];  // (keys 0-7, gp), (keys 8-15, gp), (keys 0-7, gp + 1), (keys 8-15, gp + 1)
+        const int key = row0 + 16 * kb + 8 * ((lane >> 3) & 1) + (lane & 7);
+        ldsm_x4_t(R, vbase + swz<SW>(key * RB + 16 * (gp + (lane >> 4))));
 #pragma unroll
-        for (int hb = 0; hb < 2; ++hb) {  // bytes 0-1, then 2-3, of each key's word
-          const uint32_t sel = hb ? 0x7632u : 0x5410u;
-          const uint32_t tA = __byte_perm(w[kb][0][k], w[kb][1][k], sel);
-          const uint32_t tB = __byte_perm(w[kb][2][k], w[kb][3][k], sel);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {  // nibble q: channel g*NT + 8k + 4hb + q
-            uint32_t xa, xb;
-            if (q & 1) {  // high nibble reads 1024 + 16u: /16 - 72 = code
-              xa = hfma2_u32(nib_hi_f16_biased(tA >> (4 * (q - 1)), nib_hi), 1.0f / 16.0f, -72.0f);
-              xb = hfma2_u32(nib_hi_f16_biased(tB >> (4 * (q - 1)), nib_hi), 1.0f / 16.0f, -72.0f);
-            } else {
-              xa = hsub2_u32(nib_lo_f16_biased(tA >> (4 * q), nib_lo), 1032.0f);
-              xb = hsub2_u32(nib_lo_f16_biased(tB >> (4 * q), nib_lo), 1032.0f);
-            }
-            mma_f16_16816(ot[8 * k + 4 * hb + q], pa[kb], hmul2_u32(xa, sA[kb]), hmul2_u32(xb, sB[kb]));
-          }
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int gi = gp + h2;
+          const uint32_t aw[4] = {hmul2_u32(pa[kb][0], sp0[kb][gi]), hmul2_u32(pa[kb][1], sp0[kb][gi]),
+                                  hmul2_u32(pa[kb][2], sp1[kb][gi]), hmul2_u32(pa[kb][3], sp1[kb][gi])};
+          const uint32_t lo = R[2 * h2], hi = R[2 * h2 + 1];
+          const uint32_t lo8 = lo >> 8, hi8 = hi >> 8;
+          mma_f16_16816(ot[4 * gi + 0], aw, hsub2_u32(nib_lo_f16_biased(lo, nib_lo), 1032.0f),
+                        hsub2_u32(nib_lo_f16_biased(hi, nib_lo), 1032.0f));
+          mma_f16_16816(ot[4 * gi + 1], aw, hfma2_u32(nib_hi_f16_biased(lo, nib_hi), 1.0f / 16.0f, -72.0f),
+                        hfma2_u32(nib_hi_f16_biased(hi, nib_hi), 1.0f / 16.0f, -72.0f));
+          mma_f16_16816(ot[4 * gi + 2], aw, hsub2_u32(nib_lo_f16_biased(lo8, nib_lo), 1032.0f),
+                        hsub2_u32(nib_lo_f16_biased(hi8, nib_lo), 1032.0f));
+          mma_f16_16816(ot[4 * gi + 3], aw, hfma2_u32(nib_hi_f16_biased(lo8, nib_hi), 1.0f / 16.0f, -72.0f),
+                        hfma2_u32(nib_hi_f16_biased(hi8, nib_hi), 1.0f / 16.0f, -72.0f));
         }
       }
     }
@@ -1559,7 +1567,13 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
       float *w1 = co + (warp * 16 + g + 8) * C::CROW;
 #pragma unroll
       for (int j = 0; j < D / 8; ++j) {
-        if constexpr (C::QUANT) {  // n-tile j, d-slot n holds channel n * NT + j
+        if constexpr (KIND == KV_I4) {  // n-tile j = 4 gi + q, column n holds channel 32 gi + 4 n + q
+          const int ch = 32 * (j / 4) + 8 * c + (j % 4);
+          w0[ch] = o[j][0];
+          w0[ch + 4] = o[j][1];
+          w1[ch] = o[j][2];
+          w1[ch + 4] = o[j][3];
+        } else if constexpr (C::QUANT) {  // n-tile j, d-slot n holds channel n * NT + j
           w0[(2 * c) * C::NT + j] = o[j][0];
           w0[(2 * c + 1) * C::NT + j] = o[j][1];
           w1[(2 * c) * C::NT + j] = o[j][2];
