@@ -31,10 +31,12 @@
 //        the matching channel order (a dot product does not care about the
 //        order of its terms). K scales multiply the fp32 scores (per
 //        32-channel group for int4, from one accumulator per group).
-//      - V, int8: thread (g, c) owns D/8 consecutive channels of its 4 keys;
-//        a byte permute pairs two keys' codes at one channel, giving exact
-//        fp16 B fragments; the per-key V scale is folded into the
-//        probabilities (fp16).
+//      - V, int8 (16-row tile): thread (g, c) owns D/8 consecutive channels
+//        of its 4 keys; a byte permute pairs two keys' codes at one channel,
+//        giving exact fp16 B fragments; the per-key V scale is folded into
+//        the probabilities (fp16). The narrow tiles (int8 and int4) take
+//        their V A fragments from ldmatrix.trans, which pairs two keys' codes
+//        without byte permutes.
 //      - V, int4: ldmatrix.trans of 8 keys x one scale group's 16 bytes hands
 //        each thread the 4 nibbles of two keys at 4 channels of the group, so
 //        every PV n-tile lies inside one 32-channel group; the group's V
@@ -640,9 +642,10 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
 // of warp_block_q's B fragments (qb[ks] = that order's row-g Q fragment).
 // S^T's fragment holds keys (g, g + 8) x rows (2c, 2c + 1): a row's max
 // reduces over the 8 lanes of one c. P^T reaches the B-fragment layout of PV
-// through two 8x8 transposes (movmatrix). V codes become A fragments with
-// warp_block_q's byte permutes: m-tile j, slots g / g + 8 hold channels
-// g*NT + 2j / g*NT + 2j + 1 of rows (2c, 2c + 1) in o[j][0,1] / o[j][2,3].
+// through two 8x8 transposes (movmatrix). V codes become A fragments from
+// ldmatrix.trans (see the V^T step below for the channel of each m-tile
+// slot); o[j][0,1] / o[j][2,3] hold the m-tile's slot g / g + 8 channel for
+// rows (2c, 2c + 1).
 // l holds the thread's partial row sums over its keys (reduced across the 8
 // lanes of a row by the caller); m is the full row max.
 template <class C, int KIND>
@@ -791,85 +794,68 @@ __device__ __forceinline__ void warp_block_km(const uint8_t *kt, const uint8_t *
     pb1[kb] = movmatrix_trans(pack_f16x2(p[kb][2], p[kb][3]));
   }
 
-  // ---- V^T as A fragments: keys (2c, 2c+1) and (2c+8, 2c+9) of each
-  // sub-block, channels [g*NT, g*NT + NT). Keys at or past c1 read as 0.
+  // ---- V^T as A fragments, from ldmatrix.trans of 8 keys x 16 bytes: thread
+  // (g, c) gets the 16-bit element g of keys 2c and 2c + 1 (and of 2c + 8,
+  // 2c + 9 from the next matrix), so each register pairs two keys' codes as
+  // the MMA wants them, with no byte permutes. Keys at or past c1 meet a zero
+  // probability (their codes are finite) and, int4, a zero V scale.
+  //   int8: m-tile j = channels 16 j ..: row g = channel 16 j + 2 g (bytes 0
+  //         and 2 of the register), row g + 8 = 16 j + 2 g + 1 (bytes 1, 3).
+  //   int4: m-tile j = 2 gi + qq inside scale group gi: row g = channel
+  //         32 gi + 4 g + 2 qq, row g + 8 = the next channel; the group's V
+  //         scale multiplies the probabilities (the B operand).
+  const uint32_t vbase = smem_u32(vt);
 #pragma unroll
   for (int kb = 0; kb < KB; ++kb) {
-    const int kA = row0 + 16 * kb + 2 * c, kB = kA + 8;
-    const int vrows[4] = {kA, kA + 1, kB, kB + 1};
-    bool valid[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) valid[i] = full || tok_row0 + (vrows[i] - row0) < c1;
+    const int key = row0 + 16 * kb + 8 * ((lane >> 3) & 1) + (lane & 7);
     if constexpr (KIND == KV_I8) {
-      static_assert(NT % 4 == 0, "int8 V words");
-      constexpr int NW = NT / 4;  // 32-bit words per key
-      uint32_t w[4][NW];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint8_t *src = vt + swz<SW>(vrows[i] * RB + g * NT);
-        if constexpr (NW == 4) {
-          const uint4 v = *reinterpret_cast<const uint4 *>(src);
-          w[i][0] = v.x;
-          w[i][1] = v.y;
-          w[i][2] = v.z;
-          w[i][3] = v.w;
-        } else {
-          const uint2 v = *reinterpret_cast<const uint2 *>(src);
-          w[i][0] = v.x;
-          w[i][1] = v.y;
-        }
-      }
-      if (!full) {  // keys past the split end read as code 0 (a raw 0)
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int k = 0; k < NW; ++k) w[i][k] = valid[i] ? w[i][k] : 0u;
-      }
+      static_assert(C::OT % 2 == 0, "int8: 16-channel slices in pairs");
       const uint32_t u8_bias = kU8Bias;
-      auto pair = [&](uint32_t wa, uint32_t wb, int bi) {  // byte bi of two keys -> exact f16x2 codes
-        const uint32_t sel = bi | (bi << 4) | ((4u + bi) << 8) | ((4u + bi) << 12);
-        return hsub2_u32(i8pair_to_f16_biased(__byte_perm(wa, wb, sel), u8_bias), 1152.0f);
-      };
 #pragma unroll
-      for (int j = 0; j < C::OT; ++j) {  // channels g*NT + 2j, + 1: word j / 2, bytes 2 (j % 2) + {0, 1}
-        const int k = j / 2, bi = 2 * (j % 2);
-        const uint32_t a[4] = {pair(w[0][k], w[1][k], bi), pair(w[0][k], w[1][k], bi + 1),
-                               pair(w[2][k], w[3][k], bi), pair(w[2][k], w[3][k], bi + 1)};
-        mma_f16_16816(o[j], a, pb0[kb], pb1[kb]);
+      for (int sp = 0; sp < C::OT; sp += 2) {
+        uint32_t R[4];  // (keys 0-7, slice sp), (keys 8-15, sp), (keys 0-7, sp + 1), (keys 8-15, sp + 1)
+        ldsm_x4_t(R, vbase + swz<SW>(key * RB + 16 * (sp + (lane >> 4))));
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const uint32_t lo = R[2 * h2], hi = R[2 * h2 + 1];
+          const uint32_t a[4] = {hsub2_u32(i8pair_to_f16_biased(lo, u8_bias), 1152.0f),
+                                 hsub2_u32(i8pair_to_f16_biased(lo >> 8, u8_bias), 1152.0f),
+                                 hsub2_u32(i8pair_to_f16_biased(hi, u8_bias), 1152.0f),
+                                 hsub2_u32(i8pair_to_f16_biased(hi >> 8, u8_bias), 1152.0f)};
+          mma_f16_16816(o[sp + h2], a, pb0[kb], pb1[kb]);
+        }
       }
     } else {
-      static_assert(NT % 8 == 0, "int4 V words");
-      constexpr int NW = NT / 8;  // 32-bit words per key
-      const int grp = (g * NT) / 32;
-      uint32_t w[4][NW];
-      float vsf[4];
+      static_assert(C::OT == 2 * NG && NG % 2 == 0, "int4: two m-tiles per 32-channel scale group");
+      const int kA = row0 + 16 * kb + 2 * c, kB = kA + 8;
+      const int vrows[4] = {kA, kA + 1, kB, kB + 1};
+      float sk[4][NG];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint8_t *src = vt + swz<SW>(vrows[i] * RB + g * (NT / 2));
-        if constexpr (NW == 2) {
-          const uint2 v = *reinterpret_cast<const uint2 *>(src);
-          w[i][0] = v.x;
-          w[i][1] = v.y;
-        } else {
-          w[i][0] = *reinterpret_cast<const uint32_t *>(src);
-        }
-        vsf[i] = valid[i] ? vsc[vrows[i] * NG + grp] : 0.f;
+        const bool valid = full || tok_row0 + (vrows[i] - row0) < c1;
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) sk[i][gi] = valid ? vsc[vrows[i] * NG + gi] : 0.f;
       }
-      const uint32_t sA = pack_f16x2(vsf[0], vsf[1]);
-      const uint32_t sB = pack_f16x2(vsf[2], vsf[3]);
       auto code = [&](uint32_t t, int q) {  // nibble q of two keys -> exact f16x2 codes
         return (q & 1) ? hfma2_u32(nib_hi_f16_biased(t >> (4 * (q - 1)), nib_hi), 1.0f / 16.0f, -72.0f)
                        : hsub2_u32(nib_lo_f16_biased(t >> (4 * q), nib_lo), 1032.0f);
       };
 #pragma unroll
-      for (int j = 0; j < C::OT; ++j) {  // channels g*NT + 2j, + 1: word j / 4, bytes 2 ((j / 2) % 2) + {0, 1}
-        const int k = j / 4, hb = (j / 2) % 2, q = 2 * (j % 2);
-        const uint32_t sel = hb ? 0x7632u : 0x5410u;
-        const uint32_t tA = __byte_perm(w[0][k], w[1][k], sel);
-        const uint32_t tB = __byte_perm(w[2][k], w[3][k], sel);
-        const uint32_t a[4] = {hmul2_u32(code(tA, q), sA), hmul2_u32(code(tA, q + 1), sA),
-                               hmul2_u32(code(tB, q), sB), hmul2_u32(code(tB, q + 1), sB)};
-        mma_f16_16816(o[j], a, pb0[kb], pb1[kb]);
+      for (int gp = 0; gp < NG; gp += 2) {
+        uint32_t R[4];  // (keys 0-7, group gp), (keys 8-15, gp), (keys 0-7, gp + 1), (keys 8-15, gp + 1)
+        ldsm_x4_t(R, vbase + swz<SW>(key * RB + 16 * (gp + (lane >> 4))));
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int gi = gp + h2;
+          const uint32_t b0 = hmul2_u32(pb0[kb], pack_f16x2(sk[0][gi], sk[1][gi]));
+          const uint32_t b1 = hmul2_u32(pb1[kb], pack_f16x2(sk[2][gi], sk[3][gi]));
+          const uint32_t lo = R[2 * h2], hi = R[2 * h2 + 1];
+#pragma unroll
+          for (int qq = 0; qq < 2; ++qq) {
+            const uint32_t a[4] = {code(lo, 2 * qq), code(lo, 2 * qq + 1), code(hi, 2 * qq), code(hi, 2 * qq + 1)};
+            mma_f16_16816(o[2 * gi + qq], a, b0, b1);
+          }
+        }
       }
     }
   }
@@ -1546,14 +1532,16 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
     float *cm = reinterpret_cast<float *>(smem + C::CMB_O);
     float *cl = cm + C::NUM_CW * C::TR;
     if constexpr (NARROW) {
-      // rows 2c, 2c + 1: o[j] = (channel g*NT + 2j: rows 2c, 2c+1), (g*NT + 2j + 1: rows 2c, 2c+1)
+      // rows 2c, 2c + 1: o[j] = (channel ch: rows 2c, 2c+1), (ch + 1: rows 2c, 2c+1), ch below
       const int c = lane & 3;
-      float *w0 = co + (warp * C::TR + 2 * c) * C::CROW + g * C::NT;
+      float *w0 = co + (warp * C::TR + 2 * c) * C::CROW;
       float *w1 = w0 + C::CROW;
 #pragma unroll
       for (int j = 0; j < C::OT; ++j) {
-        *reinterpret_cast<float2 *>(w0 + 2 * j) = make_float2(o[j][0], o[j][2]);
-        *reinterpret_cast<float2 *>(w1 + 2 * j) = make_float2(o[j][1], o[j][3]);
+        // m-tile j: channel pair (row g, row g + 8) of the m-tile (see warp_block_km)
+        const int ch = KIND == KV_I8 ? 16 * j + 2 * g : 32 * (j / 2) + 4 * g + 2 * (j % 2);
+        *reinterpret_cast<float2 *>(w0 + ch) = make_float2(o[j][0], o[j][2]);
+        *reinterpret_cast<float2 *>(w1 + ch) = make_float2(o[j][1], o[j][3]);
       }
       if (g == 0) {
         cm[warp * C::TR + 2 * c] = m[0];
