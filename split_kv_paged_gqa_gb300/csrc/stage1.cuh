@@ -31,12 +31,10 @@
 //        the matching channel order (a dot product does not care about the
 //        order of its terms). K scales multiply the fp32 scores (per
 //        32-channel group for int4, from one accumulator per group).
-//      - V, int8 (16-row tile): thread (g, c) owns D/8 consecutive channels
-//        of its 4 keys; a byte permute pairs two keys' codes at one channel,
-//        giving exact fp16 B fragments; the per-key V scale is folded into
-//        the probabilities (fp16). The narrow tiles (int8 and int4) take
-//        their V A fragments from ldmatrix.trans, which pairs two keys' codes
-//        without byte permutes.
+//      - V, int8: ldmatrix.trans of 8 keys x 16 channels pairs two keys'
+//        codes at a channel in one register (bytes 0, 2 and 1, 3), so each
+//        fp16 fragment takes one LOP3 and one subtract; the per-key V scale
+//        is folded into the probabilities (fp16).
 //      - V, int4: ldmatrix.trans of 8 keys x one scale group's 16 bytes hands
 //        each thread the 4 nibbles of two keys at 4 channels of the group, so
 //        every PV n-tile lies inside one 32-channel group; the group's V
@@ -508,9 +506,8 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
     }
   }
 
-  // ---- V fragments: keys (2c, 2c+1) -> b0b1, (2c+8, 2c+9) -> b2b3 of each
-  // sub-block, channels [g*NT, g*NT + NT), one channel per n-tile. Keys at or
-  // past c1 read as 0.
+  // ---- V fragments: keys (2c, 2c+1) -> b0, (2c+8, 2c+9) -> b1 of each
+  // sub-block (the int4 V scales of keys at or past c1 read as 0)
   int vrows[KB][4];
   bool valid[KB][4];
 #pragma unroll
@@ -526,43 +523,28 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
   if constexpr (KIND == KV_I8) {
     static_assert(NT % 4 == 0, "int8 V words");
     static_assert(!C::O_TMEM, "int8 keeps O in registers");
-    constexpr int NW = NT / 4;  // 32-bit words per key
+    // ldmatrix.trans of 8 keys x 16 channels (16 bytes) gives thread (g, c)
+    // the codes of channels 16 s + 2 g and + 1 of keys 2c, 2c + 1 (bytes 0, 2
+    // and 1, 3 of the register): n-tile 2 s + e holds channel 16 s + 2 n + e
+    // at MMA column n. Keys at or past c1 meet a zero probability (their codes
+    // are finite).
+    const uint32_t vbase = smem_u32(vt);
+    const uint32_t u8_bias = kU8Bias;
 #pragma unroll
     for (int kb = 0; kb < KB; ++kb) {
-      uint32_t w[4][NW];
+      const int key = row0 + 16 * kb + 8 * ((lane >> 3) & 1) + (lane & 7);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint8_t *src = vt + swz<SW>(vrows[kb][i] * RB + g * NT);
-        if constexpr (NW == 4) {
-          const uint4 v = *reinterpret_cast<const uint4 *>(src);
-          w[i][0] = v.x;
-          w[i][1] = v.y;
-          w[i][2] = v.z;
-          w[i][3] = v.w;
-        } else {
-          const uint2 v = *reinterpret_cast<const uint2 *>(src);
-          w[i][0] = v.x;
-          w[i][1] = v.y;
-        }
-      }
-      if (!full) {  // keys past the split end read as code 0 (a raw 0)
+      for (int sp = 0; sp < C::D / 16; sp += 2) {
+        uint32_t R[4];  // (keys 0-7, slice sp), (keys 8-15, sp), (keys 0-7, sp + 1), (keys 8-15, sp + 1)
+        ldsm_x4_t(R, vbase + swz<SW>(key * RB + 16 * (sp + (lane >> 4))));
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int k = 0; k < NW; ++k) w[i][k] = valid[kb][i] ? w[i][k] : 0u;
-      }
-      const uint32_t u8_bias = kU8Bias;
-#pragma unroll
-      for (int k = 0; k < NW; ++k) {
-#pragma unroll
-        for (int bi = 0; bi < 4; ++bi) {
-          // byte bi of both keys -> bits 0-7 and 16-23: channel g*NT + 4k + bi
-          const uint32_t sel = (bi) | (bi << 4) | ((4u + bi) << 8) | ((4u + bi) << 12);
-          const uint32_t b0 =
-              hsub2_u32(i8pair_to_f16_biased(__byte_perm(w[0][k], w[1][k], sel), u8_bias), 1152.0f);
-          const uint32_t b1 =
-              hsub2_u32(i8pair_to_f16_biased(__byte_perm(w[2][k], w[3][k], sel), u8_bias), 1152.0f);
-          mma_f16_16816(o[4 * k + bi], pa[kb], b0, b1);
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int sl = sp + h2;
+          const uint32_t lo = R[2 * h2], hi = R[2 * h2 + 1];
+          mma_f16_16816(o[2 * sl], pa[kb], hsub2_u32(i8pair_to_f16_biased(lo, u8_bias), 1152.0f),
+                        hsub2_u32(i8pair_to_f16_biased(hi, u8_bias), 1152.0f));
+          mma_f16_16816(o[2 * sl + 1], pa[kb], hsub2_u32(i8pair_to_f16_biased(lo >> 8, u8_bias), 1152.0f),
+                        hsub2_u32(i8pair_to_f16_biased(hi >> 8, u8_bias), 1152.0f));
         }
       }
     }
@@ -1561,11 +1543,12 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
           w0[ch + 4] = o[j][1];
           w1[ch] = o[j][2];
           w1[ch + 4] = o[j][3];
-        } else if constexpr (C::QUANT) {  // n-tile j, d-slot n holds channel n * NT + j
-          w0[(2 * c) * C::NT + j] = o[j][0];
-          w0[(2 * c + 1) * C::NT + j] = o[j][1];
-          w1[(2 * c) * C::NT + j] = o[j][2];
-          w1[(2 * c + 1) * C::NT + j] = o[j][3];
+        } else if constexpr (C::QUANT) {  // int8: n-tile j = 2 s + e, column n holds channel 16 s + 2 n + e
+          const int ch = 16 * (j / 2) + 4 * c + (j % 2);
+          w0[ch] = o[j][0];
+          w0[ch + 2] = o[j][1];
+          w1[ch] = o[j][2];
+          w1[ch + 2] = o[j][3];
         } else {
           *reinterpret_cast<float2 *>(w0 + j * 8 + 2 * c) = make_float2(o[j][0], o[j][1]);
           *reinterpret_cast<float2 *>(w1 + j * 8 + 2 * c) = make_float2(o[j][2], o[j][3]);
