@@ -132,6 +132,9 @@ struct S1Cfg {
   // (int8 measured faster with O in registers; narrow O is half the size)
   static constexpr bool O_TMEM = KIND == KV_I4 && !NARROW;
   static constexpr int TMEM_COLS = D / 2;
+  // int8 V codes enter PV as subnormals (kU8Sub): one fragment of bias row sums
+  static constexpr bool V_SUB = KIND == KV_I8;
+  static constexpr int NR = 1;
   static constexpr int OFF_TMEM = OFF_META + 16;
   static constexpr int SMEM = OFF_TMEM + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;         // slack to align the base to 1024
@@ -148,14 +151,6 @@ struct S1Cfg {
 // ----------------------------------------------------------------------------
 // In-register conversions of cache codes to fp16 (exact: |code| <= 128).
 
-// f16x2 (1024 + u_lo, 1024 + u_hi), u = code + 128, from the raw int8 codes
-// at bits 0-7 and 16-23 (u = code ^ 0x80): mask, sign flip and exponent in
-// one LOP3, with c = kU8Bias in a register.
-constexpr uint32_t kU8Bias = 0x64806480u;
-__device__ __forceinline__ uint32_t i8pair_to_f16_biased(uint32_t t, uint32_t c) {
-  return and_xor<0x00FF00FFu>(t, c);
-}
-
 // int4 codes are stored as two's-complement nibbles n = code & 15, and
 // n ^ 8 = code + 8 = u in [0, 15]. From the nibbles at bits 0-3 and 16-19:
 // f16x2 (1024 + u, 1024 + u'); from those at bits 4-7 and 20-23:
@@ -168,6 +163,21 @@ __device__ __forceinline__ uint32_t nib_lo_f16_biased(uint32_t t, uint32_t c) {
 __device__ __forceinline__ uint32_t nib_hi_f16_biased(uint32_t t, uint32_t c) {
   return and_xor<0x00F000F0u>(t, c);
 }
+
+// int8 V codes enter PV as fp16 subnormals: a half whose bits are u < 1024
+// has the value u * 2^-24 exactly, so one LOP3 (mask, and flip the code's
+// sign bit: u = code + 128) gives the operand pair, with no fp16
+// subtraction. The bias left in the products is 128 times the row sum R of
+// the probability operand over the keys; one more MMA against ones per
+// 16-key sub-block accumulates R beside O, and the epilogue takes
+// O = 2^24 O_raw - 128 R (remove_v_bias). Products and R are exact in fp32
+// before accumulation, and for codes of either sign the bias term is of the
+// order of the result, so the cancellation costs a bit or two of the sum.
+// (int4 keeps exact biased fp16 codes: its sixteen bias sums per block,
+// one per scale group, cost more registers than the subtractions they save.)
+constexpr uint32_t kU8Sub = 0x00800080u;     // bytes 0 and 2: u = code ^ 0x80
+constexpr uint32_t kOnesF16 = 0x3C003C00u;   // f16x2 (1, 1)
+__device__ __forceinline__ uint32_t i8pair_to_f16_sub(uint32_t t, uint32_t c) { return and_xor<0x00FF00FFu>(t, c); }
 
 // ----------------------------------------------------------------------------
 // One 16-key block of one warp, bf16 cache: scores, online softmax, PV.
@@ -347,8 +357,9 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
                                              const float *vsc, int row0,
                                              const uint32_t (&qa)[C::D / 16][4],
                                              const float (&qc)[2][C::NG], const float (&rs)[2],
-                                             float (&o)[C::NT][4], uint32_t tm_o, float (&m)[2], float (&l)[2],
-                                             int tok_row0, int c1, int lim0, int lim1, int lane) {
+                                             float (&o)[C::NT][4], float (&ra)[C::NR][4], uint32_t tm_o,
+                                             float (&m)[2], float (&l)[2], int tok_row0, int c1, int lim0,
+                                             int lim1, int lane) {
   constexpr int NG = C::NG, RB = C::ROW_BYTES, SW = C::BOX_BYTES, NT = C::NT;
   constexpr int KB = C::KPW / 16;  // 16-key sub-blocks
   constexpr int CH = RB / 16;      // 16-byte chunks per cache row
@@ -468,10 +479,10 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
   // folds the V scale into P, so it keeps the exact running max
   const bool rescale = softmax_update_kb<KB, KIND == KV_I4>(s, p, m, l, al);
   // alpha-rescale of O if the max moved
-  auto rescale_o = [&](float (&oo)[NT][4]) {
+  auto rescale_o = [&](auto &oo) {  // O fragments and the V-bias row sums alike
     if (rescale) {
 #pragma unroll
-      for (int j = 0; j < NT; ++j) {
+      for (int j = 0; j < static_cast<int>(sizeof(oo) / sizeof(oo[0])); ++j) {
         oo[j][0] *= al[0];
         oo[j][1] *= al[0];
         oo[j][2] *= al[1];
@@ -480,6 +491,7 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
     }
   };
   if constexpr (!C::O_TMEM) rescale_o(o);  // (O in tensor memory is rescaled once loaded)
+  if constexpr (C::V_SUB) rescale_o(ra);
 
   // ---- P as the fp16 A operand (int8: the per-key V scale folded in)
   uint32_t pa[KB][4];
@@ -492,7 +504,7 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float vs = vsc[row0 + 16 * kb + nt * 8 + 2 * c + (e & 1)];
-          pv[nt][e] = p[kb][nt][e] == 0.f ? 0.f : p[kb][nt][e] * vs;
+          pv[nt][e] = p[kb][nt][e] * vs;
         }
       pa[kb][0] = pack_f16x2(pv[0][0], pv[0][1]);
       pa[kb][1] = pack_f16x2(pv[0][2], pv[0][3]);
@@ -507,9 +519,9 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
   }
 
   // ---- V fragments: keys (2c, 2c+1) -> b0, (2c+8, 2c+9) -> b1 of each
-  // sub-block (the int4 V scales of keys at or past c1 read as 0)
+  // sub-block (keys at or past c1 meet a zero probability; their codes and
+  // scales are finite)
   int vrows[KB][4];
-  bool valid[KB][4];
 #pragma unroll
   for (int kb = 0; kb < KB; ++kb) {
     const int kA = row0 + 16 * kb + 2 * c, kB = kA + 8;
@@ -517,8 +529,6 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
     vrows[kb][1] = kA + 1;
     vrows[kb][2] = kB;
     vrows[kb][3] = kB + 1;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) valid[kb][i] = full || tok_row0 + (vrows[kb][i] - row0) < c1;
   }
   if constexpr (KIND == KV_I8) {
     static_assert(NT % 4 == 0, "int8 V words");
@@ -527,11 +537,12 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
     // the codes of channels 16 s + 2 g and + 1 of keys 2c, 2c + 1 (bytes 0, 2
     // and 1, 3 of the register): n-tile 2 s + e holds channel 16 s + 2 n + e
     // at MMA column n. Keys at or past c1 meet a zero probability (their codes
-    // are finite).
+    // are finite). Codes as subnormals; ra accumulates the row sums of P.
     const uint32_t vbase = smem_u32(vt);
-    const uint32_t u8_bias = kU8Bias;
+    const uint32_t u8_sub = kU8Sub, ones = kOnesF16;
 #pragma unroll
     for (int kb = 0; kb < KB; ++kb) {
+      mma_f16_16816(ra[0], pa[kb], ones, ones);
       const int key = row0 + 16 * kb + 8 * ((lane >> 3) & 1) + (lane & 7);
 #pragma unroll
       for (int sp = 0; sp < C::D / 16; sp += 2) {
@@ -541,10 +552,9 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
         for (int h2 = 0; h2 < 2; ++h2) {
           const int sl = sp + h2;
           const uint32_t lo = R[2 * h2], hi = R[2 * h2 + 1];
-          mma_f16_16816(o[2 * sl], pa[kb], hsub2_u32(i8pair_to_f16_biased(lo, u8_bias), 1152.0f),
-                        hsub2_u32(i8pair_to_f16_biased(hi, u8_bias), 1152.0f));
-          mma_f16_16816(o[2 * sl + 1], pa[kb], hsub2_u32(i8pair_to_f16_biased(lo >> 8, u8_bias), 1152.0f),
-                        hsub2_u32(i8pair_to_f16_biased(hi >> 8, u8_bias), 1152.0f));
+          mma_f16_16816(o[2 * sl], pa[kb], i8pair_to_f16_sub(lo, u8_sub), i8pair_to_f16_sub(hi, u8_sub));
+          mma_f16_16816(o[2 * sl + 1], pa[kb], i8pair_to_f16_sub(lo >> 8, u8_sub),
+                        i8pair_to_f16_sub(hi >> 8, u8_sub));
         }
       }
     }
@@ -559,7 +569,7 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
 #pragma unroll
     for (int i = 0; i < NT / 8; ++i) tmem_ld32(tm_o + 32 * i, &ot[8 * i][0]);
     // V-scale pairs per group of the thread's keys (2c, 2c + 1) and
-    // (2c + 8, 2c + 9) of each sub-block; 0 for keys past the split end
+    // (2c + 8, 2c + 9) of each sub-block
     uint32_t sp0[KB][NG], sp1[KB][NG];
 #pragma unroll
     for (int kb = 0; kb < KB; ++kb) {
@@ -567,7 +577,7 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
 #pragma unroll
-        for (int gi = 0; gi < NG; ++gi) sk[i][gi] = valid[kb][i] ? vsc[vrows[kb][i] * NG + gi] : 0.f;
+        for (int gi = 0; gi < NG; ++gi) sk[i][gi] = vsc[vrows[kb][i] * NG + gi];
       }
 #pragma unroll
       for (int gi = 0; gi < NG; ++gi) {
@@ -634,8 +644,8 @@ template <class C, int KIND>
 __device__ __forceinline__ void warp_block_km(const uint8_t *kt, const uint8_t *vt, const float *ksc,
                                               const float *vsc, int row0, const uint32_t (&qb)[C::D / 16][2],
                                               const float (&qc)[2][C::NG], const float (&rs)[2],
-                                              float (&o)[C::OT][4], float (&m)[2], float (&l)[2], int tok_row0,
-                                              int c1, int lim0, int lim1, int lane) {
+                                              float (&o)[C::OT][4], float (&ra)[C::NR][4], float (&m)[2],
+                                              float (&l)[2], int tok_row0, int c1, int lim0, int lim1, int lane) {
   constexpr int NG = C::NG, RB = C::ROW_BYTES, SW = C::BOX_BYTES, NT = C::NT;
   constexpr int KB = C::KPW / 16;  // 16-key sub-blocks
   constexpr int CH = RB / 16;      // 16-byte chunks per cache row
@@ -754,6 +764,12 @@ __device__ __forceinline__ void warp_block_km(const uint8_t *kt, const uint8_t *
       o[j][2] *= al0;
       o[j][3] *= al1;
     }
+    if constexpr (C::V_SUB) {
+      ra[0][0] *= al0;
+      ra[0][1] *= al1;
+      ra[0][2] *= al0;
+      ra[0][3] *= al1;
+    }
   }
 
   // ---- P^T -> the B fragments of PV (int8: the per-key V scale folded in)
@@ -761,11 +777,7 @@ __device__ __forceinline__ void warp_block_km(const uint8_t *kt, const uint8_t *
 #pragma unroll
   for (int kb = 0; kb < KB; ++kb) {
     if constexpr (KIND == KV_I8) {
-      float vg = vsc[row0 + 16 * kb + g], v8 = vsc[row0 + 16 * kb + g + 8];
-      if (!full) {  // the scale of a key past the split end may be anything: it meets p = 0
-        if (tok_row0 + 16 * kb + g >= c1) vg = 0.f;
-        if (tok_row0 + 16 * kb + g + 8 >= c1) v8 = 0.f;
-      }
+      const float vg = vsc[row0 + 16 * kb + g], v8 = vsc[row0 + 16 * kb + g + 8];
       p[kb][0] *= vg;
       p[kb][1] *= vg;
       p[kb][2] *= v8;
@@ -780,19 +792,24 @@ __device__ __forceinline__ void warp_block_km(const uint8_t *kt, const uint8_t *
   // (g, c) gets the 16-bit element g of keys 2c and 2c + 1 (and of 2c + 8,
   // 2c + 9 from the next matrix), so each register pairs two keys' codes as
   // the MMA wants them, with no byte permutes. Keys at or past c1 meet a zero
-  // probability (their codes are finite) and, int4, a zero V scale.
+  // probability (their codes and scales are finite).
   //   int8: m-tile j = channels 16 j ..: row g = channel 16 j + 2 g (bytes 0
   //         and 2 of the register), row g + 8 = 16 j + 2 g + 1 (bytes 1, 3).
   //   int4: m-tile j = 2 gi + qq inside scale group gi: row g = channel
   //         32 gi + 4 g + 2 qq, row g + 8 = the next channel; the group's V
   //         scale multiplies the probabilities (the B operand).
+  // int8 codes enter as subnormals, and ra sums the B operand over the keys
+  // (an MMA with an A operand of ones).
   const uint32_t vbase = smem_u32(vt);
+  const uint32_t ones = kOnesF16;
+  const uint32_t ones4[4] = {ones, ones, ones, ones};
 #pragma unroll
   for (int kb = 0; kb < KB; ++kb) {
     const int key = row0 + 16 * kb + 8 * ((lane >> 3) & 1) + (lane & 7);
     if constexpr (KIND == KV_I8) {
       static_assert(C::OT % 2 == 0, "int8: 16-channel slices in pairs");
-      const uint32_t u8_bias = kU8Bias;
+      const uint32_t u8_sub = kU8Sub;
+      mma_f16_16816(ra[0], ones4, pb0[kb], pb1[kb]);
 #pragma unroll
       for (int sp = 0; sp < C::OT; sp += 2) {
         uint32_t R[4];  // (keys 0-7, slice sp), (keys 8-15, sp), (keys 0-7, sp + 1), (keys 8-15, sp + 1)
@@ -800,10 +817,8 @@ __device__ __forceinline__ void warp_block_km(const uint8_t *kt, const uint8_t *
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           const uint32_t lo = R[2 * h2], hi = R[2 * h2 + 1];
-          const uint32_t a[4] = {hsub2_u32(i8pair_to_f16_biased(lo, u8_bias), 1152.0f),
-                                 hsub2_u32(i8pair_to_f16_biased(lo >> 8, u8_bias), 1152.0f),
-                                 hsub2_u32(i8pair_to_f16_biased(hi, u8_bias), 1152.0f),
-                                 hsub2_u32(i8pair_to_f16_biased(hi >> 8, u8_bias), 1152.0f)};
+          const uint32_t a[4] = {i8pair_to_f16_sub(lo, u8_sub), i8pair_to_f16_sub(lo >> 8, u8_sub),
+                                 i8pair_to_f16_sub(hi, u8_sub), i8pair_to_f16_sub(hi >> 8, u8_sub)};
           mma_f16_16816(o[sp + h2], a, pb0[kb], pb1[kb]);
         }
       }
@@ -814,9 +829,8 @@ __device__ __forceinline__ void warp_block_km(const uint8_t *kt, const uint8_t *
       float sk[4][NG];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const bool valid = full || tok_row0 + (vrows[i] - row0) < c1;
 #pragma unroll
-        for (int gi = 0; gi < NG; ++gi) sk[i][gi] = valid ? vsc[vrows[i] * NG + gi] : 0.f;
+        for (int gi = 0; gi < NG; ++gi) sk[i][gi] = vsc[vrows[i] * NG + gi];
       }
       auto code = [&](uint32_t t, int q) {  // nibble q of two keys -> exact f16x2 codes
         return (q & 1) ? hfma2_u32(nib_hi_f16_biased(t >> (4 * (q - 1)), nib_hi), 1.0f / 16.0f, -72.0f)
@@ -840,6 +854,18 @@ __device__ __forceinline__ void warp_block_km(const uint8_t *kt, const uint8_t *
         }
       }
     }
+  }
+}
+
+// The int8 V codes entered PV as subnormals (see kU8Sub): O = 2^24 O_raw -
+// 128 R, with R the row sums in ra[0], whose entries line up with those of
+// every O fragment (16-row: rows g, g + 8; narrow: rows 2c, 2c + 1).
+template <class C>
+__device__ __forceinline__ void remove_v_bias(float (&o)[C::OT][4], const float (&ra)[C::NR][4]) {
+#pragma unroll
+  for (int j = 0; j < C::OT; ++j) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[j][e] = fmaf(o[j][e], 16777216.0f, -128.0f * ra[0][e]);
   }
 }
 
@@ -1115,6 +1141,16 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
       mbar_init(&empty[i], C::NUM_CW);
     }
     fence_mbar_init();
+  }
+  if constexpr (C::QUANT) {
+    // The scale slots start at zero. The producer fills only the slots of
+    // keys before the split end, so a slot past it holds zero or a scale of
+    // an earlier block of this split: always a finite value (for finite
+    // inputs), which meets a zero probability without a selection.
+    constexpr int N16 = 2 * C::SC / 16;
+    for (int i = threadIdx.x; i < C::STAGES * N16; i += C::THREADS)
+      *reinterpret_cast<uint4 *>(smem + (i / N16) * C::STAGE + 2 * C::TILE + (i % N16) * 16) =
+          make_uint4(0u, 0u, 0u, 0u);
   }
   __syncthreads();
 
@@ -1409,8 +1445,11 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
     }
 
     float o[C::OT][4];
+    float ra[C::NR][4];  // quantised V: the bias row sums (registers unless O is in tensor memory)
 #pragma unroll
     for (int j = 0; j < C::OT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+#pragma unroll
+    for (int j = 0; j < C::NR; ++j) ra[j][0] = ra[j][1] = ra[j][2] = ra[j][3] = 0.f;
     // warp w's threads own TMEM lanes 32w .. 32w + 31
     const uint32_t tm_o = C::O_TMEM ? *tmem_slot + ((static_cast<uint32_t>(warp) * 32u) << 16) : 0u;
     if constexpr (C::O_TMEM) {
@@ -1443,8 +1482,8 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
               qr[ks][0] = v.x;
               qr[ks][1] = v.y;
             }
-            warp_block_km<C, KIND>(kt, vt, ksc, vsc, row0, qr, qc, rs, o, m, l, tok_row0, c1, lim[0], lim[1],
-                                   lane);
+            warp_block_km<C, KIND>(kt, vt, ksc, vsc, row0, qr, qc, rs, o, ra, m, l, tok_row0, c1, lim[0],
+                                   lim[1], lane);
           } else {
             static_assert(C::QA_SMEM, "the 16-row quantised block reads its Q fragments from shared memory");
             uint32_t qf[D / 16][4];
@@ -1457,8 +1496,8 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
               qf[ks][2] = v.z;
               qf[ks][3] = v.w;
             }
-            warp_block_q<C, KIND>(kt, vt, ksc, vsc, row0, qf, qc, rs, o, tm_o, m, l, tok_row0, c1, lim[0],
-                                  lim[1], lane);
+            warp_block_q<C, KIND>(kt, vt, ksc, vsc, row0, qf, qc, rs, o, ra, tm_o, m, l, tok_row0, c1,
+                                  lim[0], lim[1], lane);
           }
         } else {
           if (tok_row0 + 16 > c1) {  // zero V rows past the split end before PV
@@ -1490,6 +1529,7 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
       tmem_wait_ld();
       tc_fence_before();
     }
+    if constexpr (C::V_SUB) remove_v_bias<C>(o, ra);
 
     // ---- merge the consumer warps' (max, sum, O) through shared memory
     // (a row's partial sums sit in the 4 lanes of a quad, or, narrow, in the
