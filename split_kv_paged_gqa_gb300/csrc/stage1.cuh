@@ -992,6 +992,36 @@ __device__ __forceinline__ void write_row_outputs(const Stage1Params &p, bool fu
   }
 }
 
+// One output row from a warp: lane l holds columns 2l + 64k and 2l + 64k + 1
+// in vals[k]; lane 0 writes the LSE. Destinations as in write_row_outputs.
+template <class C>
+__device__ __forceinline__ void write_row_pairs(const Stage1Params &p, bool fused, int b, int h, int s,
+                                                int row_glob, int lane, const float2 (&vals)[C::D / 64],
+                                                float lse_nat) {
+  const int t = row_glob / p.G, g = row_glob - t * p.G;
+  const int hq = h * p.G + g;
+  if (fused) {
+    if (p.out_f32) {
+      float *dst = reinterpret_cast<float *>(p.out) + b * p.o_sb + t * p.o_st + hq * p.o_sh + 2 * lane;
+#pragma unroll
+      for (int k = 0; k < C::D / 64; ++k) *reinterpret_cast<float2 *>(dst + 64 * k) = vals[k];
+    } else {
+      __nv_bfloat16 *dst =
+          reinterpret_cast<__nv_bfloat16 *>(p.out) + b * p.o_sb + t * p.o_st + hq * p.o_sh + 2 * lane;
+#pragma unroll
+      for (int k = 0; k < C::D / 64; ++k)
+        *reinterpret_cast<uint32_t *>(dst + 64 * k) = pack_bf16x2(vals[k].x, vals[k].y);
+    }
+    if (lane == 0 && p.lse) p.lse[b * p.l_sb + t * p.l_st + hq * p.l_sh] = lse_nat;
+  } else {
+    const int64_t rowi = ((static_cast<int64_t>(b) * p.Tq + t) * p.Hq + hq) * p.s_cap + s;
+    float *dst = p.o_part + rowi * C::D + 2 * lane;
+#pragma unroll
+    for (int k = 0; k < C::D / 64; ++k) *reinterpret_cast<float2 *>(dst + 64 * k) = vals[k];
+    if (lane == 0) p.lse_part[rowi] = lse_nat;
+  }
+}
+
 // The merge of the last split CTA of a tile: for each of the tile's rows, the
 // nv non-empty split partials (o_s, lse_s) combine as
 //   M = max_s lse_s, w_s = exp(lse_s - M), out = sum w_s o_s / sum w_s,
@@ -1602,37 +1632,59 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
       }
     }
     named_barrier(1, C::NUM_CW * 32);
-    if (threadIdx.x < 8 * C::TR) {  // 8 threads per row of the tile (narrow: 8 rows)
-      constexpr int TPR = 8;
-      constexpr int DPT = D / TPR;  // columns per thread
-      const int tid = threadIdx.x;
-      const int row = tid / TPR;
-      const int d0 = (tid % TPR) * DPT;
-      const int rg = rt * 16 + row;
-      float mw[C::NUM_CW], wt[C::NUM_CW];
+    // Lane r of every consumer warp forms row r's weights (lanes past the
+    // tile's rows repeat them); then each warp combines whole rows, lane l
+    // taking the column pairs 2l + 64k, so every read of a partial row is 256
+    // consecutive bytes (conflict-free) and every store coalesced. The rows
+    // of a warp are unrolled so their loads overlap.
+    static_assert(C::TR % C::NUM_CW == 0, "rows per consumer warp");
+    float wl[C::NUM_CW], inv_l, lse_l;
+    {
+      const int rr = lane % C::TR;
+      float mw[C::NUM_CW];
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < C::NUM_CW; ++w) {
-        mw[w] = cm[w * C::TR + row];
+        mw[w] = cm[w * C::TR + rr];
         M = fmaxf(M, mw[w]);
       }
       float Lsum = 0.f;
 #pragma unroll
       for (int w = 0; w < C::NUM_CW; ++w) {
-        wt[w] = mw[w] == -INFINITY ? 0.f : fast_exp2(mw[w] - M);
-        Lsum = fmaf(wt[w], cl[w * C::TR + row], Lsum);
+        wl[w] = mw[w] == -INFINITY ? 0.f : fast_exp2(mw[w] - M);
+        Lsum = fmaf(wl[w], cl[w * C::TR + rr], Lsum);
       }
-      const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-      const float lse_nat = Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
-      float vals[DPT];
+      inv_l = Lsum > 0.f ? 1.f / Lsum : 0.f;
+      lse_l = Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
+    }
+    auto combine_row = [&](int i) {
+      const int row = warp + i * C::NUM_CW;
+      const int rg = rt * 16 + row;
+      float wt[C::NUM_CW];
 #pragma unroll
-      for (int i = 0; i < DPT; ++i) {
-        float a = 0.f;
+      for (int w = 0; w < C::NUM_CW; ++w) wt[w] = __shfl_sync(0xffffffffu, wl[w], row);
+      const float inv = __shfl_sync(0xffffffffu, inv_l, row);
+      const float lse_nat = __shfl_sync(0xffffffffu, lse_l, row);
+      float2 vals[D / 64];
 #pragma unroll
-        for (int w = 0; w < C::NUM_CW; ++w) a = fmaf(wt[w], co[(w * C::TR + row) * C::CROW + d0 + i], a);
-        vals[i] = a * inv;
+      for (int k = 0; k < D / 64; ++k) {
+        float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < C::NUM_CW; ++w) {
+          const float2 v = *reinterpret_cast<const float2 *>(co + (w * C::TR + row) * C::CROW + 2 * lane + 64 * k);
+          a.x = fmaf(wt[w], v.x, a.x);
+          a.y = fmaf(wt[w], v.y, a.y);
+        }
+        vals[k] = make_float2(a.x * inv, a.y * inv);
       }
-      if (rg < p.R) write_row_outputs<C>(p, direct_e, b_e, h_e, s_e, rg, d0, vals, DPT, lse_nat, d0 == 0);
+      if (rg < p.R) write_row_pairs<C>(p, direct_e, b_e, h_e, s_e, rg, lane, vals, lse_nat);
+    };
+    if constexpr (C::QUANT) {  // (unrolled rows cost the quantised kernels registers in their main loop)
+#pragma unroll 1
+      for (int i = 0; i < C::TR / C::NUM_CW; ++i) combine_row(i);
+    } else {
+#pragma unroll
+      for (int i = 0; i < C::TR / C::NUM_CW; ++i) combine_row(i);
     }
     if constexpr (!FUSED) {
       if (p.counters && !direct_e) {
