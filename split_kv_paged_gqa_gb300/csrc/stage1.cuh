@@ -1194,10 +1194,8 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
   if constexpr (DEEP) {
     if (warp == C::NUM_CW) {
       if (p.balanced) {
-        const int cp = balanced_chunk_pages(
-            batch_pages<true>(p.seqlens, p.sl_s, p.batch, cap, p.log2_page, lane), p.batch, p.num_splits);
-        const SplitUnit su = locate_unit<true>(p.seqlens, p.sl_s, p.batch, cap, p.log2_page, cp, p.s_cap,
-                                               p.chunk_min, u, lane);
+        const SplitUnit su = locate_balanced<true>(p.seqlens, p.sl_s, p.batch, cap, p.log2_page, p.num_splits,
+                                                   p.s_cap, p.chunk_min, u, lane);
         hint_b = su.b;
         hint_s = su.s;
         hint_S = su.sb;
@@ -1215,22 +1213,8 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
   // on the resources their last wave uses.
   if constexpr (DEEP) griddep_launch_dependents();
 
-  if (p.balanced) {  // every warp locates the unit (same loads, same answer)
-    const int cp = balanced_chunk_pages(batch_pages<false>(p.seqlens, p.sl_s, p.batch, cap, p.log2_page, lane),
-                                        p.batch, p.num_splits);
-    const SplitUnit su =
-        locate_unit<false>(p.seqlens, p.sl_s, p.batch, cap, p.log2_page, cp, p.s_cap, p.chunk_min, u, lane);
-    if (su.b < 0) {  // past the batch's last split
-      if constexpr (!DEEP) griddep_launch_dependents();
-      return;
-    }
-    b = su.b;
-    s = su.s;
-    S_req = su.sb;
-  }
-
   // The deep producer loads its first page ids now, at the hinted split range,
-  // in the same round trip as the length; they are used only if the length
+  // in the same round trip as the lengths; they are used only if the length
   // read after the wait equals the hint (then the range is the same).
   int pn0 = 0, pn1 = 0;
   if constexpr (DEEP) {
@@ -1245,6 +1229,20 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
         pn1 = lane + 32 < np ? ld_cg(pt + first + 32 + lane) : 0;
       }
     }
+  }
+
+  int L_bal = 0;  // balanced: the located request's stored length
+  if (p.balanced) {  // every warp locates the unit (same loads, same answer)
+    const SplitUnit su = locate_balanced<false>(p.seqlens, p.sl_s, p.batch, cap, p.log2_page, p.num_splits,
+                                                p.s_cap, p.chunk_min, u, lane);
+    if (su.b < 0) {  // past the batch's last split
+      if constexpr (!DEEP) griddep_launch_dependents();
+      return;
+    }
+    b = su.b;
+    s = su.s;
+    S_req = su.sb;
+    L_bal = su.L;
   }
 
   // Consumers issue their query-tile loads now, so their latency overlaps the
@@ -1269,8 +1267,9 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
   const int P = p.page_size;
 
   // ---- split range from cache_seqlens (on the device; no host metadata)
-  // (the deep variant read these words before the wait: take them from L2)
-  int L = DEEP ? ld_cg(p.seqlens + b * p.sl_s) : p.seqlens[b * p.sl_s];
+  // (the balanced map read it already; the deep variant read these words
+  // before the wait: take them from L2)
+  int L = p.balanced ? L_bal : (DEEP ? ld_cg(p.seqlens + b * p.sl_s) : p.seqlens[b * p.sl_s]);
   if (L < 0 || L > cap) {
     if (threadIdx.x == 0) atomicOr(p.status, FD_DEVSTAT_SEQLEN_OVERFLOW);
     L = L < 0 ? 0 : cap;

@@ -396,11 +396,10 @@ __global__ void __launch_bounds__(TcCfg<KIND>::THREADS, 1)
   __syncthreads();
   griddep_wait();  // inputs written by the previous kernel are visible from here on
 
+  int L_bal = 0;
   if (p.balanced) {
-    const int cp = balanced_chunk_pages(batch_pages<false>(p.seqlens, p.sl_s, p.batch, cap, p.log2_page, lane),
-                                        p.batch, p.num_splits);
-    const SplitUnit su =
-        locate_unit<false>(p.seqlens, p.sl_s, p.batch, cap, p.log2_page, cp, p.s_cap, p.chunk_min, u, lane);
+    const SplitUnit su = locate_balanced<false>(p.seqlens, p.sl_s, p.batch, cap, p.log2_page, p.num_splits,
+                                                p.s_cap, p.chunk_min, u, lane);
     if (su.b < 0) {
       griddep_launch_dependents();
       return;
@@ -408,8 +407,9 @@ __global__ void __launch_bounds__(TcCfg<KIND>::THREADS, 1)
     b = su.b;
     s = su.s;
     S_req = su.sb;
+    L_bal = su.L;
   }
-  int L = p.seqlens[b * p.sl_s];
+  int L = p.balanced ? L_bal : p.seqlens[b * p.sl_s];
   if (L < 0 || L > cap) {
     if (threadIdx.x == 0) atomicOr(p.status, FD_DEVSTAT_SEQLEN_OVERFLOW);
     L = L < 0 ? 0 : cap;
