@@ -1604,25 +1604,25 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
       const int c = lane & 3;
       float *w0 = co + (warp * 16 + g) * C::CROW;
       float *w1 = co + (warp * 16 + g + 8) * C::CROW;
+      // rows g and g + 8 of the tile; the second half only if it holds queries
+      auto put_rows = [&](float *w, int e) {
 #pragma unroll
-      for (int j = 0; j < D / 8; ++j) {
-        if constexpr (KIND == KV_I4) {  // n-tile j = 4 gi + q, column n holds channel 32 gi + 4 n + q
-          const int ch = 32 * (j / 4) + 8 * c + (j % 4);
-          w0[ch] = o[j][0];
-          w0[ch + 4] = o[j][1];
-          w1[ch] = o[j][2];
-          w1[ch + 4] = o[j][3];
-        } else if constexpr (C::QUANT) {  // int8: n-tile j = 2 s + e, column n holds channel 16 s + 2 n + e
-          const int ch = 16 * (j / 2) + 4 * c + (j % 2);
-          w0[ch] = o[j][0];
-          w0[ch + 2] = o[j][1];
-          w1[ch] = o[j][2];
-          w1[ch + 2] = o[j][3];
-        } else {
-          *reinterpret_cast<float2 *>(w0 + j * 8 + 2 * c) = make_float2(o[j][0], o[j][1]);
-          *reinterpret_cast<float2 *>(w1 + j * 8 + 2 * c) = make_float2(o[j][2], o[j][3]);
+        for (int j = 0; j < D / 8; ++j) {
+          if constexpr (KIND == KV_I4) {  // n-tile j = 4 gi + q, column n holds channel 32 gi + 4 n + q
+            const int ch = 32 * (j / 4) + 8 * c + (j % 4);
+            w[ch] = o[j][e];
+            w[ch + 4] = o[j][e + 1];
+          } else if constexpr (C::QUANT) {  // int8: n-tile j = 2 s + e, column n holds channel 16 s + 2 n + e
+            const int ch = 16 * (j / 2) + 4 * c + (j % 2);
+            w[ch] = o[j][e];
+            w[ch + 2] = o[j][e + 1];
+          } else {
+            *reinterpret_cast<float2 *>(w + j * 8 + 2 * c) = make_float2(o[j][e], o[j][e + 1]);
+          }
         }
-      }
+      };
+      put_rows(w0, 0);
+      if (rt * 16 + 8 < p.R) put_rows(w1, 2);
       if (c == 0) {
         cm[warp * 16 + g] = m[0];
         cm[warp * 16 + g + 8] = m[1];
@@ -1659,6 +1659,7 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
     auto combine_row = [&](int i) {
       const int row = warp + i * C::NUM_CW;
       const int rg = rt * 16 + row;
+      if (rg >= p.R) return;  // a padding row of the tile (its partials were not written)
       float wt[C::NUM_CW];
 #pragma unroll
       for (int w = 0; w < C::NUM_CW; ++w) wt[w] = __shfl_sync(0xffffffffu, wl[w], row);
@@ -1676,7 +1677,7 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
         }
         vals[k] = make_float2(a.x * inv, a.y * inv);
       }
-      if (rg < p.R) write_row_pairs<C>(p, direct_e, b_e, h_e, s_e, rg, lane, vals, lse_nat);
+      write_row_pairs<C>(p, direct_e, b_e, h_e, s_e, rg, lane, vals, lse_nat);
     };
     if constexpr (C::QUANT) {  // (unrolled rows cost the quantised kernels registers in their main loop)
 #pragma unroll 1
