@@ -1679,13 +1679,8 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
       }
       write_row_pairs<C>(p, direct_e, b_e, h_e, s_e, rg, lane, vals, lse_nat);
     };
-    if constexpr (C::QUANT) {  // (unrolled rows cost the quantised kernels registers in their main loop)
 #pragma unroll 1
-      for (int i = 0; i < C::TR / C::NUM_CW; ++i) combine_row(i);
-    } else {
-#pragma unroll
-      for (int i = 0; i < C::TR / C::NUM_CW; ++i) combine_row(i);
-    }
+    for (int i = 0; i < C::TR / C::NUM_CW; ++i) combine_row(i);
     if constexpr (!FUSED) {
       if (p.counters && !direct_e) {
         // Fused merge: publish this split's partials, count it, and let the
