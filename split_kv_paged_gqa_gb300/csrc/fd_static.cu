@@ -14,7 +14,6 @@
 //  * it reads the device's SM count and compute capability (attribute
 //    queries, which allocate nothing);
 //  * it raises the kernels' shared-memory limit.
-// Make that first call before any stream capture.
 //
 // This path always merges splits with the stage-2 kernel: the array holds
 // only the fp32 split partials and their LSEs.
