@@ -239,8 +239,7 @@ FD_API fd_status fd_decode_paged(const fd_tensor *q, const fd_tensor *k_cache, c
  *
  * The first call on a device does a one-time set-up: it looks up the array's
  * address, reads the device's SM count and compute capability, and raises
- * the kernels' shared-memory limit. Make that first call before any stream
- * capture.
+ * the kernels' shared-memory limit.
  *
  * All calls share the array. Calls that overlap on the GPU race on it, so
  * serialise them on one stream. Kernel status bits go to an internal word
