@@ -24,7 +24,11 @@
 
 namespace fd {
 
-constexpr int kS2Warps = 8;
+// Rows per CTA: small CTAs spread a short merge over more SMs. A batch-1 ×
+// 32K call (64 rows of 16 partials) measured 24.0 us with 8-warp CTAs, 23.75
+// with 4, 23.4 with 2 and 23.45 with 1 (same process; batch 64 and the
+// mixed-length batch unchanged within 0.2 %).
+constexpr int kS2Warps = 2;
 
 template <int D>
 __global__ void __launch_bounds__(kS2Warps * 32) fd_stage2_kernel(const __grid_constant__ Stage2Params p) {
