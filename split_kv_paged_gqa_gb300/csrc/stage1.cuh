@@ -1026,9 +1026,8 @@ __device__ __forceinline__ void write_row_pairs(const Stage1Params &p, bool fuse
 // nv non-empty split partials (o_s, lse_s) combine as
 //   M = max_s lse_s, w_s = exp(lse_s - M), out = sum w_s o_s / sum w_s,
 //   lse = M + ln(sum w_s)
-// (the stage-2 merge). One warp per row, lanes over the D columns, the LSEs
-// and up to 16 partials in flight together; partials written by other CTAs
-// are read through L2.
+// (the stage-2 merge). One warp per row, lanes over the D columns, eight
+// partial loads in flight; partials written by other CTAs are read through L2.
 template <class C>
 __device__ __forceinline__ void merge_tile(const Stage1Params &p, int b, int h, int rt, int nv, int warp,
                                            int nwarps, int lane) {
@@ -1038,32 +1037,6 @@ __device__ __forceinline__ void merge_tile(const Stage1Params &p, int b, int h, 
     const int rg = rt * 16 + r;
     const int t = rg / p.G, hq = h * p.G + (rg - t * p.G);
     const int64_t base = ((static_cast<int64_t>(b) * p.Tq + t) * p.Hq + hq) * p.s_cap;
-    // the LSEs and the first 16 partials are requested together (one round
-    // trip for up to 16 splits; a split with no visible key left a finite 0)
-    const float *op = p.o_part + base * D + lane * VPL;
-    constexpr int U = 16;
-    auto load_group = [&](int s0, float (&v)[U][VPL]) {
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) v[u][i] = 0.f;
-        if (s0 + u < nv) {
-          if constexpr (VPL == 4) {
-            const float4 x = __ldcg(reinterpret_cast<const float4 *>(op + (s0 + u) * D));
-            v[u][0] = x.x;
-            v[u][1] = x.y;
-            v[u][2] = x.z;
-            v[u][3] = x.w;
-          } else {
-            const float2 x = __ldcg(reinterpret_cast<const float2 *>(op + (s0 + u) * D));
-            v[u][0] = x.x;
-            v[u][1] = x.y;
-          }
-        }
-      }
-    };
-    float v[U][VPL];
-    load_group(0, v);
     const float l0 = lane < nv ? __ldcg(p.lse_part + base + lane) : -INFINITY;
     const float l1 = lane + 32 < nv ? __ldcg(p.lse_part + base + lane + 32) : -INFINITY;
     float M = fmaxf(l0, l1);
@@ -1074,20 +1047,37 @@ __device__ __forceinline__ void merge_tile(const Stage1Params &p, int b, int h, 
     float Z = w0 + w1;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
-    float acc[VPL];
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const float *op = p.o_part + base * D + lane * VPL;
+    for (int s0 = 0; s0 < nv; s0 += 8) {
+      float w[8];
+      float v[8][VPL];
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) acc[i] = 0.f;
-    for (int s0 = 0; s0 < nv; s0 += U) {
-      if (s0 > 0) load_group(s0, v);  // more than 16 splits
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
+      for (int u = 0; u < 8; ++u) {
         const int sp = s0 + u;
         const float wa = __shfl_sync(0xffffffffu, w0, sp & 31);
         const float wb = __shfl_sync(0xffffffffu, w1, sp & 31);
-        const float w = sp < nv ? (sp < 32 ? wa : wb) : 0.f;
+        w[u] = sp < nv ? (sp < 32 ? wa : wb) : 0.f;
 #pragma unroll
-        for (int i = 0; i < VPL; ++i) acc[i] = fmaf(w, v[u][i], acc[i]);
+        for (int i = 0; i < VPL; ++i) v[u][i] = 0.f;
+        if (w[u] > 0.f) {
+          if constexpr (VPL == 4) {
+            const float4 x = __ldcg(reinterpret_cast<const float4 *>(op + sp * D));
+            v[u][0] = x.x;
+            v[u][1] = x.y;
+            v[u][2] = x.z;
+            v[u][3] = x.w;
+          } else {
+            const float2 x = __ldcg(reinterpret_cast<const float2 *>(op + sp * D));
+            v[u][0] = x.x;
+            v[u][1] = x.y;
+          }
+        }
       }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) acc[i] = fmaf(w[u], v[u][i], acc[i]);
     }
     const float inv = Z > 0.f ? 1.f / Z : 0.f;
     const int64_t ob = b * p.o_sb + t * p.o_st + hq * p.o_sh + lane * VPL;
