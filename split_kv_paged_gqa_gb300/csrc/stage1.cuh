@@ -356,7 +356,7 @@ template <class C, int KIND>
 __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *vt, const float *ksc,
                                              const float *vsc, int row0,
                                              const uint32_t (&qa)[C::D / 16][4],
-                                             const float (&qc)[2][C::NG], const float (&rs)[2],
+                                             const float (&qc)[2][C::NG], const float *qcs, const float (&rs)[2],
                                              float (&o)[C::NT][4], float (&ra)[C::NR][4], uint32_t tm_o,
                                              float (&m)[2], float (&l)[2], int tok_row0, int c1, int lim0,
                                              int lim1, int lane) {
@@ -371,6 +371,9 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
   // ---- S = Q K^T in fp16 with biased K codes. Each 16-byte chunk of a K row
   // is one scale group for int4 (32 channels); its accumulator is folded into
   // the scores as soon as its products are done: sv = sum_g ks_g (acc_g - c_g).
+  // int4 reads the constants c_g of its rows g, g + 8 from shared memory
+  // (qcs: prepare_q_rows' table at row g; row g + 8 at + 8 NG) rather than
+  // holding them in registers through the block.
   // The sub-blocks' products are independent: their MMA chains interleave.
   float sv[KB][2][4];
 #pragma unroll
@@ -411,7 +414,7 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[kb][nt][e] = -qc[e >> 1][ch];
+            for (int e = 0; e < 4; ++e) acc[kb][nt][e] = -qcs[(e >> 1) * 8 * NG + ch];
             // raw nibble k (= code & 15) is channel 32ch + 8c + k; masking it
             // and XOR-ing in 8 and the exponent of 1024 is one LOP3 per pair
             const uint32_t x = r[kb][nt * 2 + hh];
@@ -1525,8 +1528,9 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
               qf[ks][2] = v.z;
               qf[ks][3] = v.w;
             }
-            warp_block_q<C, KIND>(kt, vt, ksc, vsc, row0, qf, qc, rs, o, ra, tm_o, m, l, tok_row0, c1,
-                                  lim[0], lim[1], lane);
+            warp_block_q<C, KIND>(kt, vt, ksc, vsc, row0, qf, qc,
+                                  reinterpret_cast<const float *>(smem + C::OFF_QI) + 16 + (lane >> 2) * C::NG, rs,
+                                  o, ra, tm_o, m, l, tok_row0, c1, lim[0], lim[1], lane);
           }
         } else {
           if (tok_row0 + 16 > c1) {  // zero V rows past the split end before PV
