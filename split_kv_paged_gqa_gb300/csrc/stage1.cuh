@@ -356,7 +356,8 @@ template <class C, int KIND>
 __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *vt, const float *ksc,
                                              const float *vsc, int row0,
                                              const uint32_t (&qa)[C::D / 16][4],
-                                             const float (&qc)[2][C::NG], const float *qcs, const float (&rs)[2],
+                                             const uint4 *qa_s, const float (&qc)[2][C::NG], const float *qcs,
+                                             const float (&rs)[2],
                                              float (&o)[C::NT][4], float (&ra)[C::NR][4], uint32_t tm_o,
                                              float (&m)[2], float (&l)[2], int tok_row0, int c1, int lim0,
                                              int lim1, int lane) {
@@ -409,6 +410,9 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
           }
       } else {
         float acc[KB][2][4];  // this group's products, starting at -bias
+        // the group's two Q fragments (k-steps 2 ch, 2 ch + 1), from shared memory
+        const uint4 va = qa_s[(2 * ch) * 32 + lane], vb = qa_s[(2 * ch + 1) * 32 + lane];
+        const uint32_t qlo[4] = {va.x, va.y, va.z, va.w}, qhi[4] = {vb.x, vb.y, vb.z, vb.w};
 #pragma unroll
         for (int kb = 0; kb < KB; ++kb)
 #pragma unroll
@@ -419,8 +423,8 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
             // and XOR-ing in 8 and the exponent of 1024 is one LOP3 per pair
             const uint32_t x = r[kb][nt * 2 + hh];
             const uint32_t y = x >> 8;
-            mma_f16_16816(acc[kb][nt], qa[2 * ch], nib_lo_f16_biased(x, nib_lo), nib_lo_f16_biased(y, nib_lo));
-            mma_f16_16816(acc[kb][nt], qa[2 * ch + 1], nib_hi_f16_biased(x, nib_hi),
+            mma_f16_16816(acc[kb][nt], qlo, nib_lo_f16_biased(x, nib_lo), nib_lo_f16_biased(y, nib_lo));
+            mma_f16_16816(acc[kb][nt], qhi, nib_hi_f16_biased(x, nib_hi),
                           nib_hi_f16_biased(y, nib_hi));
           }
 #pragma unroll
@@ -571,23 +575,6 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
     tmem_wait_st();
 #pragma unroll
     for (int i = 0; i < NT / 8; ++i) tmem_ld32(tm_o + 32 * i, &ot[8 * i][0]);
-    // V-scale pairs per group of the thread's keys (2c, 2c + 1) and
-    // (2c + 8, 2c + 9) of each sub-block
-    uint32_t sp0[KB][NG], sp1[KB][NG];
-#pragma unroll
-    for (int kb = 0; kb < KB; ++kb) {
-      float sk[4][NG];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-#pragma unroll
-        for (int gi = 0; gi < NG; ++gi) sk[i][gi] = vsc[vrows[kb][i] * NG + gi];
-      }
-#pragma unroll
-      for (int gi = 0; gi < NG; ++gi) {
-        sp0[kb][gi] = pack_f16x2(sk[0][gi], sk[1][gi]);
-        sp1[kb][gi] = pack_f16x2(sk[2][gi], sk[3][gi]);
-      }
-    }
     tmem_wait_ld();
     rescale_o(ot);
     // V codes paired by ldmatrix.trans: matrix (keys 8h .. 8h + 7 of the
@@ -598,6 +585,22 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
     const uint32_t vbase = smem_u32(vt);
 #pragma unroll
     for (int kb = 0; kb < KB; ++kb) {
+      // V-scale pairs per group of the thread's keys (2c, 2c + 1) and
+      // (2c + 8, 2c + 9) of this sub-block
+      uint32_t sp0[NG], sp1[NG];
+      {
+        float sk[4][NG];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+          for (int gi = 0; gi < NG; ++gi) sk[i][gi] = vsc[vrows[kb][i] * NG + gi];
+        }
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) {
+          sp0[gi] = pack_f16x2(sk[0][gi], sk[1][gi]);
+          sp1[gi] = pack_f16x2(sk[2][gi], sk[3][gi]);
+        }
+      }
 #pragma unroll
       for (int gp = 0; gp < NG; gp += 2) {  // two groups per ldmatrix.x4
         uint32_t R[4];  // (keys 0-7, gp), (keys 8-15, gp), (keys 0-7, gp + 1), (keys 8-15, gp + 1)
@@ -606,8 +609,8 @@ __device__ __forceinline__ void warp_block_q(const uint8_t *kt, const uint8_t *v
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           const int gi = gp + h2;
-          const uint32_t aw[4] = {hmul2_u32(pa[kb][0], sp0[kb][gi]), hmul2_u32(pa[kb][1], sp0[kb][gi]),
-                                  hmul2_u32(pa[kb][2], sp1[kb][gi]), hmul2_u32(pa[kb][3], sp1[kb][gi])};
+          const uint32_t aw[4] = {hmul2_u32(pa[kb][0], sp0[gi]), hmul2_u32(pa[kb][1], sp0[gi]),
+                                  hmul2_u32(pa[kb][2], sp1[gi]), hmul2_u32(pa[kb][3], sp1[gi])};
           const uint32_t lo = R[2 * h2], hi = R[2 * h2 + 1];
           const uint32_t lo8 = lo >> 8, hi8 = hi >> 8;
           mma_f16_16816(ot[4 * gi + 0], aw, hsub2_u32(nib_lo_f16_biased(lo, nib_lo), 1032.0f),
@@ -1518,17 +1521,19 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
                                    lim[1], lane);
           } else {
             static_assert(C::QA_SMEM, "the 16-row quantised block reads its Q fragments from shared memory");
-            uint32_t qf[D / 16][4];
+            uint32_t qf[D / 16][4];  // int8: loaded here; int4 loads them group by group
             const uint4 *qa_s = reinterpret_cast<const uint4 *>(smem + C::OFF_QA);
+            if constexpr (KIND != KV_I4) {
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-              const uint4 v = qa_s[ks * 32 + lane];
-              qf[ks][0] = v.x;
-              qf[ks][1] = v.y;
-              qf[ks][2] = v.z;
-              qf[ks][3] = v.w;
+              for (int ks = 0; ks < D / 16; ++ks) {
+                const uint4 v = qa_s[ks * 32 + lane];
+                qf[ks][0] = v.x;
+                qf[ks][1] = v.y;
+                qf[ks][2] = v.z;
+                qf[ks][3] = v.w;
+              }
             }
-            warp_block_q<C, KIND>(kt, vt, ksc, vsc, row0, qf, qc,
+            warp_block_q<C, KIND>(kt, vt, ksc, vsc, row0, qf, qa_s, qc,
                                   reinterpret_cast<const float *>(smem + C::OFF_QI) + 16 + (lane >> 2) * C::NG, rs,
                                   o, ra, tm_o, m, l, tok_row0, c1, lim[0], lim[1], lane);
           }
