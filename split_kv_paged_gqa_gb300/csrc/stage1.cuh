@@ -173,8 +173,8 @@ __device__ __forceinline__ uint32_t nib_hi_f16_biased(uint32_t t, uint32_t c) {
 // O = 2^24 O_raw - 128 R (remove_v_bias). Products and R are exact in fp32
 // before accumulation, and for codes of either sign the bias term is of the
 // order of the result, so the cancellation costs a bit or two of the sum.
-// (int4 keeps exact biased fp16 codes: its sixteen bias sums per block,
-// one per scale group, cost more registers than the subtractions they save.)
+// (int4 keeps exact biased fp16 codes: with its per-group V scales the bias
+// sums it would need measured no faster.)
 constexpr uint32_t kU8Sub = 0x00800080u;     // bytes 0 and 2: u = code ^ 0x80
 constexpr uint32_t kOnesF16 = 0x3C003C00u;   // f16x2 (1, 1)
 __device__ __forceinline__ uint32_t i8pair_to_f16_sub(uint32_t t, uint32_t c) { return and_xor<0x00FF00FFu>(t, c); }
@@ -1643,8 +1643,9 @@ __global__ void __launch_bounds__(S1Cfg<KIND, D, DEEP, NARROW>::THREADS, S1Cfg<K
     // Lane r of every consumer warp forms row r's weights (lanes past the
     // tile's rows repeat them); then each warp combines whole rows, lane l
     // taking the column pairs 2l + 64k, so every read of a partial row is 256
-    // consecutive bytes (conflict-free) and every store coalesced. The rows
-    // of a warp are unrolled so their loads overlap.
+    // consecutive bytes (conflict-free) and every store coalesced. (Unrolling
+    // a warp's rows measured the same for bf16 and cost the quantised
+    // kernels registers in their main loop.)
     static_assert(C::TR % C::NUM_CW == 0, "rows per consumer warp");
     float wl[C::NUM_CW], inv_l, lse_l;
     {
